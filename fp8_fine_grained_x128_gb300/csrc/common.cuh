@@ -1,0 +1,311 @@
+// common.cuh -- device helpers shared by the sm_103a kernels of the fine-grained
+// FP8 Linear library: FP8 conversion, the per-element IEEE division x / s,
+// BF16 unpacking, the device status word, and the inline-PTX wrappers for
+// mbarriers, TMA and the tcgen05 tensor-core / tensor-memory instructions.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp8fg.h"
+
+#ifndef __CUDA_ARCH__
+#define FP8FG_HOST_ONLY 1
+#endif
+
+namespace fp8fg {
+
+// Largest finite magnitude of the two formats ([FP8-LM] "FP8 data formats";
+// E4M3 spans [-448, 448] per the FP8-RL article).
+__host__ __device__ constexpr float fmax_of(int fmt) { return fmt == FP8_E5M2 ? 57344.0f : 448.0f; }
+
+// Default bound for every spin-wait on the device (nanoseconds).
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
+
+// ------------------------------------------------------------------ status
+
+// Records the first error seen by any thread in the device status word.
+__device__ __forceinline__ void set_status(int *status, int code)
+{
+    if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ------------------------------------------------------------------ numbers
+
+// The two BF16 halves of a 32-bit word, widened exactly to FP32.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// |x| of both BF16 halves, as bit patterns (unsigned order = magnitude order
+// for everything but NaN, which sorts above +Inf and is caught separately).
+__device__ __forceinline__ uint32_t bf16x2_abs(uint32_t w) { return w & 0x7FFF7FFFu; }
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
+__device__ __forceinline__ uint32_t halfmax(uint32_t w) { return max(w & 0xFFFFu, w >> 16); }
+
+// Scale of a group from its amax (as BF16 magnitude bits): s = fp32(amax / fmax),
+// 1 for an all-zero group ([FP8-LM] "Tensor scaling"; s = amax / fmax).
+__device__ __forceinline__ float scale_from_amax_bits(uint32_t amax_bf16_bits, int fmt)
+{
+    float amax = __uint_as_float(amax_bf16_bits << 16);
+    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, fmax_of(fmt));
+}
+
+// Division x / s rounded to nearest binary32, computed from r = RN(1/s) with
+// Markstein's correction (P. Markstein, "Computation of elementary functions
+// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
+// r within half an ulp of 1/s and q0 within one ulp of x/s, the remainder
+// e = x - q0*s is exact under FMA and RN(q0 + e*r) is the correctly rounded
+// quotient.  Valid while s and 1/s are normal and nothing overflows; callers
+// use it only when 2^-125 <= s <= 2^125 and fall back to __fdiv_rn otherwise.
+// The sign is forced from x so that -0 / s = -0 like the IEEE division.
+struct Divider {
+    float s, r;
+    bool fast;
+    __device__ __forceinline__ explicit Divider(float s_) : s(s_)
+    {
+        fast = (s_ >= 0x1p-125f) && (s_ <= 0x1p125f);
+        r = fast ? __frcp_rn(s_) : 0.0f;
+    }
+    __device__ __forceinline__ float operator()(float x) const
+    {
+        if (fast) {
+            float q0 = __fmul_rn(x, r);
+            float e = __fmaf_rn(-q0, s, x);
+            float q = __fmaf_rn(e, r, q0);
+            return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
+        }
+        return __fdiv_rn(x, s);
+    }
+};
+
+// FP8 encode of two binary32 values (round to nearest even, saturating to
+// +-fmax): the byte of `lo` lands in bits 0..7, `hi` in bits 8..15.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt2(float lo, float hi)
+{
+    uint16_t r;
+    if (FMT == FP8_E5M2)
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r;
+}
+
+// Quantize 8 BF16 values (a uint4) with one divider; returns 8 codes in a uint2.
+template <int FMT>
+__device__ __forceinline__ uint2 quant8(uint4 v, const Divider &d)
+{
+    uint2 out;
+    out.x = cvt2<FMT>(d(bf16_lo(v.x)), d(bf16_hi(v.x))) | (cvt2<FMT>(d(bf16_lo(v.y)), d(bf16_hi(v.y))) << 16);
+    out.y = cvt2<FMT>(d(bf16_lo(v.z)), d(bf16_hi(v.z))) | (cvt2<FMT>(d(bf16_lo(v.w)), d(bf16_hi(v.w))) << 16);
+    return out;
+}
+
+__device__ __forceinline__ uint32_t absmax8(uint4 v)
+{
+    uint32_t m = bf16x2_absmax(bf16x2_abs(v.x), bf16x2_abs(v.y));
+    m = bf16x2_absmax(m, bf16x2_abs(v.z));
+    m = bf16x2_absmax(m, bf16x2_abs(v.w));
+    return halfmax(m);
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// --------------------------------------------------------- shared / barriers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits until the phase with parity `parity` of `bar` has completed.  Gives
+// up (returns false) after `timeout_ns`, or early when *abort becomes
+// nonzero; it never spins without bound.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                  uint64_t timeout_ns = kWaitTimeoutNs)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0u) {
+            if (abort && *abort) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------- TMA
+
+// 2-D tiled bulk tensor load global -> shared, completion counted in bytes
+// on `bar`.  x is the innermost coordinate (elements of the map's type).
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int x, int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D(tmem) (+)= A(smem desc) x B(smem desc)^T, FP8 operands, FP32 accumulator.
+__device__ __forceinline__ void tc_mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation issued so far by this
+// thread has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 32 columns of 32-bit TMEM words: thread i of the warp receives
+// lane (base lane + i), columns [col, col + 32).
+__device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// 32 lanes x 16 columns (16 registers per thread).
+__device__ __forceinline__ void tc_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile stored in the
+// 128-byte swizzle layout that a TMA load with CU_TENSOR_MAP_SWIZZLE_128B
+// writes: rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte
+// offset), leading byte offset unused (1), descriptor version 1, swizzle mode
+// 2 = 128B.  The tile base must be 1024-byte aligned; advancing along K
+// inside the 128-byte row is done by adding the byte offset to the start.
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1u << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma .kind::f8f6f4 with an FP32
+// accumulator, both operands K-major, dense: D format bits 4-5 (1 = F32),
+// A type bits 7-9 and B type bits 10-12 (0 = E4M3, 1 = E5M2), N/8 at bits
+// 17-22, M/16 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f8f6f4(int fmtA, int fmtB, int M, int N)
+{
+    return (1u << 4) | ((uint32_t)(fmtA == FP8_E5M2 ? 1 : 0) << 7) | ((uint32_t)(fmtB == FP8_E5M2 ? 1 : 0) << 10) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+}  // namespace fp8fg

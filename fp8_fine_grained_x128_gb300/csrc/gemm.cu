@@ -1,0 +1,499 @@
+// gemm.cu -- block-scaled / per-tensor / grouped FP8 GEMM on the sm_103a
+// tensor cores (tcgen05), D = A . B^T with A [M][K] and B [N][K] K-major.
+//
+// Method (Ling 2.0 FP8 pretraining blog, "Where does the error come from?":
+// an FP8 GEMM whose accumulator is kept in FP32 adds negligible error;
+// "Fine-grained quantization": one scale per 1x128 activation tile / 128x128
+// weight block): every 128-deep K chunk is multiplied on the tensor cores into
+// its own FP32 accumulator in tensor memory, then promoted into an FP32
+// running sum in registers with the chunk's two scales:
+//     acc[m][n] += sA(m, kb) * sB(n, kb) * P_kb[m][n].
+// For per-tensor scales (the coarse delayed-scaling recipe) the whole K is
+// accumulated in tensor memory and sA*sB applied once.
+//
+// Structure (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: A tile 128x128 B and B tile BNx128 B per stage,
+//               128-byte swizzle, STAGES-deep ring of shared-memory stages.
+//   warp 1      owns the tensor memory (2 accumulators of BN columns) and
+//               issues tcgen05.mma kind::f8f6f4 (M=128, N=BN, K=32, 4 per
+//               chunk) from one thread; tcgen05.commit frees the stage and
+//               publishes the accumulator.
+//   warps 2..9  epilogue: tcgen05.ld 32x32b of their lane quarter and column
+//               half, FP32 promotion with the scales, BF16/FP32 stores.  The
+//               two accumulators alternate per chunk, so the tensor cores fill
+//               one while the epilogue drains the other.
+// Every mbarrier wait is bounded (about 1 s): on a timeout the CTA records
+// FP8_ERR_TIMEOUT, tells the other roles through a shared flag, waits for
+// its own copies and MMAs in flight (bounded again), frees the tensor memory
+// and returns.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8fg {
+
+constexpr int kGemmThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kMaxGroups = 1024;
+
+struct GemmArgs {
+    int M, N, K;          // M = rows of A (the capacity for the grouped GEMM)
+    const float *sA;      // scale arrays, layouts per granularity
+    int64_t ldsA;
+    int granA;
+    const float *sB;
+    int64_t ldsB;
+    int64_t sB_group_stride;
+    void *D;
+    int64_t ldD;
+    int out_f32;
+    const int32_t *offsets;
+    int G;
+    int *status;
+};
+
+enum { SB_BLOCK = 0, SB_ROW = 1 };
+
+template <int BN, int STAGES>
+struct GemmSmem {
+    static constexpr int kA = 128 * 128;
+    static constexpr int kB = BN * 128;
+    static constexpr int kStage = kA + kB;
+    static constexpr int kBars = 2 * STAGES + 2 + 2 + 1;
+    static constexpr int kCtrl = kBars * 8 + 16;
+    static constexpr int kBytes = 1024 + STAGES * kStage + kCtrl + 4 * (kMaxGroups + 1);
+    static constexpr int kTmemCols = 2 * BN;
+};
+
+__device__ __forceinline__ void tile_coords_raster(int tile, int num_mt, int num_nt, int &mt, int &nt)
+{
+    constexpr int GM = 16;   // 16 M-tiles share each B tile while it is hot in L2
+    const int group = tile / (GM * num_nt);
+    const int first = group * GM;
+    const int gm = min(GM, num_mt - first);
+    const int local = tile - group * GM * num_nt;
+    mt = first + local % gm;
+    nt = local / gm;
+}
+
+// Largest g with off[g] <= row (skips empty groups).
+__device__ __forceinline__ int group_of_row(const int32_t *off, int G, int row)
+{
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= row) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              int *status)
+{
+    if (mbar_wait_bounded(bar, parity, abort_flag)) return true;
+    if (!*abort_flag) {
+        *abort_flag = 1;
+        set_status(status, FP8_ERR_TIMEOUT);
+    }
+    return false;
+}
+
+// One warp waits through lane 0; the outcome is broadcast so the warp stays
+// converged for the .sync.aligned tcgen05 instructions that follow.
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                   int *status)
+{
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, abort_flag, status) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <int NCOL>
+__device__ __forceinline__ void store_row(void *D, int64_t ldD, int out_f32, int64_t row, int64_t col0,
+                                          const float (&v)[NCOL])
+{
+    if (out_f32) {
+        float *p = static_cast<float *>(D) + row * ldD + col0;
+#pragma unroll
+        for (int c = 0; c < NCOL; c += 4)
+            *reinterpret_cast<float4 *>(p + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+    } else {
+        uint16_t *p = static_cast<uint16_t *>(D) + row * ldD + col0;
+#pragma unroll
+        for (int c = 0; c < NCOL; c += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(v[c], v[c + 1]);
+            w.y = pack_bf16x2(v[c + 2], v[c + 3]);
+            w.z = pack_bf16x2(v[c + 4], v[c + 5]);
+            w.w = pack_bf16x2(v[c + 6], v[c + 7]);
+            *reinterpret_cast<uint4 *>(p + c) = w;
+        }
+    }
+}
+
+template <int BN, int STAGES, bool PROMOTE, int SBG, bool GROUPED>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, uint32_t idesc,
+           GemmArgs a)
+{
+    using L = GemmSmem<BN, STAGES>;
+    constexpr int HALF = BN / 2;        // columns per epilogue warp
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * L::kStage);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *mma_done = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *bad_offsets = reinterpret_cast<int *>(tmem_slot + 2);
+    int32_t *sh_off = reinterpret_cast<int32_t *>(smem + STAGES * L::kStage + L::kCtrl);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], kEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        *bad_offsets = 0;
+        fence_barrier_init();
+    }
+    if (GROUPED) {
+        for (int i = threadIdx.x; i <= a.G; i += blockDim.x) sh_off[i] = a.offsets[i];
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, L::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (GROUPED && threadIdx.x == 0) {
+        bool ok = sh_off[0] == 0;
+        for (int i = 0; i < a.G; ++i) ok = ok && (sh_off[i] <= sh_off[i + 1]) && ((sh_off[i + 1] & 127) == 0);
+        ok = ok && sh_off[a.G] <= a.M;
+        if (!ok) {
+            *bad_offsets = 1;
+            set_status(a.status, FP8_ERR_INVALID_ARG);
+        }
+    }
+    if (GROUPED) __syncthreads();
+
+    const int num_nt = a.N / BN;
+    const int num_mt = GROUPED ? (*bad_offsets ? 0 : sh_off[a.G] / 128) : a.M / 128;
+    const int ntiles = num_mt * num_nt;
+    const int nk = a.K / 128;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                int mt, nt;
+                if (GROUPED) { mt = tile / num_nt; nt = tile - mt * num_nt; }
+                else tile_coords_raster(tile, num_mt, num_nt, mt, nt);
+                const int brow = nt * BN + (GROUPED ? group_of_row(sh_off, a.G, mt * 128) * a.N : 0);
+                for (int kb = 0; kb < nk; ++kb) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!wait_or_abort(&empty[s], ph ^ 1, abort_flag, a.status)) { ok = false; break; }
+                    uint8_t *st = smem + s * L::kStage;
+                    mbar_arrive_expect_tx(&full[s], L::kStage);
+                    tma_load_2d(st, &tmA, &full[s], kb * 128, mt * 128);
+                    tma_load_2d(st + L::kA, &tmB, &full[s], kb * 128, brow);
+                    ++it;
+                }
+            }
+            // copies still in flight land before the CTA may exit
+            const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0;
+            for (uint32_t j = first; j < it; ++j) mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1, nullptr);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, cc = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                uint32_t buf = cc & 1;
+                if (!PROMOTE) {
+                    if (!wait_or_abort(&tempty[buf], ((cc >> 1) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+                    tc_fence_after();
+                }
+                for (int kb = 0; kb < nk; ++kb) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (PROMOTE) {
+                        buf = cc & 1;
+                        if (!wait_or_abort(&tempty[buf], ((cc >> 1) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+                    }
+                    if (!wait_or_abort(&full[s], ph, abort_flag, a.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(smem + s * L::kStage));
+                    const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * L::kStage + L::kA));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        // advance 32 bytes (K = 32 FP8) inside the 128-byte swizzled row
+                        tc_mma_f8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+                                      (k > 0 || (!PROMOTE && kb > 0)) ? 1u : 0u);
+                    }
+                    tc_commit(&empty[s]);
+                    if (PROMOTE) {
+                        tc_commit(&tfull[buf]);
+                        ++cc;
+                    }
+                    ++it;
+                }
+                if (!ok) break;
+                if (!PROMOTE) {
+                    tc_commit(&tfull[buf]);
+                    ++cc;
+                }
+            }
+            // every MMA issued by this thread completes before the CTA frees TMEM
+            tc_commit(mma_done);
+            mbar_wait_bounded(mma_done, 0, nullptr);
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int ew = warp - 2;
+        const int lg = warp & 3;             // TMEM lane quarter this warp may access
+        const int colbase = (ew >> 2) * HALF;
+        const int row = lg * 32 + lane;
+        const uint32_t tm_lane = tmem_base + ((uint32_t)(lg * 32) << 16);
+        uint32_t cc = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            int mt, nt;
+            if (GROUPED) { mt = tile / num_nt; nt = tile - mt * num_nt; }
+            else tile_coords_raster(tile, num_mt, num_nt, mt, nt);
+            const int m0 = mt * 128, n0 = nt * BN;
+            const float *sB = a.sB;
+            if (GROUPED) sB += (int64_t)group_of_row(sh_off, a.G, m0) * a.sB_group_stride;
+            if (PROMOTE) {
+                float acc[HALF];
+#pragma unroll
+                for (int i = 0; i < HALF; ++i) acc[i] = 0.0f;
+                for (int kb = 0; kb < nk; ++kb) {
+                    const uint32_t buf = cc & 1;
+                    const float sa = a.granA == FP8_GRAN_1x128 ? a.sA[(int64_t)kb * a.ldsA + m0 + row]
+                                                              : a.sA[(int64_t)(m0 >> 7) * a.ldsA + kb];
+                    float sb = 0.0f;
+                    if (SBG == SB_BLOCK) sb = sB[(int64_t)((n0 + colbase) >> 7) * a.ldsB + kb];
+                    if (!warp_wait_or_abort(&tfull[buf], (cc >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const float sab = sa * sb;
+#pragma unroll
+                    for (int j = 0; j < HALF / 16; ++j) {
+                        uint32_t r[16];
+                        tc_ld_32x32b_x16(tm_lane + buf * BN + colbase + j * 16, r);
+                        tc_wait_ld();
+                        if (SBG == SB_BLOCK) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(__uint_as_float(r[i]), sab, acc[j * 16 + i]);
+                        } else {
+                            const float4 *sbv = reinterpret_cast<const float4 *>(sB + (int64_t)kb * a.ldsB + n0 + colbase + j * 16);
+#pragma unroll
+                            for (int i4 = 0; i4 < 4; ++i4) {
+                                const float4 b4 = __ldg(sbv + i4);
+                                acc[j * 16 + 4 * i4 + 0] = fmaf(__uint_as_float(r[4 * i4 + 0]) * b4.x, sa, acc[j * 16 + 4 * i4 + 0]);
+                                acc[j * 16 + 4 * i4 + 1] = fmaf(__uint_as_float(r[4 * i4 + 1]) * b4.y, sa, acc[j * 16 + 4 * i4 + 1]);
+                                acc[j * 16 + 4 * i4 + 2] = fmaf(__uint_as_float(r[4 * i4 + 2]) * b4.z, sa, acc[j * 16 + 4 * i4 + 2]);
+                                acc[j * 16 + 4 * i4 + 3] = fmaf(__uint_as_float(r[4 * i4 + 3]) * b4.w, sa, acc[j * 16 + 4 * i4 + 3]);
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[buf]);
+                    ++cc;
+                }
+                if (!ok) break;
+                store_row<HALF>(a.D, a.ldD, a.out_f32, (int64_t)m0 + row, (int64_t)n0 + colbase, acc);
+            } else {
+                const uint32_t buf = cc & 1;
+                const float sab = a.sA[0] * a.sB[0];
+                if (!warp_wait_or_abort(&tfull[buf], (cc >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < HALF / 32; ++j) {
+                    uint32_t r[32];
+                    tc_ld_32x32b_x32(tm_lane + buf * BN + colbase + j * 32, r);
+                    tc_wait_ld();
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * sab;
+                    store_row<32>(a.D, a.ldD, a.out_f32, (int64_t)m0 + row, (int64_t)n0 + colbase + j * 32, v);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[buf]);
+                ++cc;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, L::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D map over an FP8 (byte) matrix [rows][inner], box 128 (K) x box_rows,
+// 128-byte swizzle (the layout the MMA descriptors expect).
+static bool make_map(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t rows, uint32_t box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, bool PROMOTE, int SBG, bool GROUPED>
+static int run_gemm(const CUtensorMap &mA, const CUtensorMap &mB, uint32_t idesc, const GemmArgs &args, int grid,
+                    cudaStream_t st)
+{
+    using L = GemmSmem<BN, STAGES>;
+    auto kern = k_gemm<BN, STAGES, PROMOTE, SBG, GROUPED>;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_done[dev & 63]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) != cudaSuccess)
+            return FP8_ERR_CUDA;
+        attr_done[dev & 63] = true;
+    }
+    kern<<<grid, kGemmThreads, L::kBytes, st>>>(mA, mB, idesc, args);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+int launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const float *sA, int granA, const void *B,
+                int fmtB, const float *sB, int granB, void *D, int out_dtype, int64_t ldD, int *status,
+                cudaStream_t st)
+{
+    if (M == 0 || N == 0) return FP8_OK;
+    if (K == 0) {
+        const size_t esz = out_dtype == FP8_OUT_F32 ? 4 : 2;
+        return cudaMemset2DAsync(D, (size_t)ldD * esz, 0, (size_t)N * esz, (size_t)M, st) == cudaSuccess
+                   ? FP8_OK
+                   : FP8_ERR_CUDA;
+    }
+    const int BN = (N % 256 == 0) ? 256 : 128;
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, A, (uint64_t)K, (uint64_t)M, 128) || !make_map(&mB, B, (uint64_t)K, (uint64_t)N, BN))
+        return FP8_ERR_CUDA;
+    GemmArgs g{};
+    g.M = (int)M;
+    g.N = (int)N;
+    g.K = (int)K;
+    g.sA = sA;
+    g.granA = granA;
+    g.ldsA = granA == FP8_GRAN_1x128 ? M : K / 128;
+    g.sB = sB;
+    g.ldsB = granB == FP8_GRAN_1x128 ? N : K / 128;
+    g.D = D;
+    g.ldD = ldD;
+    g.out_f32 = out_dtype == FP8_OUT_F32;
+    g.status = status;
+    const int64_t ntiles = (M / 128) * (N / BN);
+    const int grid = (int)std::min<int64_t>(ntiles, sm_count());
+    const bool tensor = granA == FP8_GRAN_TENSOR;
+    if (BN == 256) {
+        const uint32_t idesc = idesc_f8f6f4(fmtA, fmtB, 128, 256);
+        if (tensor) return run_gemm<256, 4, false, SB_BLOCK, false>(mA, mB, idesc, g, grid, st);
+        if (granB == FP8_GRAN_1x128) return run_gemm<256, 4, true, SB_ROW, false>(mA, mB, idesc, g, grid, st);
+        return run_gemm<256, 4, true, SB_BLOCK, false>(mA, mB, idesc, g, grid, st);
+    } else {
+        const uint32_t idesc = idesc_f8f6f4(fmtA, fmtB, 128, 128);
+        if (tensor) return run_gemm<128, 6, false, SB_BLOCK, false>(mA, mB, idesc, g, grid, st);
+        if (granB == FP8_GRAN_1x128) return run_gemm<128, 6, true, SB_ROW, false>(mA, mB, idesc, g, grid, st);
+        return run_gemm<128, 6, true, SB_BLOCK, false>(mA, mB, idesc, g, grid, st);
+    }
+}
+
+int launch_grouped_gemm(int G, const int32_t *offsets, int64_t Mcap, int64_t N, int64_t K, const void *A,
+                        const float *sA, const void *B, const float *sB, void *D, int out_dtype, int64_t ldD,
+                        int *status, cudaStream_t st)
+{
+    if (Mcap == 0 || N == 0 || K == 0) return FP8_OK;
+    const int BN = (N % 256 == 0) ? 256 : 128;
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, A, (uint64_t)K, (uint64_t)Mcap, 128) ||
+        !make_map(&mB, B, (uint64_t)K, (uint64_t)G * (uint64_t)N, BN))
+        return FP8_ERR_CUDA;
+    GemmArgs g{};
+    g.M = (int)Mcap;
+    g.N = (int)N;
+    g.K = (int)K;
+    g.sA = sA;
+    g.granA = FP8_GRAN_1x128;
+    g.ldsA = Mcap;
+    g.sB = sB;
+    g.ldsB = K / 128;
+    g.sB_group_stride = (N / 128) * (K / 128);
+    g.D = D;
+    g.ldD = ldD;
+    g.out_f32 = out_dtype == FP8_OUT_F32;
+    g.offsets = offsets;
+    g.G = G;
+    g.status = status;
+    const int64_t ntiles_max = (Mcap / 128) * (N / BN);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ntiles_max, sm_count()));
+    if (BN == 256) return run_gemm<256, 4, true, SB_BLOCK, true>(mA, mB, idesc_f8f6f4(FP8_E4M3, FP8_E4M3, 128, 256), g, grid, st);
+    return run_gemm<128, 6, true, SB_BLOCK, true>(mA, mB, idesc_f8f6f4(FP8_E4M3, FP8_E4M3, 128, 128), g, grid, st);
+}
+
+}  // namespace fp8fg

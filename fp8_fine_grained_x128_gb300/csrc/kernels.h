@@ -1,0 +1,47 @@
+// kernels.h -- host-side launchers of the sm_103a kernels.  Arguments are
+// validated by the C ABI layer (api.cu) before any of these is called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp8fg {
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// quant.cu
+int launch_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, void *q, float *s,
+                       void *qT, float *sT, int *status, cudaStream_t st);
+int launch_quant_128x128(const void *w, int64_t rows, int64_t cols, int64_t ldw, int fmt, void *q, float *s,
+                         void *qT, float *sT, int *status, cudaStream_t st);
+int launch_transpose_128x128(const void *q, const float *s, int64_t rows, int64_t cols, void *qT, float *sT,
+                             cudaStream_t st);
+
+// pertensor.cu
+size_t pertensor_workspace_bytes();
+int launch_pertensor_delayed(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, int hist_len,
+                             int margin, int algo, float *hist, int32_t *step, float *scale, void *q, void *qT,
+                             void *stats, void *ws, int *status, cudaStream_t st);
+int launch_quant_stats(const void *x, int64_t rows, int64_t cols, int64_t ldx, const void *q, const float *s,
+                       int gran, int fmt, void *stats, void *ws, int *status, cudaStream_t st);
+int launch_selftest_wait(int timeout_ms, int *status, cudaStream_t st);
+
+// gemm.cu
+int launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const float *sA, int granA,
+                const void *B, int fmtB, const float *sB, int granB, void *D, int out_dtype, int64_t ldD,
+                int *status, cudaStream_t st);
+int launch_grouped_gemm(int G, const int32_t *offsets, int64_t Mcap, int64_t N, int64_t K, const void *A,
+                        const float *sA, const void *B, const float *sB, void *D, int out_dtype, int64_t ldD,
+                        int *status, cudaStream_t st);
+
+// moe.cu
+int launch_moe_route_pad(const float *logits, int64_t T, int E, int topk, int align, int64_t Mcap,
+                         int32_t *topk_idx, float *topk_prob, int32_t *counts, int32_t *offsets, int32_t *row_token,
+                         float *row_prob, uint8_t *row_is_pad, int *status, cudaStream_t st);
+int launch_moe_gather(const void *q, const float *s, int64_t T, int64_t K, const int32_t *row_token,
+                      const int32_t *offsets, int E, int64_t Mcap, void *qg, float *sg, cudaStream_t st);
+int launch_swiglu_fwd(const void *gu, int64_t rows, int64_t F, void *h, cudaStream_t st);
+int launch_swiglu_bwd(const void *gu, const void *dh, int64_t rows, int64_t F, void *dgu, cudaStream_t st);
+
+}  // namespace fp8fg

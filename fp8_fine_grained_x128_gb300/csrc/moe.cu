@@ -1,0 +1,341 @@
+// moe.cu -- MoE routing with the padded routing map, FP8 dispatch gather, and
+// the SwiGLU glue between the up and down projections (sm_103a).
+//
+// Ling 2.0 FP8 pretraining blog, "FP8 padding routing map": instead of
+// padding/unpadding layers around the FP8 GEMM, the routing map itself is
+// edited before dispatch so every expert's token count meets the GEMM's
+// multiple; the added entries carry router probability 0, so the result is
+// mathematically unchanged.  Here the multiple is 128 (the GEMM's M tile and
+// the 1x128 scale group), the added entries are the lowest-index tokens not
+// already routed to that expert, and the rows of an expert are its tokens in
+// ascending order -- all decided on the device, no host round trip.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8fg {
+
+// ---------------------------------------------------------------- top-k
+
+template <int EPL>
+__global__ void __launch_bounds__(256) k_moe_topk(const float *__restrict__ logits, int64_t T, int E, int topk,
+                                                  int32_t *__restrict__ topk_idx, float *__restrict__ topk_prob)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t t = w0; t < T; t += nw) {
+        float z[EPL];
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int e = j * 32 + lane;
+            z[j] = e < E ? logits[t * E + e] : -INFINITY;
+            m = fmaxf(m, z[j]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float sum = 0.0f;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j)
+            if (j * 32 + lane < E) sum += expf(z[j] - m);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        uint32_t taken = 0;
+        for (int k = 0; k < topk; ++k) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) {
+                const int e = j * 32 + lane;
+                if (e < E && !((taken >> j) & 1u) && (z[j] > bv || (z[j] == bv && e < bi))) {
+                    bv = z[j];
+                    bi = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            if (lane == 0) {
+                topk_idx[t * topk + k] = bi;
+                topk_prob[t * topk + k] = expf(bv - m) / sum;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------ per-expert count
+
+__device__ __forceinline__ bool routed_to(const int32_t *__restrict__ topk_idx, int64_t t, int topk, int e)
+{
+    bool r = false;
+    for (int k = 0; k < topk; ++k) r |= topk_idx[t * topk + k] == e;
+    return r;
+}
+
+__global__ void __launch_bounds__(256) k_moe_count(const int32_t *__restrict__ topk_idx, int64_t T, int topk,
+                                                   int32_t *__restrict__ counts)
+{
+    const int e = blockIdx.x;
+    int total = 0;
+    for (int64_t t0 = 0; t0 < T; t0 += blockDim.x) {
+        const int64_t t = t0 + threadIdx.x;
+        total += __syncthreads_count(t < T && routed_to(topk_idx, t, topk, e));
+    }
+    if (threadIdx.x == 0) counts[e] = total;
+}
+
+// Block-wide exclusive prefix sum of a 0/1 flag (256 threads) and the total.
+__device__ __forceinline__ int block_excl_scan(int flag, int *warp_tot, int &total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t bal = __ballot_sync(0xffffffffu, flag);
+    const int within = __popc(bal & ((1u << lane) - 1u));
+    __syncthreads();
+    if (lane == 0) warp_tot[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0;
+    total = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+        if (w < warp) before += warp_tot[w];
+        total += warp_tot[w];
+    }
+    return before + within;
+}
+
+__device__ __forceinline__ int64_t padded_count(int c, int align) { return ((int64_t)c + align - 1) / align * align; }
+
+// One CTA per expert: offset from the padded counts of earlier experts, the
+// routing-map edit (first `need` free tokens), and the dispatch rows.
+__global__ void __launch_bounds__(256) k_moe_fill(const int32_t *__restrict__ topk_idx,
+                                                  const float *__restrict__ topk_prob, const int32_t *__restrict__ counts,
+                                                  int64_t T, int E, int topk, int align, int64_t Mcap,
+                                                  int32_t *__restrict__ offsets, int32_t *__restrict__ row_token,
+                                                  float *__restrict__ row_prob, uint8_t *__restrict__ row_is_pad,
+                                                  int *status)
+{
+    __shared__ int warp_tot[8];
+    __shared__ int64_t red[8];
+    const int e = blockIdx.x;
+    // offset of this expert and the total, from the counts of all experts
+    int64_t before = 0, all = 0;
+    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+        const int64_t p = padded_count(counts[i], align);
+        if (i < e) before += p;
+        all += p;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+        all += __shfl_xor_sync(0xffffffffu, all, o);
+    }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = before;
+    __syncthreads();
+    int64_t off = 0;
+    for (int w = 0; w < 8; ++w) off += red[w];
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = all;
+    __syncthreads();
+    int64_t total = 0;
+    for (int w = 0; w < 8; ++w) total += red[w];
+
+    const int c = counts[e];
+    const int64_t need = padded_count(c, align) - c;
+    if (threadIdx.x == 0) {
+        offsets[e] = (int32_t)off;
+        if (e == E - 1) {
+            offsets[E] = (int32_t)total;
+            if (total > Mcap) set_status(status, FP8_ERR_INVALID_ARG);
+        }
+    }
+    int64_t free_seen = 0, placed = 0;
+    for (int64_t t0 = 0; t0 < T; t0 += blockDim.x) {
+        const int64_t t = t0 + threadIdx.x;
+        const bool in = t < T;
+        int k_hit = -1;
+        if (in)
+            for (int k = 0; k < topk; ++k)
+                if (topk_idx[t * topk + k] == e) k_hit = k;
+        const bool routed = k_hit >= 0;
+        const bool fr = in && !routed;
+        int nfree = 0;
+        const int fpos = block_excl_scan(fr ? 1 : 0, warp_tot, nfree);
+        const bool pad = fr && (free_seen + fpos < need);
+        const bool member = routed || pad;
+        int nmem = 0;
+        const int mpos = block_excl_scan(member ? 1 : 0, warp_tot, nmem);
+        if (member) {
+            const int64_t r = off + placed + mpos;
+            if (r < Mcap) {
+                row_token[r] = (int32_t)t;
+                row_prob[r] = routed ? topk_prob[t * topk + k_hit] : 0.0f;
+                if (row_is_pad) row_is_pad[r] = pad ? 1 : 0;
+            }
+        }
+        free_seen += nfree;
+        placed += nmem;
+    }
+    // rows past the last expert
+    for (int64_t r = total + (int64_t)e * blockDim.x + threadIdx.x; r < Mcap; r += (int64_t)E * blockDim.x) {
+        row_token[r] = -1;
+        row_prob[r] = 0.0f;
+        if (row_is_pad) row_is_pad[r] = 0;
+    }
+}
+
+// ---------------------------------------------------------------- gather
+
+// One warp per dispatched row: K FP8 bytes and K/128 scales of its token.
+__global__ void __launch_bounds__(256) k_moe_gather(const uint8_t *__restrict__ q, const float *__restrict__ s,
+                                                    int64_t T, int64_t K, const int32_t *__restrict__ row_token,
+                                                    const int32_t *__restrict__ offsets, int E, int64_t Mcap,
+                                                    uint8_t *__restrict__ qg, float *__restrict__ sg)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t total = min((int64_t)offsets[E], Mcap);
+    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r = w0; r < total; r += nw) {
+        const int64_t t = row_token[r];
+        if (t < 0 || t >= T) continue;
+        const uint4 *src = reinterpret_cast<const uint4 *>(q + t * K);
+        uint4 *dst = reinterpret_cast<uint4 *>(qg + r * K);
+        for (int64_t i = lane; i < K / 16; i += 32) dst[i] = src[i];
+        for (int64_t kb = lane; kb < K / 128; kb += 32) sg[kb * Mcap + r] = s[kb * T + t];
+    }
+}
+
+// ---------------------------------------------------------------- SwiGLU
+
+__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__global__ void __launch_bounds__(256) k_swiglu_fwd(const uint16_t *__restrict__ gu, int64_t rows, int64_t F,
+                                                    uint16_t *__restrict__ h)
+{
+    const int64_t nvec = rows * (F / 8);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / (F / 8), j = (i - r * (F / 8)) * 8;
+        const uint4 g4 = *reinterpret_cast<const uint4 *>(gu + r * 2 * F + j);
+        const uint4 u4 = *reinterpret_cast<const uint4 *>(gu + r * 2 * F + F + j);
+        const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float g0 = bf16_lo(gw[k]), g1 = bf16_hi(gw[k]);
+            const float h0 = g0 * sigmoidf_(g0) * bf16_lo(uw[k]);
+            const float h1 = g1 * sigmoidf_(g1) * bf16_hi(uw[k]);
+            o[k] = bf16x2_rn(h0, h1);
+        }
+        *reinterpret_cast<uint4 *>(h + r * F + j) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+__global__ void __launch_bounds__(256) k_swiglu_bwd(const uint16_t *__restrict__ gu, const uint16_t *__restrict__ dh,
+                                                    int64_t rows, int64_t F, uint16_t *__restrict__ dgu)
+{
+    const int64_t nvec = rows * (F / 8);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / (F / 8), j = (i - r * (F / 8)) * 8;
+        const uint4 g4 = *reinterpret_cast<const uint4 *>(gu + r * 2 * F + j);
+        const uint4 u4 = *reinterpret_cast<const uint4 *>(gu + r * 2 * F + F + j);
+        const uint4 d4 = *reinterpret_cast<const uint4 *>(dh + r * F + j);
+        const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w},
+                       dw[4] = {d4.x, d4.y, d4.z, d4.w};
+        uint32_t og[4], ou[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float dgv[2], duv[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float g = hh ? bf16_hi(gw[k]) : bf16_lo(gw[k]);
+                const float u = hh ? bf16_hi(uw[k]) : bf16_lo(uw[k]);
+                const float d = hh ? bf16_hi(dw[k]) : bf16_lo(dw[k]);
+                const float sg = sigmoidf_(g);
+                dgv[hh] = d * u * sg * (1.0f + g * (1.0f - sg));
+                duv[hh] = d * g * sg;
+            }
+            og[k] = bf16x2_rn(dgv[0], dgv[1]);
+            ou[k] = bf16x2_rn(duv[0], duv[1]);
+        }
+        *reinterpret_cast<uint4 *>(dgu + r * 2 * F + j) = make_uint4(og[0], og[1], og[2], og[3]);
+        *reinterpret_cast<uint4 *>(dgu + r * 2 * F + F + j) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+
+static int check_launch() { return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
+
+int launch_moe_route_pad(const float *logits, int64_t T, int E, int topk, int align, int64_t Mcap, int32_t *topk_idx,
+                         float *topk_prob, int32_t *counts, int32_t *offsets, int32_t *row_token, float *row_prob,
+                         uint8_t *row_is_pad, int *status, cudaStream_t st)
+{
+    int64_t blocks = (T + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    const unsigned b = (unsigned)blocks;
+    const int epl = (E + 31) / 32;
+    if (epl <= 1) k_moe_topk<1><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob);
+    else if (epl <= 2) k_moe_topk<2><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob);
+    else if (epl <= 4) k_moe_topk<4><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob);
+    else k_moe_topk<8><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob);
+    k_moe_count<<<E, 256, 0, st>>>(topk_idx, T, topk, counts);
+    k_moe_fill<<<E, 256, 0, st>>>(topk_idx, topk_prob, counts, T, E, topk, align, Mcap, offsets, row_token, row_prob,
+                                  row_is_pad, status);
+    return check_launch();
+}
+
+int launch_moe_gather(const void *q, const float *s, int64_t T, int64_t K, const int32_t *row_token,
+                      const int32_t *offsets, int E, int64_t Mcap, void *qg, float *sg, cudaStream_t st)
+{
+    int64_t blocks = (Mcap + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    k_moe_gather<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint8_t *>(q), s, T, K, row_token, offsets, E,
+                                                   Mcap, static_cast<uint8_t *>(qg), sg);
+    return check_launch();
+}
+
+int launch_swiglu_fwd(const void *gu, int64_t rows, int64_t F, void *h, cudaStream_t st)
+{
+    const int64_t nvec = rows * (F / 8);
+    if (nvec == 0) return FP8_OK;
+    int64_t blocks = (nvec + 255) / 256;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    k_swiglu_fwd<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t *>(gu), rows, F,
+                                                   static_cast<uint16_t *>(h));
+    return check_launch();
+}
+
+int launch_swiglu_bwd(const void *gu, const void *dh, int64_t rows, int64_t F, void *dgu, cudaStream_t st)
+{
+    const int64_t nvec = rows * (F / 8);
+    if (nvec == 0) return FP8_OK;
+    int64_t blocks = (nvec + 255) / 256;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    k_swiglu_bwd<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t *>(gu),
+                                                   static_cast<const uint16_t *>(dh), rows, F,
+                                                   static_cast<uint16_t *>(dgu));
+    return check_launch();
+}
+
+}  // namespace fp8fg

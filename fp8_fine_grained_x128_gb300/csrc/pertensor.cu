@@ -1,0 +1,522 @@
+// pertensor.cu -- per-tensor delayed scaling with fused monitors, and the
+// standalone monitor kernels (sm_103a).
+//
+// Delayed scaling ("FP8 training infrastructure" guide, "Transformer Engine"
+// DelayedScaling and "Scaling strategies: delayed scaling"): the scale of
+// step t comes from the amax history of earlier steps, so quantization needs
+// no grid-wide reduction before it starts.  One persistent pass quantizes
+// with s_t, reduces this step's amax and the monitors, and the last CTA to
+// finish (atomic ticket, no spinning) writes the history slot, the next scale
+// and the step counter, and re-zeroes the workspace.
+//
+// Monitors (Ling 2.0 FP8 pretraining blog, "Where does the error come
+// from?" and the underflow / distortion monitor table): nonzero, underflow
+// (nonzero -> +-0), saturated (|x/s| > fmax), distinct values in and out per
+// scaling group (+-0 counted once).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8fg {
+
+// Caller-owned workspace for tensor-wide reductions.  Zeroed by the caller
+// once; every call that completes leaves it zeroed again.
+struct PtWorkspace {
+    unsigned int ticket;
+    unsigned int amax_bits;
+    unsigned int pad[2];
+    unsigned int bmx[2048];   // presence of the 65536 BF16 keys
+    unsigned int bmq[8];      // presence of the 256 FP8 keys
+};
+
+size_t pertensor_workspace_bytes() { return sizeof(PtWorkspace); }
+
+__device__ __forceinline__ uint32_t key_bf16(uint32_t b) { return (b & 0x7FFFu) == 0 ? 0u : b; }
+__device__ __forceinline__ uint32_t key_fp8(uint32_t c) { return (c & 0x7Fu) == 0 ? 0u : c; }
+
+__device__ __forceinline__ void bitmap_set(uint32_t *bm, uint32_t key)
+{
+    const uint32_t bit = 1u << (key & 31);
+    uint32_t *w = bm + (key >> 5);
+    if (!(*reinterpret_cast<volatile uint32_t *>(w) & bit)) atomicOr(w, bit);
+}
+
+struct Counts {
+    uint32_t nz = 0, uf = 0, sat = 0;
+};
+
+// Quantize 8 BF16 values with one scale and (optionally) account the monitors.
+template <int FMT, bool STATS>
+__device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider &d, Counts &c, uint32_t *bmx, uint32_t *bmq)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float qv[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        qv[2 * j] = d(bf16_lo(w[j]));
+        qv[2 * j + 1] = d(bf16_hi(w[j]));
+    }
+    uint2 out;
+    out.x = cvt2<FMT>(qv[0], qv[1]) | (cvt2<FMT>(qv[2], qv[3]) << 16);
+    out.y = cvt2<FMT>(qv[4], qv[5]) | (cvt2<FMT>(qv[6], qv[7]) << 16);
+    if (STATS) {
+        const float fm = fmax_of(FMT);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t xb = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+            const uint32_t code = ((e < 4 ? out.x : out.y) >> (8 * (e & 3))) & 0xFFu;
+            const bool nzero = (xb & 0x7FFFu) != 0;
+            c.nz += nzero;
+            c.uf += nzero && ((code & 0x7Fu) == 0);
+            c.sat += fabsf(qv[e]) > fm;
+            bitmap_set(bmx, key_bf16(xb));
+            bitmap_set(bmq, key_fp8(code));
+        }
+    }
+    return out;
+}
+
+// Block-wide sum / max of per-thread values (256 threads), result in thread 0.
+__device__ __forceinline__ uint32_t block_reduce_sum(uint32_t v, uint32_t *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    uint32_t r = 0;
+    if (threadIdx.x == 0)
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) r += red[i];
+    return r;
+}
+
+__device__ __forceinline__ uint32_t block_reduce_max(uint32_t v, uint32_t *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    uint32_t r = 0;
+    if (threadIdx.x == 0)
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) r = max(r, red[i]);
+    return r;
+}
+
+// Merges this CTA's counts and presence bitmaps into the stats / workspace,
+// takes a ticket, and returns true in every thread of the last CTA.
+template <bool STATS>
+__device__ bool merge_and_ticket(const Counts &c, uint32_t amax, const uint32_t *bmx, const uint32_t *bmq,
+                                 fp8_stats_t *stats, PtWorkspace *ws, uint32_t *red, int *is_last)
+{
+    const uint32_t a = block_reduce_max(amax, red);
+    if (threadIdx.x == 0) atomicMax(&ws->amax_bits, a);
+    if (STATS) {
+        const uint32_t nz = block_reduce_sum(c.nz, red);
+        const uint32_t uf = block_reduce_sum(c.uf, red);
+        const uint32_t sat = block_reduce_sum(c.sat, red);
+        if (threadIdx.x == 0) {
+            atomicAdd(reinterpret_cast<unsigned long long *>(&stats->nonzero), (unsigned long long)nz);
+            atomicAdd(reinterpret_cast<unsigned long long *>(&stats->underflow), (unsigned long long)uf);
+            atomicAdd(reinterpret_cast<unsigned long long *>(&stats->saturated), (unsigned long long)sat);
+        }
+        for (int i = threadIdx.x; i < 2048; i += blockDim.x)
+            if (bmx[i]) atomicOr(&ws->bmx[i], bmx[i]);
+        if (threadIdx.x < 8 && bmq[threadIdx.x]) atomicOr(&ws->bmq[threadIdx.x], bmq[threadIdx.x]);
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *is_last = (atomicAdd(&ws->ticket, 1u) == gridDim.x - 1);
+    __syncthreads();
+    return *is_last != 0;
+}
+
+// In the last CTA: distinct counts from the merged bitmaps, workspace reset.
+template <bool STATS>
+__device__ void finalize_distinct_and_reset(fp8_stats_t *stats, PtWorkspace *ws, uint32_t *red)
+{
+    __threadfence();
+    if (STATS) {
+        uint32_t din = 0, dout = 0;
+        for (int i = threadIdx.x; i < 2048; i += blockDim.x) {
+            din += __popc(__ldcg(&ws->bmx[i]));
+            ws->bmx[i] = 0;
+        }
+        if (threadIdx.x < 8) {
+            dout = __popc(__ldcg(&ws->bmq[threadIdx.x]));
+            ws->bmq[threadIdx.x] = 0;
+        }
+        din = block_reduce_sum(din, red);
+        dout = block_reduce_sum(dout, red);
+        if (threadIdx.x == 0) {
+            atomicAdd(reinterpret_cast<unsigned long long *>(&stats->distinct_in), (unsigned long long)din);
+            atomicAdd(reinterpret_cast<unsigned long long *>(&stats->distinct_out), (unsigned long long)dout);
+        }
+    }
+    if (threadIdx.x == 0) ws->ticket = 0;
+}
+
+// ---------------------------------------------------------------------------
+// Delayed-scaling quantization of one tensor, one step.
+// ---------------------------------------------------------------------------
+template <int FMT, bool TRANS, bool STATS>
+__global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
+                                                           int64_t ldx, int hist_len, int margin, int algo,
+                                                           float *hist, int32_t *step, float *scale,
+                                                           uint8_t *__restrict__ q, uint8_t *__restrict__ qT,
+                                                           fp8_stats_t *stats, PtWorkspace *ws, int *status)
+{
+    __shared__ uint32_t ct[TRANS ? 128 * 33 : 1];
+    __shared__ uint32_t bmx[STATS ? 2048 : 1];
+    __shared__ uint32_t bmq[8];
+    __shared__ uint32_t red[32];
+    __shared__ int is_last;
+
+    const int t = threadIdx.x;
+    const int g = t & 15, rr = t >> 4;
+    if (STATS) {
+        for (int i = t; i < 2048; i += 256) bmx[i] = 0;
+        if (t < 8) bmq[t] = 0;
+    }
+    const float s_t = *scale;   // chosen from the amax of earlier steps
+    const Divider d(s_t);
+    __syncthreads();
+
+    Counts c;
+    uint32_t amax = 0;
+    const int64_t ncb = cols / 128, nrb = (rows + 127) / 128;
+    const int64_t ntiles = nrb * ncb;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t rb = tile / ncb, cb = tile - rb * ncb;
+        const int64_t r0 = rb * 128, c0 = cb * 128;
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int64_t r = r0 + rr + 16 * i;
+            v[i] = r < rows ? ldg_stream(x + r * ldx + c0 + g * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int row = rr + 16 * i;
+            if (r0 + row < rows) {
+                amax = max(amax, absmax8(v[i]));
+                const uint2 code = quant8_mon<FMT, STATS>(v[i], d, c, bmx, bmq);
+                *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = code;
+                if (TRANS) {
+                    ct[row * 33 + 2 * g] = code.x;
+                    ct[row * 33 + 2 * g + 1] = code.y;
+                }
+            }
+        }
+        if (TRANS) {
+            __syncthreads();
+            // transposed copy: same scale, so exactly q^T
+            const int lane = t & 31, warp = t >> 5;
+            const int cw = (lane >> 3) + 4 * warp;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int mg = (lane & 7) + 8 * k;
+                const uint32_t w0 = ct[(4 * mg + 0) * 33 + cw];
+                const uint32_t w1 = ct[(4 * mg + 1) * 33 + cw];
+                const uint32_t w2 = ct[(4 * mg + 2) * 33 + cw];
+                const uint32_t w3 = ct[(4 * mg + 3) * 33 + cw];
+                const uint32_t t0 = __byte_perm(w0, w1, 0x5140), t1 = __byte_perm(w2, w3, 0x5140);
+                const uint32_t t2 = __byte_perm(w0, w1, 0x7362), t3 = __byte_perm(w2, w3, 0x7362);
+                uint8_t *dst = qT + (c0 + 4 * cw) * rows + r0 + 4 * mg;
+                *reinterpret_cast<uint32_t *>(dst) = __byte_perm(t0, t1, 0x5410);
+                *reinterpret_cast<uint32_t *>(dst + rows) = __byte_perm(t0, t1, 0x7632);
+                *reinterpret_cast<uint32_t *>(dst + 2 * rows) = __byte_perm(t2, t3, 0x5410);
+                *reinterpret_cast<uint32_t *>(dst + 3 * rows) = __byte_perm(t2, t3, 0x7632);
+            }
+            __syncthreads();
+        }
+    }
+
+    if (!merge_and_ticket<STATS>(c, amax, bmx, bmq, stats, ws, red, &is_last)) return;
+
+    // ---- last CTA: state update (history slot, next scale, step) ----
+    finalize_distinct_and_reset<STATS>(stats, ws, red);
+    if (t == 0) {
+        const uint32_t a = atomicExch(&ws->amax_bits, 0u);
+        if (a >= 0x7F80u) {
+            // Inf/NaN in this step: report it and leave the state untouched
+            set_status(status, FP8_ERR_NONFINITE);
+        } else {
+            const float amax_t = __uint_as_float(a << 16);
+            const int32_t st = *step;
+            hist[st % hist_len] = amax_t;
+            float m = amax_t;
+            if (algo == FP8_AMAX_MAX) {
+                m = 0.0f;
+                for (int i = 0; i < hist_len; ++i) m = fmaxf(m, hist[i]);
+            }
+            if (m > 0.0f) {
+                const float p2 = __uint_as_float((uint32_t)(127 + margin) << 23);   // 2^margin, exact
+                *scale = __fdiv_rn(__fmul_rn(m, p2), fmax_of(FMT));
+            }
+            *step = st + 1;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Monitors of an existing quantization.
+// ---------------------------------------------------------------------------
+
+// Groups of 128 elements (1x128 tiles, or 128 rows of one column for the
+// transposed copy): one warp per group, 4 elements per lane; distinct values
+// by comparing every element with all earlier ones through shuffles.
+template <int FMT, bool COLS>
+__global__ void __launch_bounds__(256) k_stats_g128(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
+                                                    int64_t ldx, const uint8_t *__restrict__ q,
+                                                    const float *__restrict__ s, fp8_stats_t *stats)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t ngroups = COLS ? (rows / 128) * cols : rows * (cols / 128);
+    const float fm = fmax_of(FMT);
+    uint32_t nz = 0, uf = 0, sat = 0, din = 0, dout = 0;
+    for (int64_t gi = warp0; gi < ngroups; gi += nwarps) {
+        uint32_t kx[4], kq[4];
+        float sc;
+        if (COLS) {
+            const int64_t mb = gi / cols, c = gi - mb * cols;
+            sc = s[mb * cols + c];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t r = mb * 128 + j * 32 + lane;
+                kx[j] = x[r * ldx + c];
+                kq[j] = q[c * rows + r];
+            }
+        } else {
+            const int64_t ncb = cols / 128;
+            const int64_t r = gi / ncb, cb = gi - r * ncb;
+            sc = s[cb * rows + r];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                kx[j] = x[r * ldx + cb * 128 + j * 32 + lane];
+                kq[j] = q[r * cols + cb * 128 + j * 32 + lane];
+            }
+        }
+        const Divider d(sc);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool nzero = (kx[j] & 0x7FFFu) != 0;
+            nz += nzero;
+            uf += nzero && ((kq[j] & 0x7Fu) == 0);
+            sat += fabsf(d(__uint_as_float(kx[j] << 16))) > fm;
+            kx[j] = key_bf16(kx[j]);
+            kq[j] = key_fp8(kq[j]);
+        }
+        uint32_t dupx = 0, dupq = 0;   // bit j: element j*32+lane repeats an earlier one
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            for (int src = 0; src < 32; ++src) {
+                const uint32_t ox = __shfl_sync(0xffffffffu, kx[jj], src);
+                const uint32_t oq = __shfl_sync(0xffffffffu, kq[jj], src);
+                const int other = jj * 32 + src;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (other < j * 32 + lane) {
+                        dupx |= (uint32_t)(ox == kx[j]) << j;
+                        dupq |= (uint32_t)(oq == kq[j]) << j;
+                    }
+                }
+            }
+        }
+        din += 4 - __popc(dupx);
+        dout += 4 - __popc(dupq);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        nz += __shfl_xor_sync(0xffffffffu, nz, o);
+        uf += __shfl_xor_sync(0xffffffffu, uf, o);
+        sat += __shfl_xor_sync(0xffffffffu, sat, o);
+        din += __shfl_xor_sync(0xffffffffu, din, o);
+        dout += __shfl_xor_sync(0xffffffffu, dout, o);
+    }
+    if (lane == 0 && nz + sat + din + dout > 0) {
+        atomicAdd(reinterpret_cast<unsigned long long *>(&stats->nonzero), (unsigned long long)nz);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&stats->underflow), (unsigned long long)uf);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&stats->saturated), (unsigned long long)sat);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&stats->distinct_in), (unsigned long long)din);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&stats->distinct_out), (unsigned long long)dout);
+    }
+}
+
+// 128x128 blocks (one CTA per block, shared presence bitmaps) and the whole
+// tensor as one group (persistent grid, bitmaps merged in the workspace).
+template <int FMT, bool TENSOR>
+__global__ void __launch_bounds__(256) k_stats_blocks(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
+                                                      int64_t ldx, const uint8_t *__restrict__ q,
+                                                      const float *__restrict__ s, fp8_stats_t *stats,
+                                                      PtWorkspace *ws)
+{
+    __shared__ uint32_t bmx[2048];
+    __shared__ uint32_t bmq[8];
+    __shared__ uint32_t red[32];
+    __shared__ int is_last;
+    const int t = threadIdx.x, g = t & 15, rr = t >> 4;
+    const float fm = fmax_of(FMT);
+    const int64_t ncb = cols / 128, nrb = rows / 128, ntiles = ncb * nrb;
+    Counts c;
+    uint32_t din = 0, dout = 0;
+    if (TENSOR) {
+        for (int i = t; i < 2048; i += 256) bmx[i] = 0;
+        if (t < 8) bmq[t] = 0;
+        __syncthreads();
+    }
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t rb = tile / ncb, cb = tile - rb * ncb;
+        if (!TENSOR) {
+            __syncthreads();
+            for (int i = t; i < 2048; i += 256) bmx[i] = 0;
+            if (t < 8) bmq[t] = 0;
+            __syncthreads();
+        }
+        const Divider d(TENSOR ? s[0] : s[rb * ncb + cb]);
+#pragma unroll 2
+        for (int i = 0; i < 8; ++i) {
+            const int64_t r = rb * 128 + rr + 16 * i;
+            const uint4 v = ldg_stream(x + r * ldx + cb * 128 + g * 8);
+            const uint2 qq = *reinterpret_cast<const uint2 *>(q + r * cols + cb * 128 + g * 8);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t xb = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+                const uint32_t code = ((e < 4 ? qq.x : qq.y) >> (8 * (e & 3))) & 0xFFu;
+                const bool nzero = (xb & 0x7FFFu) != 0;
+                c.nz += nzero;
+                c.uf += nzero && ((code & 0x7Fu) == 0);
+                c.sat += fabsf(d(__uint_as_float(xb << 16))) > fm;
+                bitmap_set(bmx, key_bf16(xb));
+                bitmap_set(bmq, key_fp8(code));
+            }
+        }
+        if (!TENSOR) {
+            __syncthreads();
+            for (int i = t; i < 2048; i += 256) din += __popc(bmx[i]);
+            if (t < 8) dout += __popc(bmq[t]);
+        }
+    }
+    if (!TENSOR) {
+        const uint32_t nz = block_reduce_sum(c.nz, red);
+        const uint32_t uf = block_reduce_sum(c.uf, red);
+        const uint32_t sat = block_reduce_sum(c.sat, red);
+        din = block_reduce_sum(din, red);
+        dout = block_reduce_sum(dout, red);
+        if (t == 0) {
+            atomicAdd(reinterpret_cast<unsigned long long *>(&stats->nonzero), (unsigned long long)nz);
+            atomicAdd(reinterpret_cast<unsigned long long *>(&stats->underflow), (unsigned long long)uf);
+            atomicAdd(reinterpret_cast<unsigned long long *>(&stats->saturated), (unsigned long long)sat);
+            atomicAdd(reinterpret_cast<unsigned long long *>(&stats->distinct_in), (unsigned long long)din);
+            atomicAdd(reinterpret_cast<unsigned long long *>(&stats->distinct_out), (unsigned long long)dout);
+        }
+        return;
+    }
+    if (!merge_and_ticket<true>(c, 0u, bmx, bmq, stats, ws, red, &is_last)) return;
+    finalize_distinct_and_reset<true>(stats, ws, red);
+    if (t == 0) ws->amax_bits = 0;
+}
+
+// ---------------------------------------------------------------------------
+// Bounded-wait self-test: one thread waits on a barrier nothing arrives at.
+// ---------------------------------------------------------------------------
+__global__ void k_selftest_wait(uint64_t timeout_ns, int *status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (!mbar_wait_bounded(&bar, 0, nullptr, timeout_ns)) set_status(status, FP8_ERR_TIMEOUT);
+        // complete the phase so the barrier is left in a clean state
+        mbar_arrive(&bar);
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ launchers
+
+static int check_launch() { return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA; }
+
+template <int FMT, bool TRANS, bool STATS>
+static void delayed_launch(int blocks, cudaStream_t st, const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                           int hist_len, int margin, int algo, float *hist, int32_t *step, float *scale, void *q,
+                           void *qT, void *stats, void *ws, int *status)
+{
+    k_pertensor_delayed<FMT, TRANS, STATS><<<blocks, 256, 0, st>>>(
+        static_cast<const uint16_t *>(x), rows, cols, ldx, hist_len, margin, algo, hist, step, scale,
+        static_cast<uint8_t *>(q), static_cast<uint8_t *>(qT), static_cast<fp8_stats_t *>(stats),
+        static_cast<PtWorkspace *>(ws), status);
+}
+
+int launch_pertensor_delayed(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, int hist_len,
+                             int margin, int algo, float *hist, int32_t *step, float *scale, void *q, void *qT,
+                             void *stats, void *ws, int *status, cudaStream_t st)
+{
+    const int64_t ntiles = ((rows + 127) / 128) * (cols / 128);
+    int64_t blocks = (int64_t)sm_count() * 4;
+    if (blocks > ntiles) blocks = ntiles;
+    if (blocks < 1) blocks = 1;   // an empty tensor still runs the state update
+    const int b = (int)blocks;
+    const bool tr = qT != nullptr, stt = stats != nullptr;
+#define FP8FG_DL(F, T, S) delayed_launch<F, T, S>(b, st, x, rows, cols, ldx, hist_len, margin, algo, hist, step, scale, q, qT, stats, ws, status)
+    if (fmt == FP8_E5M2) {
+        if (tr) { if (stt) FP8FG_DL(FP8_E5M2, true, true); else FP8FG_DL(FP8_E5M2, true, false); }
+        else { if (stt) FP8FG_DL(FP8_E5M2, false, true); else FP8FG_DL(FP8_E5M2, false, false); }
+    } else {
+        if (tr) { if (stt) FP8FG_DL(FP8_E4M3, true, true); else FP8FG_DL(FP8_E4M3, true, false); }
+        else { if (stt) FP8FG_DL(FP8_E4M3, false, true); else FP8FG_DL(FP8_E4M3, false, false); }
+    }
+#undef FP8FG_DL
+    return check_launch();
+}
+
+int launch_quant_stats(const void *x, int64_t rows, int64_t cols, int64_t ldx, const void *q, const float *s,
+                       int gran, int fmt, void *stats, void *ws, int *status, cudaStream_t st)
+{
+    (void)status;
+    if (rows == 0 || cols == 0) return FP8_OK;
+    auto X = static_cast<const uint16_t *>(x);
+    auto Q = static_cast<const uint8_t *>(q);
+    auto S = static_cast<fp8_stats_t *>(stats);
+    auto W = static_cast<PtWorkspace *>(ws);
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (gran == FP8_GRAN_1x128 || gran == FP8_GRAN_128x1) {
+        const bool cols_mode = gran == FP8_GRAN_128x1;
+        const int64_t groups = cols_mode ? (rows / 128) * cols : rows * (cols / 128);
+        int64_t blocks = (groups + 7) / 8;
+        if (blocks > cap) blocks = cap;
+        const unsigned b = (unsigned)blocks;
+        if (fmt == FP8_E5M2) {
+            if (cols_mode) k_stats_g128<FP8_E5M2, true><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S);
+            else k_stats_g128<FP8_E5M2, false><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S);
+        } else {
+            if (cols_mode) k_stats_g128<FP8_E4M3, true><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S);
+            else k_stats_g128<FP8_E4M3, false><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S);
+        }
+        return check_launch();
+    }
+    const int64_t ntiles = (rows / 128) * (cols / 128);
+    int64_t blocks = gran == FP8_GRAN_TENSOR ? std::min<int64_t>(ntiles, (int64_t)sm_count() * 4) : ntiles;
+    const unsigned b = (unsigned)blocks;
+    if (fmt == FP8_E5M2) {
+        if (gran == FP8_GRAN_TENSOR) k_stats_blocks<FP8_E5M2, true><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S, W);
+        else k_stats_blocks<FP8_E5M2, false><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S, W);
+    } else {
+        if (gran == FP8_GRAN_TENSOR) k_stats_blocks<FP8_E4M3, true><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S, W);
+        else k_stats_blocks<FP8_E4M3, false><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S, W);
+    }
+    return check_launch();
+}
+
+int launch_selftest_wait(int timeout_ms, int *status, cudaStream_t st)
+{
+    k_selftest_wait<<<1, 32, 0, st>>>((uint64_t)timeout_ms * 1000000ull, status);
+    return check_launch();
+}
+
+}  // namespace fp8fg

@@ -1,0 +1,378 @@
+// quant.cu -- BF16 -> FP8 quantizers of the fine-grained FP8 Linear (sm_103a).
+//
+//   * 1x128 activation/gradient tiles (Ling 2.0 FP8 pretraining blog,
+//     "Fine-grained quantization (per-tile/block wise scaling)"; activations
+//     are quantized dynamically, FP8-RL article "dynamic weight sync").
+//   * the same plus the transposed copy quantized along the token dimension
+//     for the wgrad operand ("grad (transpose)" in the blog's monitor table),
+//     from ONE read of the input.
+//   * 128x128 weight blocks (FP8-RL article, "dynamic weight sync"), with an
+//     optional transposed copy written in the same pass.
+//   * the on-demand FP8 weight transpose (blog, "FP8 on-demand transpose
+//     weight").
+// Quantization rule ("FP8-LM: Training FP8 Large Language Models", "Tensor
+// scaling"): s = fp32(amax / fmax), q = RNE_satfinite(fp32(x) / s).
+//
+// All of these are HBM-bound streaming kernels: 16-byte vector loads, amax by
+// warp shuffles, coalesced FP8 stores, no tensor-core work.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8fg {
+
+// ---------------------------------------------------------------------------
+// 1x128 along rows only.  A half-warp owns one 1x128 tile (16 lanes x 8 BF16);
+// each thread keeps U tiles in flight to cover HBM latency.
+// ---------------------------------------------------------------------------
+template <int FMT, int U>
+__global__ void __launch_bounds__(256) k_quant_1x128_rows(const uint16_t *__restrict__ x, uint32_t rows,
+                                                          uint32_t ncb, int64_t ldx, uint8_t *__restrict__ q,
+                                                          float *__restrict__ s, int *status)
+{
+    const int l16 = threadIdx.x & 15;
+    const uint32_t hw0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+    const uint32_t nhw = (gridDim.x * blockDim.x) >> 4;
+    const uint32_t ntiles = rows * ncb;
+    const int64_t cols = (int64_t)ncb * 128;
+    // both half-warps of a warp share the loop test (shuffles below use the full mask)
+    for (uint32_t base = hw0; (base & ~1u) < ntiles; base += nhw * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t t = base + u * nhw;
+            if (t < ntiles) {
+                const uint32_t r = t / ncb, cb = t - r * ncb;
+                v[u] = ldg_stream(x + (int64_t)r * ldx + (int64_t)cb * 128 + l16 * 8);
+            } else {
+                v[u] = make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t t = base + u * nhw;
+            uint32_t m = absmax8(v[u]);
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            if (t < ntiles) {
+                const uint32_t r = t / ncb, cb = t - r * ncb;
+                if (m >= 0x7F80u && l16 == 0) set_status(status, FP8_ERR_NONFINITE);
+                const float sc = scale_from_amax_bits(m, FMT);
+                const Divider d(sc);
+                *reinterpret_cast<uint2 *>(q + (int64_t)r * cols + (int64_t)cb * 128 + l16 * 8) = quant8<FMT>(v[u], d);
+                if (l16 == 0) s[(int64_t)cb * rows + r] = sc;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Fused 1x128 + transposed 128x1.  One CTA per 128x128 tile of x:
+//  1. each thread loads 8 rows x 8 columns (16 B per row) -- one HBM read;
+//  2. row scales by half-warp shuffles, row codes stored straight from
+//     registers; the raw tile is kept in shared memory (16-B chunks XOR-
+//     swizzled by row so both the row stores and the 4x4 column reads are
+//     bank-conflict free);
+//  3. column amax over the 128 rows (registers -> shuffle -> shared), the
+//     128 column scales and their reciprocals;
+//  4. each thread quantizes 4x4 sub-blocks with the column scales and writes
+//     4 words of the transposed codes (32-byte segments per 8 lanes).
+// ---------------------------------------------------------------------------
+struct ColDiv {
+    float s, r;
+    int fast;
+};
+
+template <int FMT>
+__device__ __forceinline__ float div_col(float x, const ColDiv &c)
+{
+    if (c.fast) {
+        float q0 = __fmul_rn(x, c.r);
+        float e = __fmaf_rn(-q0, c.s, x);
+        float qv = __fmaf_rn(e, c.r, q0);
+        return __uint_as_float(__float_as_uint(qv) | (__float_as_uint(x) & 0x80000000u));
+    }
+    return __fdiv_rn(x, c.s);
+}
+
+constexpr int kFusedSmem = 32768 + 4096 + 128 * sizeof(ColDiv);
+
+template <int FMT>
+__global__ void __launch_bounds__(256) k_quant_1x128_fused_t(const uint16_t *__restrict__ x, int64_t rows,
+                                                             int64_t cols, int64_t ldx, uint8_t *__restrict__ q,
+                                                             float *__restrict__ s, uint8_t *__restrict__ qT,
+                                                             float *__restrict__ sT, int *status)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t *tile = smem;                                        // [128][256 B], swizzled 16-B chunks
+    uint32_t *colpart = reinterpret_cast<uint32_t *>(smem + 32768);  // [8 warps][128]
+    ColDiv *cdiv = reinterpret_cast<ColDiv *>(smem + 32768 + 4096);  // [128]
+
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int g = t & 15, rr = t >> 4;
+    const int64_t cb = blockIdx.x, mb = blockIdx.y;
+    const int64_t r0 = mb * 128, c0 = cb * 128;
+
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = ldg_stream(x + (r0 + rr + 16 * i) * ldx + c0 + g * 8);
+
+    uint32_t cm0 = 0, cm1 = 0, cm2 = 0, cm3 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = rr + 16 * i;
+        uint32_t m = absmax8(v[i]);
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        if (m >= 0x7F80u && g == 0) set_status(status, FP8_ERR_NONFINITE);
+        const float sc = scale_from_amax_bits(m, FMT);
+        const Divider d(sc);
+        *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = quant8<FMT>(v[i], d);
+        if (g == 0) s[cb * rows + r0 + row] = sc;
+        *reinterpret_cast<uint4 *>(tile + row * 256 + ((g ^ ((row >> 2) & 7)) << 4)) = v[i];
+        cm0 = bf16x2_absmax(cm0, bf16x2_abs(v[i].x));
+        cm1 = bf16x2_absmax(cm1, bf16x2_abs(v[i].y));
+        cm2 = bf16x2_absmax(cm2, bf16x2_abs(v[i].z));
+        cm3 = bf16x2_absmax(cm3, bf16x2_abs(v[i].w));
+    }
+    // lanes l and l^16 hold rows rr and rr+1 of the same columns
+    cm0 = bf16x2_absmax(cm0, __shfl_xor_sync(0xffffffffu, cm0, 16));
+    cm1 = bf16x2_absmax(cm1, __shfl_xor_sync(0xffffffffu, cm1, 16));
+    cm2 = bf16x2_absmax(cm2, __shfl_xor_sync(0xffffffffu, cm2, 16));
+    cm3 = bf16x2_absmax(cm3, __shfl_xor_sync(0xffffffffu, cm3, 16));
+    if (lane < 16) {
+        uint32_t *p = colpart + warp * 128 + g * 8;
+        p[0] = cm0 & 0xFFFFu; p[1] = cm0 >> 16;
+        p[2] = cm1 & 0xFFFFu; p[3] = cm1 >> 16;
+        p[4] = cm2 & 0xFFFFu; p[5] = cm2 >> 16;
+        p[6] = cm3 & 0xFFFFu; p[7] = cm3 >> 16;
+    }
+    __syncthreads();
+    if (t < 128) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) m = max(m, colpart[w * 128 + t]);
+        if (m >= 0x7F80u) set_status(status, FP8_ERR_NONFINITE);
+        const float sc = scale_from_amax_bits(m, FMT);
+        ColDiv c;
+        c.s = sc;
+        c.fast = (sc >= 0x1p-125f) && (sc <= 0x1p125f);
+        c.r = c.fast ? __frcp_rn(sc) : 0.0f;
+        cdiv[t] = c;
+        sT[mb * cols + c0 + t] = sc;
+    }
+    __syncthreads();
+
+    const int cw = (lane >> 3) + 4 * warp;   // 4 columns 4cw .. 4cw+3
+    const ColDiv d0 = cdiv[4 * cw], d1 = cdiv[4 * cw + 1], d2 = cdiv[4 * cw + 2], d3 = cdiv[4 * cw + 3];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int mg = (lane & 7) + 8 * k;   // rows 4mg .. 4mg+3
+        uint32_t o0 = 0, o1 = 0, o2 = 0, o3 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = 4 * mg + i;
+            const uint2 pr = *reinterpret_cast<const uint2 *>(
+                tile + row * 256 + (((cw >> 1) ^ ((row >> 2) & 7)) << 4) + ((cw & 1) << 3));
+            const uint32_t c01 = cvt2<FMT>(div_col<FMT>(bf16_lo(pr.x), d0), div_col<FMT>(bf16_hi(pr.x), d1));
+            const uint32_t c23 = cvt2<FMT>(div_col<FMT>(bf16_lo(pr.y), d2), div_col<FMT>(bf16_hi(pr.y), d3));
+            o0 |= (c01 & 0xFFu) << (8 * i);
+            o1 |= (c01 >> 8) << (8 * i);
+            o2 |= (c23 & 0xFFu) << (8 * i);
+            o3 |= (c23 >> 8) << (8 * i);
+        }
+        uint8_t *dst = qT + (c0 + 4 * cw) * rows + r0 + 4 * mg;
+        *reinterpret_cast<uint32_t *>(dst) = o0;
+        *reinterpret_cast<uint32_t *>(dst + rows) = o1;
+        *reinterpret_cast<uint32_t *>(dst + 2 * rows) = o2;
+        *reinterpret_cast<uint32_t *>(dst + 3 * rows) = o3;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Transposed write of a 128x128 tile of codes held in shared memory as
+// [128 rows][33 words] (one pad word per row): each thread byte-transposes
+// 4x4 sub-blocks and stores 4 words of the transposed tile.  Lane mapping
+// (mg = lane & 7, cw = lane >> 3) keeps the shared reads conflict free and
+// gives full 32-byte segments on the global stores.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void store_code_tile_transposed(const uint32_t *ct, uint8_t *qT, int64_t ldT,
+                                                           int64_t c0, int64_t r0)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cw = (lane >> 3) + 4 * warp;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int mg = (lane & 7) + 8 * k;
+        const uint32_t w0 = ct[(4 * mg + 0) * 33 + cw];
+        const uint32_t w1 = ct[(4 * mg + 1) * 33 + cw];
+        const uint32_t w2 = ct[(4 * mg + 2) * 33 + cw];
+        const uint32_t w3 = ct[(4 * mg + 3) * 33 + cw];
+        const uint32_t t0 = __byte_perm(w0, w1, 0x5140), t1 = __byte_perm(w2, w3, 0x5140);
+        const uint32_t t2 = __byte_perm(w0, w1, 0x7362), t3 = __byte_perm(w2, w3, 0x7362);
+        uint8_t *dst = qT + (c0 + 4 * cw) * ldT + r0 + 4 * mg;
+        *reinterpret_cast<uint32_t *>(dst) = __byte_perm(t0, t1, 0x5410);
+        *reinterpret_cast<uint32_t *>(dst + ldT) = __byte_perm(t0, t1, 0x7632);
+        *reinterpret_cast<uint32_t *>(dst + 2 * ldT) = __byte_perm(t2, t3, 0x5410);
+        *reinterpret_cast<uint32_t *>(dst + 3 * ldT) = __byte_perm(t2, t3, 0x7632);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 128x128 blocks: one CTA per block, 8 rows x 16 B per thread, block amax by
+// shuffles + shared, codes stored from registers; optionally the codes are
+// staged in shared memory and written transposed too.
+// ---------------------------------------------------------------------------
+template <int FMT, bool TRANS>
+__global__ void __launch_bounds__(256) k_quant_128x128(const uint16_t *__restrict__ w, int64_t rows, int64_t cols,
+                                                       int64_t ldw, uint8_t *__restrict__ q, float *__restrict__ s,
+                                                       uint8_t *__restrict__ qT, float *__restrict__ sT, int *status)
+{
+    __shared__ uint32_t red[8];
+    __shared__ uint32_t ct[TRANS ? 128 * 33 : 1];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int g = t & 15, rr = t >> 4;
+    const int64_t cb = blockIdx.x, rb = blockIdx.y;
+    const int64_t r0 = rb * 128, c0 = cb * 128;
+
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = ldg_stream(w + (r0 + rr + 16 * i) * ldw + c0 + g * 8);
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = max(m, absmax8(v[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = max(m, red[i]);
+    if (m >= 0x7F80u && t == 0) set_status(status, FP8_ERR_NONFINITE);
+    const float sc = scale_from_amax_bits(m, FMT);
+    const Divider d(sc);
+    const int64_t ncb = cols / 128, nrb = rows / 128;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = rr + 16 * i;
+        const uint2 c = quant8<FMT>(v[i], d);
+        *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = c;
+        if (TRANS) {
+            ct[row * 33 + 2 * g] = c.x;
+            ct[row * 33 + 2 * g + 1] = c.y;
+        }
+    }
+    if (t == 0) {
+        s[rb * ncb + cb] = sc;
+        if (TRANS) sT[cb * nrb + rb] = sc;
+    }
+    if (TRANS) {
+        __syncthreads();
+        store_code_tile_transposed(ct, qT, rows, c0, r0);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// On-demand FP8 transpose of a 128x128-block-quantized weight.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_transpose_128x128(const uint8_t *__restrict__ q, const float *__restrict__ s,
+                                                           int64_t rows, int64_t cols, uint8_t *__restrict__ qT,
+                                                           float *__restrict__ sT)
+{
+    __shared__ uint32_t ct[128 * 33];
+    const int t = threadIdx.x;
+    const int64_t cb = blockIdx.x, rb = blockIdx.y;
+    const int64_t r0 = rb * 128, c0 = cb * 128;
+    // 128 rows x 8 chunks of 16 B: 4 chunks per thread
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int idx = t + 256 * k;
+        const int row = idx >> 3, ch = idx & 7;
+        const uint4 v = ldg_stream(q + (r0 + row) * cols + c0 + ch * 16);
+        uint32_t *p = ct + row * 33 + ch * 4;
+        p[0] = v.x; p[1] = v.y; p[2] = v.z; p[3] = v.w;
+    }
+    if (t == 0) sT[cb * (rows / 128) + rb] = s[rb * (cols / 128) + cb];
+    __syncthreads();
+    store_code_tile_transposed(ct, qT, rows, c0, r0);
+}
+
+// ------------------------------------------------------------------ launchers
+
+static int check_launch()
+{
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+template <int FMT>
+static int quant_1x128_fmt(const void *x, int64_t rows, int64_t cols, int64_t ldx, void *q, float *s, void *qT,
+                           float *sT, int *status, cudaStream_t st)
+{
+    if (qT) {
+        static bool attr_done[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (!attr_done[dev & 63]) {
+            if (cudaFuncSetAttribute(k_quant_1x128_fused_t<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kFusedSmem) != cudaSuccess)
+                return FP8_ERR_CUDA;
+            attr_done[dev & 63] = true;
+        }
+        dim3 grid((unsigned)(cols / 128), (unsigned)(rows / 128));
+        k_quant_1x128_fused_t<FMT><<<grid, 256, kFusedSmem, st>>>(
+            static_cast<const uint16_t *>(x), rows, cols, ldx, static_cast<uint8_t *>(q), s,
+            static_cast<uint8_t *>(qT), sT, status);
+        return check_launch();
+    }
+    constexpr int U = 4;
+    const int64_t ntiles = rows * (cols / 128);
+    int64_t blocks = (ntiles + 16 * U - 1) / (16 * U);
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    k_quant_1x128_rows<FMT, U><<<(unsigned)blocks, 256, 0, st>>>(
+        static_cast<const uint16_t *>(x), (uint32_t)rows, (uint32_t)(cols / 128), ldx, static_cast<uint8_t *>(q), s,
+        status);
+    return check_launch();
+}
+
+int launch_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, void *q, float *s,
+                       void *qT, float *sT, int *status, cudaStream_t st)
+{
+    if (rows == 0 || cols == 0) return FP8_OK;
+    return fmt == FP8_E5M2 ? quant_1x128_fmt<FP8_E5M2>(x, rows, cols, ldx, q, s, qT, sT, status, st)
+                           : quant_1x128_fmt<FP8_E4M3>(x, rows, cols, ldx, q, s, qT, sT, status, st);
+}
+
+int launch_quant_128x128(const void *w, int64_t rows, int64_t cols, int64_t ldw, int fmt, void *q, float *s,
+                         void *qT, float *sT, int *status, cudaStream_t st)
+{
+    if (rows == 0 || cols == 0) return FP8_OK;
+    dim3 grid((unsigned)(cols / 128), (unsigned)(rows / 128));
+    auto W = static_cast<const uint16_t *>(w);
+    auto Q = static_cast<uint8_t *>(q);
+    auto QT = static_cast<uint8_t *>(qT);
+    if (fmt == FP8_E5M2) {
+        if (qT) k_quant_128x128<FP8_E5M2, true><<<grid, 256, 0, st>>>(W, rows, cols, ldw, Q, s, QT, sT, status);
+        else k_quant_128x128<FP8_E5M2, false><<<grid, 256, 0, st>>>(W, rows, cols, ldw, Q, s, QT, sT, status);
+    } else {
+        if (qT) k_quant_128x128<FP8_E4M3, true><<<grid, 256, 0, st>>>(W, rows, cols, ldw, Q, s, QT, sT, status);
+        else k_quant_128x128<FP8_E4M3, false><<<grid, 256, 0, st>>>(W, rows, cols, ldw, Q, s, QT, sT, status);
+    }
+    return check_launch();
+}
+
+int launch_transpose_128x128(const void *q, const float *s, int64_t rows, int64_t cols, void *qT, float *sT,
+                             cudaStream_t st)
+{
+    if (rows == 0 || cols == 0) return FP8_OK;
+    dim3 grid((unsigned)(cols / 128), (unsigned)(rows / 128));
+    k_transpose_128x128<<<grid, 256, 0, st>>>(static_cast<const uint8_t *>(q), s, rows, cols,
+                                              static_cast<uint8_t *>(qT), sT);
+    return check_launch();
+}
+
+}  // namespace fp8fg

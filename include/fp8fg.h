@@ -1,0 +1,273 @@
+/*
+ * fp8fg.h -- C ABI of the fine-grained FP8 Linear library for GB300 (sm_103a).
+ *
+ * The library quantizes BF16 tensors to FP8 with one FP32 scale per 1x128
+ * activation/gradient tile or per 128x128 weight block, multiplies the FP8
+ * operands on the tcgen05 tensor cores while applying the per-128-K-chunk
+ * scales to FP32 partial sums, and provides the coarse per-tensor delayed-
+ * scaling variant with its underflow/distortion monitors, the MoE grouped
+ * variant over a 128-padded routing map, and the SwiGLU glue between the two
+ * MLP GEMMs.
+ *
+ * Sources, cited by page title and section:
+ *   [FP8-LM] "FP8-LM: Training FP8 Large Language Models" (paper review),
+ *            "Core formulas": FP8 formats, tensor scaling x_fp8 = Cast(x / s).
+ *   [Ling]   Ling 2.0 FP8 pretraining blog: "Where does the error come from?",
+ *            "Fine-grained quantization (per-tile/block wise scaling)", the
+ *            underflow/distortion monitor table, "FP8 on-demand transpose
+ *            weight", "FP8 padding routing map".
+ *   [FP8-RL] FP8-RL article, "Core breakthrough: dynamic weight sync"
+ *            (128x128 weight blocks, E4M3 in [-448, 448], dynamic activations),
+ *            and its MoE expert layers.
+ *   [Infra]  "FP8 training infrastructure" guide, "Transformer Engine" and
+ *            "Scaling strategies" (delayed scaling, amax history, HYBRID).
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates nothing.  Its only state is one device status word
+ *     per GPU (see fp8_device_status).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream) and returns a status code.  A non-OK
+ *     return means nothing was launched; outputs are then unspecified.
+ *   - Matrices are row-major.  BF16 inputs are given as raw 16-bit patterns.
+ *   - FP8 tensors are byte arrays of E4M3 or E5M2 codes (fp8_format_t).
+ *   - Scale layouts (FP32):
+ *       1x128   tensor [R][C] quantized along C: S[C/128][R]  (chunk-major)
+ *       128x1   the transposed copy [C][R] of a tensor [R][C], quantized
+ *               along R: S[R/128][C]   (this IS the 1x128 layout of [C][R])
+ *       128x128 tensor [R][C]: S[R/128][C/128]
+ *       TENSOR  one FP32 value
+ *   - Pointers to FP8/BF16 data and to scale arrays must be 16-byte aligned;
+ *     leading dimensions are in elements and must keep rows 16-byte aligned.
+ *   - Errors found on the device (non-finite amax, bounded-wait timeout, bad
+ *     group offsets) are recorded in the device status word and read with
+ *     fp8_device_status().
+ */
+#ifndef FP8FG_H
+#define FP8FG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8FG_API __attribute__((visibility("default")))
+
+#define FP8FG_ABI_VERSION 1
+
+/* Status codes. */
+enum {
+    FP8_OK = 0,
+    FP8_ERR_INVALID_ARG = 1, /* null pointer, bad enum, bad count, device: bad group offsets */
+    FP8_ERR_SHAPE = 2,       /* a dimension is not a required multiple (128, 256) or < 0 */
+    FP8_ERR_ALIGNMENT = 3,   /* pointer or leading dimension not 16-byte aligned */
+    FP8_ERR_UNSUPPORTED = 4, /* format / granularity combination not provided */
+    FP8_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, attribute, query) */
+    FP8_ERR_NONFINITE = 6,   /* device: a scaling group held Inf or NaN */
+    FP8_ERR_TIMEOUT = 7      /* device: a bounded pipeline wait gave up (about 1 s) */
+};
+
+typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format_t;
+
+typedef enum {
+    FP8_GRAN_1x128 = 0,
+    FP8_GRAN_128x128 = 1,
+    FP8_GRAN_TENSOR = 2,
+    FP8_GRAN_128x1 = 3
+} fp8_gran_t;
+
+typedef enum { FP8_OUT_BF16 = 0, FP8_OUT_F32 = 1 } fp8_out_dtype_t;
+
+typedef enum { FP8_AMAX_MAX = 0, FP8_AMAX_MOST_RECENT = 1 } fp8_amax_algo_t;
+
+/* Monitors ([Ling] "Where does the error come from?" and its monitor table).
+ * Device-resident, ACCUMULATED by every call that is given one: zero it first.
+ *   nonzero      #(x != 0)
+ *   underflow    #(x != 0 and q is +0 or -0)        (smaller is better)
+ *   saturated    #(|fp32(x) / s| > fmax)
+ *   distinct_in  sum over scaling groups of #distinct x values (+-0 as one)
+ *   distinct_out sum over scaling groups of #distinct codes   (+-0 as one)
+ * Underflow ratio = underflow / nonzero; distortion is reported as the
+ * retention ratio distinct_out / distinct_in (larger is better). */
+typedef struct {
+    uint64_t nonzero;
+    uint64_t underflow;
+    uint64_t saturated;
+    uint64_t distinct_in;
+    uint64_t distinct_out;
+} fp8_stats_t;
+
+/* Delayed-scaling recipe ([Infra] "Transformer Engine": margin, fp8 format,
+ * amax_history_len, amax_compute_algo).  HYBRID = E4M3 for forward tensors,
+ * E5M2 for gradients: the caller picks `fmt` per tensor. */
+typedef struct {
+    int32_t fmt;         /* fp8_format_t */
+    int32_t history_len; /* 1 .. 1024 */
+    int32_t margin;      /* s = amax * 2^margin / fmax, -126 .. 126 */
+    int32_t algo;        /* fp8_amax_algo_t */
+} fp8_delayed_recipe_t;
+
+/* ---------------------------------------------------------------- utility */
+
+FP8FG_API int fp8_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+FP8FG_API const char *fp8_status_string(int status);
+
+/* Synchronizes `stream`, copies the current device's status word to *out and
+ * clears it.  Returns FP8_ERR_CUDA if the synchronize or copy fails. */
+FP8FG_API int fp8_device_status(void *stream, int *out);
+
+/* Self-test of the bounded wait used by every pipeline wait: launches one
+ * block that waits on a barrier nothing arrives at, for `timeout_ms`
+ * milliseconds (1 .. 2000), after which it records FP8_ERR_TIMEOUT in the
+ * device status word and returns.  The CUDA context stays usable. */
+FP8FG_API int fp8_selftest_wait_timeout(int timeout_ms, void *stream);
+
+/* ----------------------------------------------------------- quantizers */
+
+/* 1x128 quantization of activations / gradients ([Ling] "Fine-grained
+ * quantization"; [FP8-RL]: activations are quantized dynamically each call;
+ * [FP8-LM] "Tensor scaling").  For every row r and column chunk cb:
+ *   amax = max_k |x[r][cb*128+k]|,  s = fp32(amax / fmax) (1 if amax == 0),
+ *   q[r][c] = RNE_satfinite(fp32(x[r][c]) / s)   (IEEE binary32 division).
+ * x:  BF16 [rows][ldx], rows >= 0, cols % 128 == 0, ldx >= cols, ldx % 8 == 0.
+ * q:  [rows][cols] codes.   s: S[cols/128][rows].
+ * qT, sT (both NULL or both set; then rows % 128 == 0): the wgrad operand
+ *   ("grad (transpose)" in [Ling]'s monitor table) from the same read of x:
+ *   qT[c][m] = RNE_satfinite(x[m][c] / sT[m/128][c]) with sT = the per-column
+ *   amax over each 128 rows / fmax; qT is [cols][rows], sT is S[rows/128][cols].
+ * A group holding Inf/NaN records FP8_ERR_NONFINITE (its outputs unspecified). */
+FP8FG_API int fp8_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                              void *q, float *s, void *qT, float *sT, void *stream);
+
+/* 128x128 weight-block quantization ([FP8-RL] "dynamic weight sync": each
+ * 128x128 block of a weight gets its own scale).
+ * w: BF16 [rows][ldw], rows % 128 == 0, cols % 128 == 0.  q: [rows][cols],
+ * s: S[rows/128][cols/128].  Optional qT ([cols][rows]) and sT
+ * (S[cols/128][rows/128]) receive the transposed weight in the same pass:
+ * block quantization commutes with transposition, so qT is exactly q^T. */
+FP8FG_API int fp8_quant_128x128(const void *w, int64_t rows, int64_t cols, int64_t ldw, int fmt,
+                                void *q, float *s, void *qT, float *sT, void *stream);
+
+/* On-demand FP8 transpose of a 128x128-block-quantized weight ([Ling] "FP8
+ * on-demand transpose weight": no cached W^T, a fast transpose when dgrad
+ * needs it).  q [rows][cols] -> qT [cols][rows] byte-exact; s
+ * S[rows/128][cols/128] -> sT S[cols/128][rows/128].  rows, cols % 128 == 0. */
+FP8FG_API int fp8_transpose_128x128(const void *q, const float *s, int64_t rows, int64_t cols,
+                                    void *qT, float *sT, void *stream);
+
+/* Bytes of the caller-owned workspace used by fp8_quant_pertensor_delayed and
+ * by fp8_quant_stats(FP8_GRAN_TENSOR).  Zero it once (cudaMemset) before the
+ * first use; every call that completes leaves it zeroed again. */
+FP8FG_API size_t fp8_pertensor_workspace_bytes(void);
+
+/* Per-tensor delayed scaling, one training step ([Infra] "Transformer
+ * Engine" DelayedScaling and "Scaling strategies": the scale comes from the
+ * amax seen in earlier iterations).  State is caller-owned device memory:
+ *   amax_history[recipe->history_len], *step (starts at 0), *scale (s_t,
+ *   start it at 1).
+ * The call quantizes q = RNE_satfinite(x / s_t), writes this step's amax to
+ * amax_history[step % L], sets *scale = s_{t+1} = m * 2^margin / fmax with
+ * m = max(history) (or this step's amax for FP8_AMAX_MOST_RECENT; unchanged
+ * if m == 0) and increments *step -- all on the device, no host round trip.
+ * x: BF16 [rows][ldx], cols % 16 == 0.  q: [rows][cols].  qT (optional, then
+ * rows % 128 == 0 and cols % 128 == 0): [cols][rows] = q^T for the wgrad
+ * operand.  stats (optional): monitors with the whole tensor as one group.
+ * workspace: fp8_pertensor_workspace_bytes() bytes, see above.  Calls that
+ * share one workspace must not overlap on the GPU. */
+FP8FG_API int fp8_quant_pertensor_delayed(const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                                          const fp8_delayed_recipe_t *recipe, float *amax_history,
+                                          int32_t *step, float *scale, void *q, void *qT,
+                                          fp8_stats_t *stats, void *workspace, void *stream);
+
+/* Monitors of an existing quantization ([Ling] underflow / distortion
+ * monitors), accumulated into *stats.  x: BF16 [rows][ldx]; q and s follow
+ * `gran` (1x128, 128x128, TENSOR: q is [rows][cols]; 128x1: q is the
+ * transposed copy [cols][rows] with S[rows/128][cols]).  `workspace` is
+ * needed for FP8_GRAN_TENSOR only (same contract as above). */
+FP8FG_API int fp8_quant_stats(const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                              const void *q, const float *s, int gran, int fmt,
+                              fp8_stats_t *stats, void *workspace, void *stream);
+
+/* ---------------------------------------------------------------- GEMMs */
+
+/* Block-scaled FP8 GEMM, D = A . B^T ([Ling]: FP8 GEMM with an FP32
+ * accumulator; fine-grained tile/block scales):
+ *   D[m][n] = sum_kb sA(m,kb) * sB(n,kb) * sum_{k in chunk kb} qA[m][k]*qB[n][k]
+ * with each 128-deep chunk accumulated on the tensor cores and promoted to an
+ * FP32 running sum with its two scales.  For granA == granB == TENSOR the
+ * whole K is accumulated on the tensor cores and sA*sB applied once.
+ *   A [M][K] codes (fmtA), B [N][K] codes (fmtB), K contiguous in both.
+ *   granA in {1x128 (S[K/128][M]), 128x128 (S[M/128][K/128]), TENSOR};
+ *   granB in {1x128 (S[K/128][N]), 128x128 (S[N/128][K/128]), TENSOR};
+ *   TENSOR must be used on both sides or neither.
+ *   fmtA/fmtB: E4M3 or E5M2, mixed allowed (HYBRID dgrad/wgrad).
+ *   D [M][ldD], BF16 (round to nearest even) or FP32.
+ * M % 128 == 0, N % 128 == 0, K % 128 == 0; M, N, K >= 0 (0 = no-op). */
+FP8FG_API int fp8_blockscaled_gemm(int64_t M, int64_t N, int64_t K,
+                                   const void *A, int fmtA, const float *sA, int granA,
+                                   const void *B, int fmtB, const float *sB, int granB,
+                                   void *D, int out_dtype, int64_t ldD, void *stream);
+
+/* Grouped MoE expert GEMM ([FP8-RL]: FP8 on the MoE expert layers; [Ling]
+ * "FP8 padding routing map": every expert's row count is a multiple of 128).
+ * Rows [off[g], off[g+1]) of A use expert g's weights:
+ *   D[m][n] = the block-scaled GEMM of A's row m with B[g] (128x128 scales).
+ * group_offsets: DEVICE int32[G+1], 0 = off[0] <= ... <= off[G] <= M_capacity,
+ *   each a multiple of 128 (checked on the device: FP8_ERR_INVALID_ARG).
+ * A [M_capacity][K] E4M3 with 1x128 scales S[K/128][M_capacity];
+ * B [G][N][K] E4M3 with scales [G][N/128][K/128]; D [M_capacity][ldD]
+ * (rows >= off[G] are not written).  N % 128 == 0, K % 128 == 0,
+ * M_capacity % 128 == 0, 1 <= G <= 1024. */
+FP8FG_API int fp8_grouped_gemm(int G, const int32_t *group_offsets, int64_t M_capacity,
+                               int64_t N, int64_t K, const void *A, const float *sA,
+                               const void *B, const float *sB, void *D, int out_dtype,
+                               int64_t ldD, void *stream);
+
+/* -------------------------------------------------------------- MoE glue */
+
+/* Router + padded routing map ([Ling] "FP8 padding routing map").
+ * logits: FP32 [T][E] (E <= 256).  For each token: softmax in FP32 and the
+ * top-k experts by logit (softmax is monotone), ties to the lower index:
+ * topk_idx [T][topk], topk_prob [T][topk].  counts[E] = tokens routed to
+ * each expert.  The routing map is then edited so that each expert's row
+ * count is counts rounded up to a multiple of `align`: the added entries are
+ * the lowest-index tokens not already routed to that expert, with router
+ * probability 0 (so the result is unchanged).  Rows of expert e occupy
+ * [group_offsets[e], group_offsets[e+1]) in ascending token order:
+ * row_token[r] = token, row_prob[r] = its probability (0 for padding),
+ * row_is_pad[r] (optional) = 1 for padding.  Rows from group_offsets[E] to
+ * M_capacity get row_token = -1, row_prob = 0.  The total must fit
+ * M_capacity (else FP8_ERR_INVALID_ARG on the device); T*topk + E*(align-1)
+ * always fits.  1 <= topk <= min(E, 8), align in {1..1024}. */
+FP8FG_API int fp8_moe_route_pad(const float *logits, int64_t T, int E, int topk, int align,
+                                int64_t M_capacity, int32_t *topk_idx, float *topk_prob,
+                                int32_t *counts, int32_t *group_offsets, int32_t *row_token,
+                                float *row_prob, uint8_t *row_is_pad, void *stream);
+
+/* Dispatch: gather the FP8 rows and 1x128 scales of the routed tokens.
+ * Quantizing once before the gather is exact: 1x128 scales are per row.
+ * q [T][K], s S[K/128][T] -> qg [M_capacity][K], sg S[K/128][M_capacity] for
+ * rows r < group_offsets[E] (read on the device); other rows untouched. */
+FP8FG_API int fp8_moe_gather(const void *q, const float *s, int64_t T, int64_t K,
+                             const int32_t *row_token, const int32_t *group_offsets, int E,
+                             int64_t M_capacity, void *qg, float *sg, void *stream);
+
+/* SwiGLU between the up and down projections (glue, FP32 math, BF16 out):
+ * gu [rows][2F] holds gate in columns [0, F) and up in [F, 2F);
+ * h[r][j] = silu(g) * u.   F % 8 == 0. */
+FP8FG_API int fp8_swiglu_fwd(const void *gu, int64_t rows, int64_t F, void *h, void *stream);
+
+/* Backward of the above: dgu[r][j] = dh*u*sig(g)*(1 + g*(1 - sig(g))),
+ * dgu[r][F+j] = dh*silu(g). */
+FP8FG_API int fp8_swiglu_bwd(const void *gu, const void *dh, int64_t rows, int64_t F, void *dgu,
+                             void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8FG_H */
