@@ -144,7 +144,7 @@ def run_reference(args):
 class Clocks:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -152,10 +152,13 @@ class Clocks:
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
                  "-i", gpu_id], stdout=self.file, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
 
     def stop(self):
         if self.proc is None:
@@ -167,18 +170,28 @@ class Clocks:
             self.proc.kill()
         self.file.flush()
         self.file.seek(0)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+        rows = []
         for line in self.file.read().splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+        t0, t1 = getattr(self, "start", None), getattr(self, "end", None)
+        inside = [r for r in rows if t0 is not None and t1 is not None and t0 - 0.06 <= r[0] <= t1 + 0.06]
+        if not inside and rows and t0 is not None:
+            mid = 0.5 * (t0 + (t1 or t0))
+            inside = sorted(rows, key=lambda r: abs(r[0] - mid))[:3]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, c, m, flags in inside:
+            sm.append(c)
+            mx.append(m)
+            for n, v in zip(names, flags):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         os.unlink(self.file.name)
@@ -293,10 +306,10 @@ class RowBench:
         self.dev, self.pk = dev, pk
         self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    def time(self, fn, iters=8):
+    def time(self, fn):
         import torch
         evs = []
-        for i in range(iters + 2):
+        for i in range(self.iters + 2):
             self.flush_buf.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
@@ -319,11 +332,14 @@ class RowBench:
         return name, {"time_us": t * 1e6, "achieved": tf, "unit": "TFLOP/s", "peak": peak, "frac": tf / peak,
                       "flops": flops, "bound": "tensor", "note": note}
 
-    def run_all(self):
+    def run_all(self, only=None, iters=8):
+        """Measure every row (or only the row whose name starts with `only`)."""
         import torch
 
         import fp8_fine_grained_x128_gb300 as fg
         import synth
+        self.iters = iters
+        want = lambda name: only is None or name.startswith(only) or only.startswith(name)
         dev = self.dev
         out = {}
         u8 = lambda *s: torch.empty(s, dtype=torch.uint8, device=dev)
@@ -331,115 +347,125 @@ class RowBench:
         bf = lambda *s: torch.empty(s, dtype=torch.bfloat16, device=dev)
         E = fg.E4M3
 
-        # a1: 1x128 rows, X [8192, 4096]
+        def put(kv):
+            out[kv[0]] = kv[1]
+
         R, C = 8192, 4096
-        X = _bf16_dev(synth.bf16_normal((R, C), 0, 1.0, 1e-3, 50.0), dev)
-        q, s, qT, sT = u8(R, C), f32(C // 128, R), u8(C, R), f32(R // 128, C)
-        k, v = self.hbm("a1_quant_1x128", lambda: fg.quant_1x128(X, E, q, s), 3 * R * C + R * C // 32, "X 8192x4096")
-        out[k] = v
-        # a2: fused 1x128 + 128x1, dGU-shaped [8192, 28672]
-        R2, C2 = 8192, 28672
-        G = _bf16_dev(synth.bf16_normal((R2, C2), 5, 1e-3), dev)
-        q2, s2, qT2, sT2 = u8(R2, C2), f32(C2 // 128, R2), u8(C2, R2), f32(R2 // 128, C2)
-        k, v = self.hbm("a2_quant_1x128_fused_128x1", lambda: fg.quant_1x128(G, E, q2, s2, qT2, sT2),
-                        4 * R2 * C2 + R2 * C2 // 16, "dGU 8192x28672")
-        out[k] = v
-        del q2, qT2
-        # a3: 128x128, W_gu [28672, 4096]; with the fused transposed copy; a4 on-demand transpose
-        W = _bf16_dev(synth.bf16_normal((28672, 4096), 1000, 0.02), dev)
-        qw, sw, qwT, swT = u8(28672, 4096), f32(224, 32), u8(4096, 28672), f32(32, 224)
+        if want("a1") or want("a5") or want("a8"):
+            X = _bf16_dev(synth.bf16_normal((R, C), 0, 1.0, 1e-3, 50.0), dev)
+            q, s = u8(R, C), f32(C // 128, R)
+            fg.quant_1x128(X, E, q, s)
+        if want("a1"):
+            put(self.hbm("a1_quant_1x128", lambda: fg.quant_1x128(X, E, q, s), 3 * R * C + R * C // 32,
+                         "X 8192x4096"))
+        if want("a2"):
+            R2, C2 = 8192, 28672
+            G = _bf16_dev(synth.bf16_normal((R2, C2), 5, 1e-3), dev)
+            q2, s2, qT2, sT2 = u8(R2, C2), f32(C2 // 128, R2), u8(C2, R2), f32(R2 // 128, C2)
+            put(self.hbm("a2_quant_1x128_fused_128x1", lambda: fg.quant_1x128(G, E, q2, s2, qT2, sT2),
+                         4 * R2 * C2 + R2 * C2 // 16, "dGU 8192x28672"))
+            del G, q2, s2, qT2, sT2
         n = 28672 * 4096
-        k, v = self.hbm("a3_quant_128x128", lambda: fg.quant_128x128(W, E, qw, sw), 3 * n, "W_gu 28672x4096")
-        out[k] = v
-        k, v = self.hbm("a3_quant_128x128_fused_T", lambda: fg.quant_128x128(W, E, qw, sw, qwT, swT), 4 * n,
-                        "W_gu 28672x4096, q and q^T in one pass")
-        out[k] = v
-        k, v = self.hbm("a4_fp8_transpose_on_demand", lambda: fg.transpose_128x128(qw, sw, qwT, swT), 2 * n,
-                        "FP8 W_gu^T")
-        out[k] = v
-        del W
-        # a5: block-scaled GEMMs (headline shape, wgrad shape)
-        D = bf(8192, 28672)
-        k, v = self.tensor("a5_gemm_fprop_8192x28672x4096", lambda: fg.blockscaled_gemm(
-            q, E, s, fg.GRAN_1x128, qw, E, sw, fg.GRAN_128x128, D), 2.0 * 8192 * 28672 * 4096, "1x128 x 128x128, BF16 out")
-        out[k] = v
-        D32 = f32(28672, 4096)
-        k, v = self.tensor("a5_gemm_wgrad_28672x4096x8192", lambda: fg.blockscaled_gemm(
-            qT2, E, sT2, fg.GRAN_1x128, qT, E, sT, fg.GRAN_1x128, D32) if False else fg.blockscaled_gemm(
-            u8(28672, 8192), E, f32(64, 28672).fill_(1.0), fg.GRAN_1x128, u8(4096, 8192), E,
-            f32(64, 4096).fill_(1.0), fg.GRAN_1x128, D32), 2.0 * 28672 * 4096 * 8192, "1x128 x 1x128, FP32 out")
-        out[k] = v
-        del D, D32
-        # a6 + a8: per-tensor delayed scaling with fused monitors, X [16384, 4096]
-        R6, C6 = 16384, 4096
-        X6 = _bf16_dev(synth.delayed_step_inputs(0)[0], dev)
-        rec = fg.DelayedRecipe(E, 16, 0, fg.AMAX_MAX)
-        hist, stepc, scale = torch.zeros(16, device=dev), torch.zeros(1, dtype=torch.int32, device=dev), torch.ones(1, device=dev)
-        ws, stats = fg.new_workspace(dev), fg.new_stats(dev)
-        q6, q6T = u8(R6, C6), u8(C6, R6)
-        k, v = self.hbm("a6_a8_delayed_pertensor_with_monitors_and_T", lambda: fg.quant_pertensor_delayed(
-            X6, rec, hist, stepc, scale, q6, ws, q6T, stats), 4 * R6 * C6, "X 16384x4096 E4M3, qT, monitors")
-        out[k] = v
-        k, v = self.hbm("a6_delayed_pertensor_plain", lambda: fg.quant_pertensor_delayed(
-            X6, rec, hist, stepc, scale, q6, ws), 3 * R6 * C6, "X 16384x4096 E4M3")
-        out[k] = v
-        # a8: fine-grained monitors (standalone)
-        k, v = self.hbm("a8_monitors_1x128", lambda: fg.quant_stats(X, q, s, fg.GRAN_1x128, E, stats),
-                        3 * R * C, "X 8192x4096 (distinct counts per 1x128 tile: ALU-bound)")
-        out[k] = v
-        # a7: per-tensor GEMMs (E4M3 x E4M3, E5M2 x E4M3)
-        W7 = u8(4096, 4096)
-        D7 = bf(16384, 4096)
-        one = torch.ones(1, device=dev)
-        k, v = self.tensor("a7_gemm_pertensor_16384x4096x4096", lambda: fg.blockscaled_gemm(
-            q6, E, one, fg.GRAN_TENSOR, W7, E, one, fg.GRAN_TENSOR, D7), 2.0 * 16384 * 4096 * 4096, "E4M3 x E4M3")
-        out[k] = v
-        k, v = self.tensor("a7_gemm_hybrid_e5m2_16384x4096x4096", lambda: fg.blockscaled_gemm(
-            q6, fg.E5M2, one, fg.GRAN_TENSOR, W7, E, one, fg.GRAN_TENSOR, D7), 2.0 * 16384 * 4096 * 4096, "E5M2 x E4M3")
-        out[k] = v
-        del X6, q6, q6T, D7, X, q, s, qT, sT, G, s2, sT2, qw, sw, qwT, swT
-        # a9 / a10: MoE 128 experts, hidden 2048, FFN 768, top-8 over 8192 tokens
-        T, Hd, Ex, F, topk = 8192, 2048, 128, 768, 8
-        xb, logits, _, _ = synth.moe_inputs()
-        cap = T * topk + Ex * 127
-        Z = torch.from_numpy(logits).to(dev)
-        ti, tp = torch.empty((T, topk), dtype=torch.int32, device=dev), torch.empty((T, topk), device=dev)
-        cnt, offs = torch.empty(Ex, dtype=torch.int32, device=dev), torch.empty(Ex + 1, dtype=torch.int32, device=dev)
-        rt, rp, rpad = torch.empty(cap, dtype=torch.int32, device=dev), torch.empty(cap, device=dev), u8(cap)
-        t_route = self.time(lambda: fg.moe_route_pad(Z, topk, 128, cap, ti, tp, cnt, offs, rt, rp, rpad))
-        out["a9_moe_route_pad"] = {"time_us": t_route * 1e6, "note": "8192 tokens x 128 experts, top-8, pad to 128"}
-        XM = _bf16_dev(xb, dev)
-        qx, sx = u8(T, Hd), f32(Hd // 128, T)
-        fg.quant_1x128(XM, E, qx, sx)
-        qg, sg = torch.zeros((cap, Hd), dtype=torch.uint8, device=dev), torch.zeros((Hd // 128, cap), device=dev)
-        total = None
-        torch.cuda.synchronize()
-        total = int(offs[Ex].item())
-        k, v = self.hbm("a9_moe_gather", lambda: fg.moe_gather(qx, sx, rt, offs, Ex, cap, qg, sg),
-                        2 * total * Hd + 2 * total * (Hd // 128) * 4, f"{total} dispatched rows x 2048")
-        out[k] = v
-        qgu = u8(Ex, 2 * F, Hd); sgu = f32(Ex, 2 * F // 128, Hd // 128).fill_(1e-3)
-        qdn = u8(Ex, Hd, F); sdn = f32(Ex, Hd // 128, F // 128).fill_(1e-3)
-        qgu.random_(0, 120); qdn.random_(0, 120)
-        GU = torch.zeros((cap, 2 * F), dtype=torch.bfloat16, device=dev)
-        algo_gu = 2.0 * T * topk * 2 * F * Hd
-        k, v = self.tensor("a10_grouped_gemm_gate_up", lambda: fg.grouped_gemm(offs, qg, sg, qgu, sgu, GU), algo_gu,
-                           f"unpadded FLOPs; {total} padded rows, N=1536, K=2048")
-        out[k] = v
-        qh, sh = u8(cap, F), f32(F // 128, cap).fill_(1e-2)
-        Yd = torch.zeros((cap, Hd), dtype=torch.bfloat16, device=dev)
-        k, v = self.tensor("a10_grouped_gemm_down", lambda: fg.grouped_gemm(offs, qh, sh, qdn, sdn, Yd),
-                           2.0 * T * topk * Hd * F, f"unpadded FLOPs; N=2048, K=768")
-        out[k] = v
-        del qg, GU, Yd, qgu, qdn
-        # a11: SwiGLU glue on the MLP shapes
-        GU2 = bf(8192, 28672).normal_()
-        H2, dH2, dGU2 = bf(8192, 14336), bf(8192, 14336).normal_(), bf(8192, 28672)
-        nf = 8192 * 14336
-        k, v = self.hbm("a11_swiglu_fwd", lambda: fg.swiglu_fwd(GU2, H2), 6 * nf, "GU 8192x28672 -> H")
-        out[k] = v
-        k, v = self.hbm("a11_swiglu_bwd", lambda: fg.swiglu_bwd(GU2, dH2, dGU2), 10 * nf, "GU, dH -> dGU")
-        out[k] = v
+        if want("a3") or want("a4") or want("a5"):
+            W = _bf16_dev(synth.bf16_normal((28672, 4096), 1000, 0.02), dev)
+            qw, sw, qwT, swT = u8(28672, 4096), f32(224, 32), u8(4096, 28672), f32(32, 224)
+            fg.quant_128x128(W, E, qw, sw)
+        if want("a3"):
+            put(self.hbm("a3_quant_128x128", lambda: fg.quant_128x128(W, E, qw, sw), 3 * n, "W_gu 28672x4096"))
+            put(self.hbm("a3_quant_128x128_fused_T", lambda: fg.quant_128x128(W, E, qw, sw, qwT, swT), 4 * n,
+                         "W_gu 28672x4096, q and q^T in one pass"))
+        if want("a4"):
+            put(self.hbm("a4_fp8_transpose_on_demand", lambda: fg.transpose_128x128(qw, sw, qwT, swT), 2 * n,
+                         "FP8 W_gu^T"))
+        if want("a5"):
+            D = bf(8192, 28672)
+            put(self.tensor("a5_gemm_fprop_8192x28672x4096", lambda: fg.blockscaled_gemm(
+                q, E, s, fg.GRAN_1x128, qw, E, sw, fg.GRAN_128x128, D), 2.0 * 8192 * 28672 * 4096,
+                "1x128 x 128x128, BF16 out"))
+            del D
+        if want("a5_gemm_wgrad"):
+            D32 = f32(28672, 4096)
+            qa_w, qb_w = u8(28672, 8192).random_(0, 120), u8(4096, 8192).random_(0, 120)
+            sa_w, sb_w = f32(64, 28672).fill_(1e-2), f32(64, 4096).fill_(1e-2)
+            put(self.tensor("a5_gemm_wgrad_28672x4096x8192", lambda: fg.blockscaled_gemm(
+                qa_w, E, sa_w, fg.GRAN_1x128, qb_w, E, sb_w, fg.GRAN_1x128, D32), 2.0 * 28672 * 4096 * 8192,
+                "1x128 x 1x128, FP32 out"))
+            del qa_w, qb_w, D32
+        if want("a3") or want("a4") or want("a5"):
+            del W, qw, sw, qwT, swT
+        if want("a6") or want("a7"):
+            R6, C6 = 16384, 4096
+            X6 = _bf16_dev(synth.delayed_step_inputs(0)[0], dev)
+            rec = fg.DelayedRecipe(E, 16, 0, fg.AMAX_MAX)
+            hist, stepc = torch.zeros(16, device=dev), torch.zeros(1, dtype=torch.int32, device=dev)
+            scale = torch.ones(1, device=dev)
+            ws, stats = fg.new_workspace(dev), fg.new_stats(dev)
+            q6, q6T = u8(R6, C6), u8(C6, R6)
+            fg.quant_pertensor_delayed(X6, rec, hist, stepc, scale, q6, ws)
+        if want("a6"):
+            put(self.hbm("a6_delayed_pertensor_with_monitors_and_T", lambda: fg.quant_pertensor_delayed(
+                X6, rec, hist, stepc, scale, q6, ws, q6T, stats), 4 * R6 * C6, "X 16384x4096 E4M3, qT, monitors"))
+            put(self.hbm("a6_delayed_pertensor_plain", lambda: fg.quant_pertensor_delayed(
+                X6, rec, hist, stepc, scale, q6, ws), 3 * R6 * C6, "X 16384x4096 E4M3"))
+        if want("a8"):
+            st8 = fg.new_stats(dev)
+            put(self.hbm("a8_monitors_1x128", lambda: fg.quant_stats(X, q, s, fg.GRAN_1x128, E, st8),
+                         3 * R * C, "X 8192x4096 (distinct counts per 1x128 tile: ALU-bound)"))
+        if want("a7"):
+            W7 = u8(4096, 4096).random_(0, 120)
+            D7 = bf(16384, 4096)
+            one = torch.ones(1, device=dev)
+            put(self.tensor("a7_gemm_pertensor_16384x4096x4096", lambda: fg.blockscaled_gemm(
+                q6, E, one, fg.GRAN_TENSOR, W7, E, one, fg.GRAN_TENSOR, D7), 2.0 * 16384 * 4096 * 4096,
+                "E4M3 x E4M3"))
+            put(self.tensor("a7_gemm_hybrid_e5m2_16384x4096x4096", lambda: fg.blockscaled_gemm(
+                q6, fg.E5M2, one, fg.GRAN_TENSOR, W7, E, one, fg.GRAN_TENSOR, D7), 2.0 * 16384 * 4096 * 4096,
+                "E5M2 x E4M3"))
+            del W7, D7
+        if want("a6") or want("a7"):
+            del X6, q6, q6T
+        if want("a9") or want("a10"):
+            T, Hd, Ex, F, topk = 8192, 2048, 128, 768, 8
+            xb, logits, _, _ = synth.moe_inputs()
+            cap = T * topk + Ex * 127
+            Z = torch.from_numpy(logits).to(dev)
+            ti, tp = torch.empty((T, topk), dtype=torch.int32, device=dev), torch.empty((T, topk), device=dev)
+            cnt = torch.empty(Ex, dtype=torch.int32, device=dev)
+            offs = torch.empty(Ex + 1, dtype=torch.int32, device=dev)
+            rt, rp, rpad = torch.empty(cap, dtype=torch.int32, device=dev), torch.empty(cap, device=dev), u8(cap)
+            fg.moe_route_pad(Z, topk, 128, cap, ti, tp, cnt, offs, rt, rp, rpad)
+            XM = _bf16_dev(xb, dev)
+            qx, sx = u8(T, Hd), f32(Hd // 128, T)
+            fg.quant_1x128(XM, E, qx, sx)
+            qg, sg = torch.zeros((cap, Hd), dtype=torch.uint8, device=dev), torch.zeros((Hd // 128, cap), device=dev)
+            fg.moe_gather(qx, sx, rt, offs, Ex, cap, qg, sg)
+            torch.cuda.synchronize()
+            total = int(offs[Ex].item())
+        if want("a9"):
+            t_route = self.time(lambda: fg.moe_route_pad(Z, topk, 128, cap, ti, tp, cnt, offs, rt, rp, rpad))
+            out["a9_moe_route_pad"] = {"time_us": t_route * 1e6, "bound": "latency",
+                                       "note": "8192 tokens x 128 experts, top-8, pad to 128 (3 launches)"}
+            put(self.hbm("a9_moe_gather", lambda: fg.moe_gather(qx, sx, rt, offs, Ex, cap, qg, sg),
+                         2 * total * Hd + 2 * total * (Hd // 128) * 4, f"{total} dispatched rows x 2048"))
+        if want("a10"):
+            qgu = u8(Ex, 2 * F, Hd).random_(0, 120)
+            sgu = f32(Ex, 2 * F // 128, Hd // 128).fill_(1e-3)
+            qdn = u8(Ex, Hd, F).random_(0, 120)
+            sdn = f32(Ex, Hd // 128, F // 128).fill_(1e-3)
+            GU = torch.zeros((cap, 2 * F), dtype=torch.bfloat16, device=dev)
+            put(self.tensor("a10_grouped_gemm_gate_up", lambda: fg.grouped_gemm(offs, qg, sg, qgu, sgu, GU),
+                            2.0 * T * topk * 2 * F * Hd, f"unpadded FLOPs; {total} padded rows, N=1536, K=2048"))
+            qh, sh = u8(cap, F).random_(0, 120), f32(F // 128, cap).fill_(1e-2)
+            Yd = torch.zeros((cap, Hd), dtype=torch.bfloat16, device=dev)
+            put(self.tensor("a10_grouped_gemm_down", lambda: fg.grouped_gemm(offs, qh, sh, qdn, sdn, Yd),
+                            2.0 * T * topk * Hd * F, "unpadded FLOPs; N=2048, K=768"))
+            del qgu, qdn, GU, Yd, qh
+        if want("a11"):
+            GU2 = bf(8192, 28672).normal_()
+            H2, dH2, dGU2 = bf(8192, 14336), bf(8192, 14336).normal_(), bf(8192, 28672)
+            nf = 8192 * 14336
+            put(self.hbm("a11_swiglu_fwd", lambda: fg.swiglu_fwd(GU2, H2), 6 * nf, "GU 8192x28672 -> H"))
+            put(self.hbm("a11_swiglu_bwd", lambda: fg.swiglu_bwd(GU2, dH2, dGU2), 10 * nf, "GU, dH -> dGU"))
         st = fg.device_status()
         out["device_status"] = fg.status_string(st)
         return out
@@ -482,15 +508,18 @@ def run_ours(args):
     except Exception:
         pass
     clocks = Clocks(gpu_id)
+    time.sleep(0.5)                      # let the sampler start
     ev = []
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier()
+    clocks.mark("start")
     t_start.record(stream)
     for _ in range(args.steps):
         ev.append(step.run(timed=True))
     t_end.record(stream)
     barrier()
+    clocks.mark("end")
     clk = clocks.stop()
     ms = t_start.elapsed_time(t_end) / args.steps
     if world > 1:
@@ -552,16 +581,28 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row kernel measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--only", default=None,
+                    help="time only the hot-path row(s) whose name starts with this prefix (e.g. a5, a2) and "
+                         "print them; used for single-kernel ncu captures")
+    ap.add_argument("--iters", type=int, default=8, help="launches per row for --only")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.only:
+        import torch
+
+        import fp8_fine_grained_x128_gb300 as fg
+        torch.cuda.set_device(0)
+        fg.lib()
+        print(json.dumps(RowBench(torch.device("cuda", 0), peaks()).run_all(args.only, args.iters)))
+        return 0
     return run_ours(args)
 
 

@@ -86,6 +86,48 @@ struct Divider {
     }
 };
 
+// Packed form of the same division for the two BF16 values of a 32-bit word:
+// q0 = x*r, e = x - q0*s (exact), q = q0 + e*r, two lanes per instruction
+// (fma.rn.f32x2 rounds each lane like the scalar instruction).  For x = -0
+// it returns +0; callers restore the sign bit of zero quotients from x with
+// sign_bits4() on the codes.
+struct Divider2 {
+    uint64_t r2, ns2;
+    float s;
+    bool fast;
+    __device__ __forceinline__ explicit Divider2(float s_) : s(s_)
+    {
+        fast = (s_ >= 0x1p-125f) && (s_ <= 0x1p125f);
+        const float r = fast ? __frcp_rn(s_) : 0.0f;
+        asm("mov.b64 %0, {%1, %1};" : "=l"(r2) : "f"(r));
+        asm("mov.b64 %0, {%1, %1};" : "=l"(ns2) : "f"(-s_));
+    }
+    // quotients of (lo, hi) BF16 halves of w
+    __device__ __forceinline__ void operator()(uint32_t w, float &qlo, float &qhi) const
+    {
+        const float xlo = __uint_as_float(w << 16), xhi = __uint_as_float(w & 0xFFFF0000u);
+        if (fast) {
+            uint64_t x2, q0, e, q;
+            asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "f"(xlo), "f"(xhi));
+            asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(r2));
+            asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(ns2), "l"(x2));
+            asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(e), "l"(r2), "l"(q0));
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(qlo), "=f"(qhi) : "l"(q));
+        } else {
+            qlo = __fdiv_rn(xlo, s);
+            qhi = __fdiv_rn(xhi, s);
+        }
+    }
+};
+
+// Sign bits of the 4 BF16 values in (w0 = x0,x1 ; w1 = x2,x3) placed at bit 7
+// of bytes 0..3: OR-ed into the 4 codes this restores -0 -> 0x80 (every other
+// code already carries the sign of its value).
+__device__ __forceinline__ uint32_t sign_bits4(uint32_t w0, uint32_t w1)
+{
+    return __byte_perm(w0, w1, 0x7531) & 0x80808080u;
+}
+
 // FP8 encode of two binary32 values (round to nearest even, saturating to
 // +-fmax): the byte of `lo` lands in bits 0..7, `hi` in bits 8..15.
 template <int FMT>
@@ -107,6 +149,22 @@ __device__ __forceinline__ uint2 quant8(uint4 v, const Divider &d)
     out.x = cvt2<FMT>(d(bf16_lo(v.x)), d(bf16_hi(v.x))) | (cvt2<FMT>(d(bf16_lo(v.y)), d(bf16_hi(v.y))) << 16);
     out.y = cvt2<FMT>(d(bf16_lo(v.z)), d(bf16_hi(v.z))) | (cvt2<FMT>(d(bf16_lo(v.w)), d(bf16_hi(v.w))) << 16);
     return out;
+}
+
+// Same with the packed divider.
+template <int FMT>
+__device__ __forceinline__ uint32_t quant4p(uint32_t w0, uint32_t w1, const Divider2 &d)
+{
+    float a, b, c, e;
+    d(w0, a, b);
+    d(w1, c, e);
+    return (cvt2<FMT>(a, b) | (cvt2<FMT>(c, e) << 16)) | sign_bits4(w0, w1);
+}
+
+template <int FMT>
+__device__ __forceinline__ uint2 quant8p(uint4 v, const Divider2 &d)
+{
+    return make_uint2(quant4p<FMT>(v.x, v.y, d), quant4p<FMT>(v.z, v.w, d));
 }
 
 __device__ __forceinline__ uint32_t absmax8(uint4 v)
@@ -279,6 +337,59 @@ __device__ __forceinline__ void tc_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[1
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
+}
+
+// Packed FP32 pair arithmetic (two IEEE binary32 lanes, each rounded to
+// nearest like the scalar instruction).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// acc + (lo, hi) * s2, lane-wise
+__device__ __forceinline__ uint64_t f2_fma_bits(uint32_t lo, uint32_t hi, uint64_t s2, uint64_t acc)
+{
+    uint64_t d;
+    asm("{\n\t.reg .b64 p;\n\tmov.b64 p, {%1, %2};\n\tfma.rn.f32x2 %0, p, %3, %4;\n\t}"
+        : "=l"(d)
+        : "r"(lo), "r"(hi), "l"(s2), "l"(acc));
+    return d;
+}
+
+// (lo, hi) * b2, lane-wise
+__device__ __forceinline__ uint64_t f2_mul_bits(uint32_t lo, uint32_t hi, uint64_t b2)
+{
+    uint64_t d;
+    asm("{\n\t.reg .b64 p;\n\tmov.b64 p, {%1, %2};\n\tmul.rn.f32x2 %0, p, %3;\n\t}"
+        : "=l"(d)
+        : "r"(lo), "r"(hi), "l"(b2));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// Per-warpgroup register budget changes (all threads of the warpgroup).
+template <int N>
+__device__ __forceinline__ void regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile stored in the

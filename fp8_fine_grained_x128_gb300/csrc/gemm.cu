@@ -11,17 +11,27 @@
 // For per-tensor scales (the coarse delayed-scaling recipe) the whole K is
 // accumulated in tensor memory and sA*sB applied once.
 //
-// Structure (one persistent CTA per SM, 320 threads):
+// Structure (one persistent CTA per SM, 384 threads = 3 warpgroups):
 //   warp 0      TMA producer: A tile 128x128 B and B tile BNx128 B per stage,
 //               128-byte swizzle, STAGES-deep ring of shared-memory stages.
 //   warp 1      owns the tensor memory (2 accumulators of BN columns) and
 //               issues tcgen05.mma kind::f8f6f4 (M=128, N=BN, K=32, 4 per
 //               chunk) from one thread; tcgen05.commit frees the stage and
 //               publishes the accumulator.
-//   warps 2..9  epilogue: tcgen05.ld 32x32b of their lane quarter and column
-//               half, FP32 promotion with the scales, BF16/FP32 stores.  The
-//               two accumulators alternate per chunk, so the tensor cores fill
-//               one while the epilogue drains the other.
+//   warp 2      scale producer: runs up to SD chunks ahead and writes each
+//               chunk's scales into a shared-memory ring -- per row
+//               sA(m,kb)*sB(n-block,kb) for 128x128 B scales, or sA(m,kb) and
+//               the per-column sB(n,kb) -- so the epilogue never waits on a
+//               global load.  (Warp 3 idles.)  This warpgroup gives registers
+//               away (setmaxnreg.dec).
+//   warps 4..11 epilogue, two warpgroups raised to 216 registers: each thread
+//               owns one accumulator row and half of the tile's columns as an
+//               FP32 running sum in registers; per chunk it pulls 64 columns
+//               per wait from tensor memory (two tcgen05.ld 32x32b.x32) and
+//               promotes them with packed fma.rn.f32x2, then stores BF16/FP32
+//               rows at the end of the tile.  The two accumulators alternate
+//               per chunk, so the tensor cores fill one while the epilogue
+//               drains the other.
 // Every mbarrier wait is bounded (about 1 s): on a timeout the CTA records
 // FP8_ERR_TIMEOUT, tells the other roles through a shared flag, waits for
 // its own copies and MMAs in flight (bounded again), frees the tensor memory
@@ -33,8 +43,13 @@
 
 namespace fp8fg {
 
-constexpr int kGemmThreads = 320;
+constexpr int kGemmThreads = 384;
 constexpr int kEpiWarps = 8;
+constexpr int kEpiWarp0 = 4;          // first epilogue warp (warpgroups 1 and 2)
+constexpr int kCtrlRegs = 144;         // setmaxnreg of the control warpgroup
+constexpr int kEpiRegs = 176;         // setmaxnreg of the epilogue warpgroups
+// the split must fit the registers the CTA is launched with
+constexpr int kRegsNeededAtLaunch = (128 * kCtrlRegs + 256 * kEpiRegs + kGemmThreads - 1) / kGemmThreads;
 constexpr int kMaxGroups = 1024;
 
 struct GemmArgs {
@@ -51,24 +66,31 @@ struct GemmArgs {
     const int32_t *offsets;
     int G;
     int *status;
+    int raster_gm;        // M-tiles per raster band
 };
 
 enum { SB_BLOCK = 0, SB_ROW = 1 };
+
+constexpr int kScaleDepth = 4;     // chunks of scales staged ahead of the epilogue
 
 template <int BN, int STAGES>
 struct GemmSmem {
     static constexpr int kA = 128 * 128;
     static constexpr int kB = BN * 128;
     static constexpr int kStage = kA + kB;
-    static constexpr int kBars = 2 * STAGES + 2 + 2 + 1;
+    // per scale slot: row values for the two column halves + BN column values
+    static constexpr int kScaleSlotFloats = 2 * 128 + BN;
+    static constexpr int kScaleBytes = kScaleDepth * kScaleSlotFloats * 4;
+    static constexpr int kBars = 2 * STAGES + 2 + 2 + 1 + 2 * kScaleDepth;
     static constexpr int kCtrl = kBars * 8 + 16;
-    static constexpr int kBytes = 1024 + STAGES * kStage + kCtrl + 4 * (kMaxGroups + 1);
+    static constexpr int kBytes = 1024 + STAGES * kStage + kScaleBytes + kCtrl + 4 * (kMaxGroups + 1);
     static constexpr int kTmemCols = 2 * BN;
 };
 
-__device__ __forceinline__ void tile_coords_raster(int tile, int num_mt, int num_nt, int &mt, int &nt)
+// Tiles are walked in bands of GM M-tiles, M fastest: a band's A rows stay in
+// L2 while every B tile is streamed through it once per band.
+__device__ __forceinline__ void tile_coords_raster(int tile, int num_mt, int num_nt, int GM, int &mt, int &nt)
 {
-    constexpr int GM = 16;   // 16 M-tiles share each B tile while it is hot in L2
     const int group = tile / (GM * num_nt);
     const int first = group * GM;
     const int gm = min(GM, num_mt - first);
@@ -146,18 +168,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
            GemmArgs a)
 {
     using L = GemmSmem<BN, STAGES>;
-    constexpr int HALF = BN / 2;        // columns per epilogue warp
+    constexpr int HALF = BN / 2;        // columns per epilogue thread
+    constexpr int NP = HALF / 2;        // packed FP32 pairs per epilogue thread
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * L::kStage);
+    float *scl = reinterpret_cast<float *>(smem + STAGES * L::kStage);      // [kScaleDepth][slot floats]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * L::kStage + L::kScaleBytes);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *mma_done = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *sc_full = mma_done + 1;
+    uint64_t *sc_empty = sc_full + kScaleDepth;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sc_empty + kScaleDepth);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *bad_offsets = reinterpret_cast<int *>(tmem_slot + 2);
-    int32_t *sh_off = reinterpret_cast<int32_t *>(smem + STAGES * L::kStage + L::kCtrl);
+    int32_t *sh_off = reinterpret_cast<int32_t *>(smem + STAGES * L::kStage + L::kScaleBytes + L::kCtrl);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -171,6 +197,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&tempty[b], kEpiWarps);
         }
         mbar_init(mma_done, 1);
+        for (int i = 0; i < kScaleDepth; ++i) {
+            mbar_init(&sc_full[i], 1);
+            mbar_init(&sc_empty[i], kEpiWarps);
+        }
         *abort_flag = 0;
         *bad_offsets = 0;
         fence_barrier_init();
@@ -207,15 +237,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int ntiles = num_mt * num_nt;
     const int nk = a.K / 128;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+    if (warp < kEpiWarp0) {
+        regs_dec<kCtrlRegs>();
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------------- TMA producer
             uint32_t it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
                 int mt, nt;
                 if (GROUPED) { mt = tile / num_nt; nt = tile - mt * num_nt; }
-                else tile_coords_raster(tile, num_mt, num_nt, mt, nt);
+                else tile_coords_raster(tile, num_mt, num_nt, a.raster_gm, mt, nt);
                 const int brow = nt * BN + (GROUPED ? group_of_row(sh_off, a.G, mt * 128) * a.N : 0);
                 for (int kb = 0; kb < nk; ++kb) {
                     const int s = it % STAGES;
@@ -231,10 +262,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // copies still in flight land before the CTA may exit
             const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0;
             for (uint32_t j = first; j < it; ++j) mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1, nullptr);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------- MMA issuer
             uint32_t it = 0, cc = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
@@ -277,10 +306,51 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // every MMA issued by this thread completes before the CTA frees TMEM
             tc_commit(mma_done);
             mbar_wait_bounded(mma_done, 0, nullptr);
+        } else if (PROMOTE && warp == 2) {
+            // -------------------------------------------------- scale producer
+            uint32_t cs = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                int mt, nt;
+                if (GROUPED) { mt = tile / num_nt; nt = tile - mt * num_nt; }
+                else tile_coords_raster(tile, num_mt, num_nt, a.raster_gm, mt, nt);
+                const int m0 = mt * 128, n0 = nt * BN;
+                const float *sB = a.sB;
+                if (GROUPED) sB += (int64_t)group_of_row(sh_off, a.G, m0) * a.sB_group_stride;
+                for (int kb = 0; kb < nk; ++kb, ++cs) {
+                    const int slot = cs % kScaleDepth;
+                    if (!warp_wait_or_abort(&sc_empty[slot], ((cs / kScaleDepth) & 1) ^ 1, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    float *sv = scl + slot * L::kScaleSlotFloats;
+                    float4 sa4;
+                    if (a.granA == FP8_GRAN_1x128) {
+                        sa4 = *reinterpret_cast<const float4 *>(a.sA + (int64_t)kb * a.ldsA + m0 + 4 * lane);
+                    } else {
+                        const float v = a.sA[(int64_t)(m0 >> 7) * a.ldsA + kb];
+                        sa4 = make_float4(v, v, v, v);
+                    }
+                    if (SBG == SB_BLOCK) {
+                        const float b0 = sB[(int64_t)(n0 >> 7) * a.ldsB + kb];
+                        const float b1 = sB[(int64_t)((n0 + HALF) >> 7) * a.ldsB + kb];
+                        *reinterpret_cast<float4 *>(sv + 4 * lane) = make_float4(sa4.x * b0, sa4.y * b0, sa4.z * b0, sa4.w * b0);
+                        *reinterpret_cast<float4 *>(sv + 128 + 4 * lane) = make_float4(sa4.x * b1, sa4.y * b1, sa4.z * b1, sa4.w * b1);
+                    } else {
+                        *reinterpret_cast<float4 *>(sv + 4 * lane) = sa4;
+                        const float4 *col = reinterpret_cast<const float4 *>(sB + (int64_t)kb * a.ldsB + n0);
+#pragma unroll
+                        for (int i = lane; i < BN / 4; i += 32) reinterpret_cast<float4 *>(sv + 256)[i] = col[i];
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sc_full[slot]);
+                }
+            }
         }
     } else {
+        regs_inc<kEpiRegs>();
         // ------------------------------------------------------ epilogue
-        const int ew = warp - 2;
+        const int ew = warp - kEpiWarp0;
         const int lg = warp & 3;             // TMEM lane quarter this warp may access
         const int colbase = (ew >> 2) * HALF;
         const int row = lg * 32 + lane;
@@ -290,50 +360,67 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
             int mt, nt;
             if (GROUPED) { mt = tile / num_nt; nt = tile - mt * num_nt; }
-            else tile_coords_raster(tile, num_mt, num_nt, mt, nt);
+            else tile_coords_raster(tile, num_mt, num_nt, a.raster_gm, mt, nt);
             const int m0 = mt * 128, n0 = nt * BN;
             const float *sB = a.sB;
             if (GROUPED) sB += (int64_t)group_of_row(sh_off, a.G, m0) * a.sB_group_stride;
             if (PROMOTE) {
-                float acc[HALF];
+                uint64_t acc[NP];
 #pragma unroll
-                for (int i = 0; i < HALF; ++i) acc[i] = 0.0f;
+                for (int i = 0; i < NP; ++i) acc[i] = 0ull;
                 for (int kb = 0; kb < nk; ++kb) {
                     const uint32_t buf = cc & 1;
-                    const float sa = a.granA == FP8_GRAN_1x128 ? a.sA[(int64_t)kb * a.ldsA + m0 + row]
-                                                              : a.sA[(int64_t)(m0 >> 7) * a.ldsA + kb];
-                    float sb = 0.0f;
-                    if (SBG == SB_BLOCK) sb = sB[(int64_t)((n0 + colbase) >> 7) * a.ldsB + kb];
+                    const int slot = cc % kScaleDepth;
+                    if (!warp_wait_or_abort(&sc_full[slot], (cc / kScaleDepth) & 1, abort_flag, a.status)) { ok = false; break; }
+                    const float *sv = scl + slot * L::kScaleSlotFloats;
+                    // 128x128 B: sA*sB of this thread's row and column half; 1x128 B: sA of the row
+                    const float sr = sv[(SBG == SB_BLOCK ? (ew >> 2) * 128 : 0) + row];
                     if (!warp_wait_or_abort(&tfull[buf], (cc >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
-                    const float sab = sa * sb;
+                    const uint64_t s2 = f2_pack(sr, sr);
+                    if (SBG == SB_BLOCK) {
+                        // 64 columns per wait: two x32 loads in flight
 #pragma unroll
-                    for (int j = 0; j < HALF / 16; ++j) {
-                        uint32_t r[16];
-                        tc_ld_32x32b_x16(tm_lane + buf * BN + colbase + j * 16, r);
-                        tc_wait_ld();
-                        if (SBG == SB_BLOCK) {
+                        for (int j = 0; j < HALF / 64; ++j) {
+                            uint32_t r0[32], r1[32];
+                            tc_ld_32x32b_x32(tm_lane + buf * BN + colbase + j * 64, r0);
+                            tc_ld_32x32b_x32(tm_lane + buf * BN + colbase + j * 64 + 32, r1);
+                            tc_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(__uint_as_float(r[i]), sab, acc[j * 16 + i]);
-                        } else {
-                            const float4 *sbv = reinterpret_cast<const float4 *>(sB + (int64_t)kb * a.ldsB + n0 + colbase + j * 16);
+                            for (int i = 0; i < 16; ++i) {
+                                acc[j * 32 + i] = f2_fma_bits(r0[2 * i], r0[2 * i + 1], s2, acc[j * 32 + i]);
+                                acc[j * 32 + 16 + i] = f2_fma_bits(r1[2 * i], r1[2 * i + 1], s2, acc[j * 32 + 16 + i]);
+                            }
+                        }
+                    } else {
+                        // per-column scales sB(n, kb): 32 columns per wait
 #pragma unroll
-                            for (int i4 = 0; i4 < 4; ++i4) {
-                                const float4 b4 = __ldg(sbv + i4);
-                                acc[j * 16 + 4 * i4 + 0] = fmaf(__uint_as_float(r[4 * i4 + 0]) * b4.x, sa, acc[j * 16 + 4 * i4 + 0]);
-                                acc[j * 16 + 4 * i4 + 1] = fmaf(__uint_as_float(r[4 * i4 + 1]) * b4.y, sa, acc[j * 16 + 4 * i4 + 1]);
-                                acc[j * 16 + 4 * i4 + 2] = fmaf(__uint_as_float(r[4 * i4 + 2]) * b4.z, sa, acc[j * 16 + 4 * i4 + 2]);
-                                acc[j * 16 + 4 * i4 + 3] = fmaf(__uint_as_float(r[4 * i4 + 3]) * b4.w, sa, acc[j * 16 + 4 * i4 + 3]);
+                        for (int j = 0; j < HALF / 32; ++j) {
+                            uint32_t r0[32];
+                            tc_ld_32x32b_x32(tm_lane + buf * BN + colbase + j * 32, r0);
+                            tc_wait_ld();
+                            const float4 *sbv = reinterpret_cast<const float4 *>(sv + 256 + colbase + j * 32);
+#pragma unroll
+                            for (int i4 = 0; i4 < 8; ++i4) {
+                                const float4 b4 = sbv[i4];
+                                acc[j * 16 + 2 * i4] = f2_fma(f2_mul_bits(r0[4 * i4], r0[4 * i4 + 1], f2_pack(b4.x, b4.y)), s2, acc[j * 16 + 2 * i4]);
+                                acc[j * 16 + 2 * i4 + 1] = f2_fma(f2_mul_bits(r0[4 * i4 + 2], r0[4 * i4 + 3], f2_pack(b4.z, b4.w)), s2, acc[j * 16 + 2 * i4 + 1]);
                             }
                         }
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[buf]);
+                    if (lane == 0) {
+                        mbar_arrive(&tempty[buf]);
+                        mbar_arrive(&sc_empty[slot]);
+                    }
                     ++cc;
                 }
                 if (!ok) break;
-                store_row<HALF>(a.D, a.ldD, a.out_f32, (int64_t)m0 + row, (int64_t)n0 + colbase, acc);
+                float v[HALF];
+#pragma unroll
+                for (int i = 0; i < NP; ++i) f2_unpack(acc[i], v[2 * i], v[2 * i + 1]);
+                store_row<HALF>(a.D, a.ldD, a.out_f32, (int64_t)m0 + row, (int64_t)n0 + colbase, v);
             } else {
                 const uint32_t buf = cc & 1;
                 const float sab = a.sA[0] * a.sB[0];
@@ -412,6 +499,11 @@ static int run_gemm(const CUtensorMap &mA, const CUtensorMap &mB, uint32_t idesc
     int dev = 0;
     cudaGetDevice(&dev);
     if (!attr_done[dev & 63]) {
+        // The warpgroups re-split their registers with setmaxnreg; the split
+        // only completes if the CTA was launched with at least that many.
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return FP8_ERR_CUDA;
+        if (fa.numRegs < kRegsNeededAtLaunch) return FP8_ERR_UNSUPPORTED;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) != cudaSuccess)
             return FP8_ERR_CUDA;
         attr_done[dev & 63] = true;
@@ -448,6 +540,12 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const 
     g.ldD = ldD;
     g.out_f32 = out_dtype == FP8_OUT_F32;
     g.status = status;
+    // the band's A rows (GM x 128 x K bytes) should stay well inside L2
+    {
+        int64_t gm = ((int64_t)32 << 20) / (128 * K);
+        gm = std::max<int64_t>(8, std::min<int64_t>(gm, M / 128));
+        g.raster_gm = (int)gm;
+    }
     const int64_t ntiles = (M / 128) * (N / BN);
     const int grid = (int)std::min<int64_t>(ntiles, sm_count());
     const bool tensor = granA == FP8_GRAN_TENSOR;
@@ -490,6 +588,7 @@ int launch_grouped_gemm(int G, const int32_t *offsets, int64_t Mcap, int64_t N, 
     g.offsets = offsets;
     g.G = G;
     g.status = status;
+    g.raster_gm = 1;
     const int64_t ntiles_max = (Mcap / 128) * (N / BN);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ntiles_max, sm_count()));
     if (BN == 256) return run_gemm<256, 4, true, SB_BLOCK, true>(mA, mB, idesc_f8f6f4(FP8_E4M3, FP8_E4M3, 128, 256), g, grid, st);

@@ -183,6 +183,8 @@ __global__ void __launch_bounds__(256) k_moe_fill(const int32_t *__restrict__ to
         free_seen += nfree;
         placed += nmem;
     }
+    // fewer free tokens than padding needed: the edit is impossible
+    if (threadIdx.x == 0 && placed != padded_count(c, align)) set_status(status, FP8_ERR_INVALID_ARG);
     // rows past the last expert
     for (int64_t r = total + (int64_t)e * blockDim.x + threadIdx.x; r < Mcap; r += (int64_t)E * blockDim.x) {
         row_token[r] = -1;

@@ -46,18 +46,15 @@ struct Counts {
 
 // Quantize 8 BF16 values with one scale and (optionally) account the monitors.
 template <int FMT, bool STATS>
-__device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider &d, Counts &c, uint32_t *bmx, uint32_t *bmq)
+__device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &c, uint32_t *bmx, uint32_t *bmq)
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float qv[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        qv[2 * j] = d(bf16_lo(w[j]));
-        qv[2 * j + 1] = d(bf16_hi(w[j]));
-    }
+    for (int j = 0; j < 4; ++j) d(w[j], qv[2 * j], qv[2 * j + 1]);
     uint2 out;
-    out.x = cvt2<FMT>(qv[0], qv[1]) | (cvt2<FMT>(qv[2], qv[3]) << 16);
-    out.y = cvt2<FMT>(qv[4], qv[5]) | (cvt2<FMT>(qv[6], qv[7]) << 16);
+    out.x = (cvt2<FMT>(qv[0], qv[1]) | (cvt2<FMT>(qv[2], qv[3]) << 16)) | sign_bits4(v.x, v.y);
+    out.y = (cvt2<FMT>(qv[4], qv[5]) | (cvt2<FMT>(qv[6], qv[7]) << 16)) | sign_bits4(v.z, v.w);
     if (STATS) {
         const float fm = fmax_of(FMT);
 #pragma unroll
@@ -178,7 +175,7 @@ __global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__res
         if (t < 8) bmq[t] = 0;
     }
     const float s_t = *scale;   // chosen from the amax of earlier steps
-    const Divider d(s_t);
+    const Divider2 d(s_t);
     __syncthreads();
 
     Counts c;

@@ -15,14 +15,17 @@
 //
 // All of these are HBM-bound streaming kernels: 16-byte vector loads, amax by
 // warp shuffles, coalesced FP8 stores, no tensor-core work.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace fp8fg {
 
 // ---------------------------------------------------------------------------
-// 1x128 along rows only.  A half-warp owns one 1x128 tile (16 lanes x 8 BF16);
-// each thread keeps U tiles in flight to cover HBM latency.
+// 1x128 along rows only.  A half-warp owns a run of U consecutive 1x128 tiles
+// of one row (16 lanes x 8 BF16 per tile), so every thread keeps U 16-byte
+// loads in flight; the only division per run is the run -> (row, chunk) map.
 // ---------------------------------------------------------------------------
 template <int FMT, int U>
 __global__ void __launch_bounds__(256) k_quant_1x128_rows(const uint16_t *__restrict__ x, uint32_t rows,
@@ -32,35 +35,32 @@ __global__ void __launch_bounds__(256) k_quant_1x128_rows(const uint16_t *__rest
     const int l16 = threadIdx.x & 15;
     const uint32_t hw0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 4;
     const uint32_t nhw = (gridDim.x * blockDim.x) >> 4;
-    const uint32_t ntiles = rows * ncb;
+    const uint32_t ngrp = (ncb + U - 1) / U;        // runs per row
+    const uint32_t nitems = rows * ngrp;
     const int64_t cols = (int64_t)ncb * 128;
-    // both half-warps of a warp share the loop test (shuffles below use the full mask)
-    for (uint32_t base = hw0; (base & ~1u) < ntiles; base += nhw * U) {
+    // both half-warps of a warp share the loop test (shuffles use the full mask)
+    for (uint32_t it = hw0; (it & ~1u) < nitems; it += nhw) {
+        const bool valid = it < nitems;
+        const uint32_t r = valid ? it / ngrp : 0;
+        const uint32_t c0 = valid ? (it - r * ngrp) * U : ncb;
+        const uint16_t *xr = x + (int64_t)r * ldx + l16 * 8;
         uint4 v[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t t = base + u * nhw;
-            if (t < ntiles) {
-                const uint32_t r = t / ncb, cb = t - r * ncb;
-                v[u] = ldg_stream(x + (int64_t)r * ldx + (int64_t)cb * 128 + l16 * 8);
-            } else {
-                v[u] = make_uint4(0, 0, 0, 0);
-            }
-        }
+        for (int u = 0; u < U; ++u)
+            v[u] = (c0 + u < ncb) ? ldg_stream(xr + (int64_t)(c0 + u) * 128) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const uint32_t t = base + u * nhw;
             uint32_t m = absmax8(v[u]);
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            if (t < ntiles) {
-                const uint32_t r = t / ncb, cb = t - r * ncb;
+            const uint32_t cb = c0 + u;
+            if (cb < ncb) {
                 if (m >= 0x7F80u && l16 == 0) set_status(status, FP8_ERR_NONFINITE);
                 const float sc = scale_from_amax_bits(m, FMT);
-                const Divider d(sc);
-                *reinterpret_cast<uint2 *>(q + (int64_t)r * cols + (int64_t)cb * 128 + l16 * 8) = quant8<FMT>(v[u], d);
+                const Divider2 d(sc);
+                *reinterpret_cast<uint2 *>(q + (int64_t)r * cols + (int64_t)cb * 128 + l16 * 8) = quant8p<FMT>(v[u], d);
                 if (l16 == 0) s[(int64_t)cb * rows + r] = sc;
             }
         }
@@ -68,35 +68,44 @@ __global__ void __launch_bounds__(256) k_quant_1x128_rows(const uint16_t *__rest
 }
 
 // ---------------------------------------------------------------------------
-// Fused 1x128 + transposed 128x1.  One CTA per 128x128 tile of x:
-//  1. each thread loads 8 rows x 8 columns (16 B per row) -- one HBM read;
+// Fused 1x128 + transposed 128x1.  Persistent CTAs walk 128x128 tiles of x:
+//  1. each thread holds 8 rows x 8 columns (16 B per row) of the tile in
+//     registers -- the tile's only HBM read;
 //  2. row scales by half-warp shuffles, row codes stored straight from
-//     registers; the raw tile is kept in shared memory (16-B chunks XOR-
-//     swizzled by row so both the row stores and the 4x4 column reads are
-//     bank-conflict free);
-//  3. column amax over the 128 rows (registers -> shuffle -> shared), the
-//     128 column scales and their reciprocals;
-//  4. each thread quantizes 4x4 sub-blocks with the column scales and writes
-//     4 words of the transposed codes (32-byte segments per 8 lanes).
+//     registers; the raw tile goes to shared memory (16-B chunks XOR-
+//     swizzled by row so the row stores and the 4x4 column reads are both
+//     bank-conflict free); per-column amax partials go to shared memory;
+//  3. the 128 column scales and their reciprocals;
+//  4. the loads of the NEXT tile are issued, then each thread quantizes 4x4
+//     sub-blocks with the column scales and writes 4 words of the transposed
+//     codes (full 32-byte segments per 8 lanes) while those loads fly.
 // ---------------------------------------------------------------------------
-struct ColDiv {
-    float s, r;
+struct ColDiv2 {
+    uint64_t r2, ns2;    // (1/s_j, 1/s_j+1), (-s_j, -s_j+1)
+    float s0, s1;
     int fast;
 };
 
 template <int FMT>
-__device__ __forceinline__ float div_col(float x, const ColDiv &c)
+__device__ __forceinline__ uint32_t quant_pair_cols(uint32_t w, const ColDiv2 &c)
 {
+    float qlo, qhi;
     if (c.fast) {
-        float q0 = __fmul_rn(x, c.r);
-        float e = __fmaf_rn(-q0, c.s, x);
-        float qv = __fmaf_rn(e, c.r, q0);
-        return __uint_as_float(__float_as_uint(qv) | (__float_as_uint(x) & 0x80000000u));
+        const float xlo = __uint_as_float(w << 16), xhi = __uint_as_float(w & 0xFFFF0000u);
+        uint64_t x2, q0, e, qq;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "f"(xlo), "f"(xhi));
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(c.r2));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(c.ns2), "l"(x2));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(qq) : "l"(e), "l"(c.r2), "l"(q0));
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(qlo), "=f"(qhi) : "l"(qq));
+    } else {
+        qlo = __fdiv_rn(__uint_as_float(w << 16), c.s0);
+        qhi = __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), c.s1);
     }
-    return __fdiv_rn(x, c.s);
+    return cvt2<FMT>(qlo, qhi);
 }
 
-constexpr int kFusedSmem = 32768 + 4096 + 128 * sizeof(ColDiv);
+constexpr int kFusedSmem = 32768 + 4096 + 64 * sizeof(ColDiv2);
 
 template <int FMT>
 __global__ void __launch_bounds__(256) k_quant_1x128_fused_t(const uint16_t *__restrict__ x, int64_t rows,
@@ -105,90 +114,109 @@ __global__ void __launch_bounds__(256) k_quant_1x128_fused_t(const uint16_t *__r
                                                              float *__restrict__ sT, int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t *tile = smem;                                        // [128][256 B], swizzled 16-B chunks
-    uint32_t *colpart = reinterpret_cast<uint32_t *>(smem + 32768);  // [8 warps][128]
-    ColDiv *cdiv = reinterpret_cast<ColDiv *>(smem + 32768 + 4096);  // [128]
+    uint8_t *tile = smem;                                              // [128][256 B], swizzled 16-B chunks
+    uint32_t *colpart = reinterpret_cast<uint32_t *>(smem + 32768);    // [8 warps][128]
+    ColDiv2 *cdiv = reinterpret_cast<ColDiv2 *>(smem + 32768 + 4096);  // [64 column pairs]
 
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int g = t & 15, rr = t >> 4;
-    const int64_t cb = blockIdx.x, mb = blockIdx.y;
-    const int64_t r0 = mb * 128, c0 = cb * 128;
+    const int64_t ncb = cols / 128, nmb = rows / 128;
+    const int64_t ntiles = ncb * nmb;
 
+    int64_t tile_id = blockIdx.x;
     uint4 v[8];
+    auto load_tile = [&](int64_t id) {
+        const int64_t mb = id / ncb, cb = id - mb * ncb;
+        const uint16_t *src = x + (mb * 128 + rr) * ldx + cb * 128 + g * 8;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = ldg_stream(x + (r0 + rr + 16 * i) * ldx + c0 + g * 8);
+        for (int i = 0; i < 8; ++i) v[i] = ldg_stream(src + 16 * i * ldx);
+    };
+    if (tile_id < ntiles) load_tile(tile_id);
 
-    uint32_t cm0 = 0, cm1 = 0, cm2 = 0, cm3 = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = rr + 16 * i;
-        uint32_t m = absmax8(v[i]);
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        if (m >= 0x7F80u && g == 0) set_status(status, FP8_ERR_NONFINITE);
-        const float sc = scale_from_amax_bits(m, FMT);
-        const Divider d(sc);
-        *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = quant8<FMT>(v[i], d);
-        if (g == 0) s[cb * rows + r0 + row] = sc;
-        *reinterpret_cast<uint4 *>(tile + row * 256 + ((g ^ ((row >> 2) & 7)) << 4)) = v[i];
-        cm0 = bf16x2_absmax(cm0, bf16x2_abs(v[i].x));
-        cm1 = bf16x2_absmax(cm1, bf16x2_abs(v[i].y));
-        cm2 = bf16x2_absmax(cm2, bf16x2_abs(v[i].z));
-        cm3 = bf16x2_absmax(cm3, bf16x2_abs(v[i].w));
-    }
-    // lanes l and l^16 hold rows rr and rr+1 of the same columns
-    cm0 = bf16x2_absmax(cm0, __shfl_xor_sync(0xffffffffu, cm0, 16));
-    cm1 = bf16x2_absmax(cm1, __shfl_xor_sync(0xffffffffu, cm1, 16));
-    cm2 = bf16x2_absmax(cm2, __shfl_xor_sync(0xffffffffu, cm2, 16));
-    cm3 = bf16x2_absmax(cm3, __shfl_xor_sync(0xffffffffu, cm3, 16));
-    if (lane < 16) {
-        uint32_t *p = colpart + warp * 128 + g * 8;
-        p[0] = cm0 & 0xFFFFu; p[1] = cm0 >> 16;
-        p[2] = cm1 & 0xFFFFu; p[3] = cm1 >> 16;
-        p[4] = cm2 & 0xFFFFu; p[5] = cm2 >> 16;
-        p[6] = cm3 & 0xFFFFu; p[7] = cm3 >> 16;
-    }
-    __syncthreads();
-    if (t < 128) {
-        uint32_t m = 0;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) m = max(m, colpart[w * 128 + t]);
-        if (m >= 0x7F80u) set_status(status, FP8_ERR_NONFINITE);
-        const float sc = scale_from_amax_bits(m, FMT);
-        ColDiv c;
-        c.s = sc;
-        c.fast = (sc >= 0x1p-125f) && (sc <= 0x1p125f);
-        c.r = c.fast ? __frcp_rn(sc) : 0.0f;
-        cdiv[t] = c;
-        sT[mb * cols + c0 + t] = sc;
-    }
-    __syncthreads();
+    for (; tile_id < ntiles; tile_id += gridDim.x) {
+        const int64_t mb = tile_id / ncb, cb = tile_id - mb * ncb;
+        const int64_t r0 = mb * 128, c0 = cb * 128;
 
-    const int cw = (lane >> 3) + 4 * warp;   // 4 columns 4cw .. 4cw+3
-    const ColDiv d0 = cdiv[4 * cw], d1 = cdiv[4 * cw + 1], d2 = cdiv[4 * cw + 2], d3 = cdiv[4 * cw + 3];
+        uint32_t cm0 = 0, cm1 = 0, cm2 = 0, cm3 = 0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int mg = (lane & 7) + 8 * k;   // rows 4mg .. 4mg+3
-        uint32_t o0 = 0, o1 = 0, o2 = 0, o3 = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int row = 4 * mg + i;
-            const uint2 pr = *reinterpret_cast<const uint2 *>(
-                tile + row * 256 + (((cw >> 1) ^ ((row >> 2) & 7)) << 4) + ((cw & 1) << 3));
-            const uint32_t c01 = cvt2<FMT>(div_col<FMT>(bf16_lo(pr.x), d0), div_col<FMT>(bf16_hi(pr.x), d1));
-            const uint32_t c23 = cvt2<FMT>(div_col<FMT>(bf16_lo(pr.y), d2), div_col<FMT>(bf16_hi(pr.y), d3));
-            o0 |= (c01 & 0xFFu) << (8 * i);
-            o1 |= (c01 >> 8) << (8 * i);
-            o2 |= (c23 & 0xFFu) << (8 * i);
-            o3 |= (c23 >> 8) << (8 * i);
+        for (int i = 0; i < 8; ++i) {
+            const int row = rr + 16 * i;
+            uint32_t m = absmax8(v[i]);
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            if (m >= 0x7F80u && g == 0) set_status(status, FP8_ERR_NONFINITE);
+            const float sc = scale_from_amax_bits(m, FMT);
+            const Divider2 d(sc);
+            *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = quant8p<FMT>(v[i], d);
+            if (g == 0) s[cb * rows + r0 + row] = sc;
+            *reinterpret_cast<uint4 *>(tile + row * 256 + ((g ^ ((row >> 2) & 7)) << 4)) = v[i];
+            cm0 = bf16x2_absmax(cm0, bf16x2_abs(v[i].x));
+            cm1 = bf16x2_absmax(cm1, bf16x2_abs(v[i].y));
+            cm2 = bf16x2_absmax(cm2, bf16x2_abs(v[i].z));
+            cm3 = bf16x2_absmax(cm3, bf16x2_abs(v[i].w));
         }
-        uint8_t *dst = qT + (c0 + 4 * cw) * rows + r0 + 4 * mg;
-        *reinterpret_cast<uint32_t *>(dst) = o0;
-        *reinterpret_cast<uint32_t *>(dst + rows) = o1;
-        *reinterpret_cast<uint32_t *>(dst + 2 * rows) = o2;
-        *reinterpret_cast<uint32_t *>(dst + 3 * rows) = o3;
+        // lanes l and l^16 hold rows rr and rr+1 of the same columns
+        cm0 = bf16x2_absmax(cm0, __shfl_xor_sync(0xffffffffu, cm0, 16));
+        cm1 = bf16x2_absmax(cm1, __shfl_xor_sync(0xffffffffu, cm1, 16));
+        cm2 = bf16x2_absmax(cm2, __shfl_xor_sync(0xffffffffu, cm2, 16));
+        cm3 = bf16x2_absmax(cm3, __shfl_xor_sync(0xffffffffu, cm3, 16));
+        if (lane < 16) {
+            uint32_t *p = colpart + warp * 128 + g * 8;
+            p[0] = cm0 & 0xFFFFu; p[1] = cm0 >> 16;
+            p[2] = cm1 & 0xFFFFu; p[3] = cm1 >> 16;
+            p[4] = cm2 & 0xFFFFu; p[5] = cm2 >> 16;
+            p[6] = cm3 & 0xFFFFu; p[7] = cm3 >> 16;
+        }
+        __syncthreads();
+        if (t < 64) {
+            float sc[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t m = 0;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) m = max(m, colpart[w * 128 + 2 * t + h]);
+                if (m >= 0x7F80u) set_status(status, FP8_ERR_NONFINITE);
+                sc[h] = scale_from_amax_bits(m, FMT);
+            }
+            ColDiv2 c;
+            c.s0 = sc[0];
+            c.s1 = sc[1];
+            c.fast = (sc[0] >= 0x1p-125f) && (sc[0] <= 0x1p125f) && (sc[1] >= 0x1p-125f) && (sc[1] <= 0x1p125f);
+            const float ra = c.fast ? __frcp_rn(sc[0]) : 0.0f, rb = c.fast ? __frcp_rn(sc[1]) : 0.0f;
+            c.r2 = f2_pack(ra, rb);
+            c.ns2 = f2_pack(-sc[0], -sc[1]);
+            cdiv[t] = c;
+            *reinterpret_cast<float2 *>(sT + mb * cols + c0 + 2 * t) = make_float2(sc[0], sc[1]);
+        }
+        __syncthreads();
+        // the next tile's loads fly during the transposed quantization
+        if (tile_id + gridDim.x < ntiles) load_tile(tile_id + gridDim.x);
+
+        const int cw = (lane >> 3) + 4 * warp;   // columns 4cw .. 4cw+3
+        const ColDiv2 d01 = cdiv[2 * cw], d23 = cdiv[2 * cw + 1];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int mg = (lane & 7) + 8 * k;   // rows 4mg .. 4mg+3
+            uint32_t rw[4];                      // codes of row 4mg+i, columns 4cw..4cw+3
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int row = 4 * mg + i;
+                const uint2 pr = *reinterpret_cast<const uint2 *>(
+                    tile + row * 256 + (((cw >> 1) ^ ((row >> 2) & 7)) << 4) + ((cw & 1) << 3));
+                rw[i] = (quant_pair_cols<FMT>(pr.x, d01) | (quant_pair_cols<FMT>(pr.y, d23) << 16)) |
+                        sign_bits4(pr.x, pr.y);
+            }
+            const uint32_t t0 = __byte_perm(rw[0], rw[1], 0x5140), t1 = __byte_perm(rw[2], rw[3], 0x5140);
+            const uint32_t t2 = __byte_perm(rw[0], rw[1], 0x7362), t3 = __byte_perm(rw[2], rw[3], 0x7362);
+            uint8_t *dst = qT + (c0 + 4 * cw) * rows + r0 + 4 * mg;
+            *reinterpret_cast<uint32_t *>(dst) = __byte_perm(t0, t1, 0x5410);
+            *reinterpret_cast<uint32_t *>(dst + rows) = __byte_perm(t0, t1, 0x7632);
+            *reinterpret_cast<uint32_t *>(dst + 2 * rows) = __byte_perm(t2, t3, 0x5410);
+            *reinterpret_cast<uint32_t *>(dst + 3 * rows) = __byte_perm(t2, t3, 0x7632);
+        }
+        __syncthreads();   // the tile buffer is rewritten by the next iteration
     }
 }
 
@@ -253,12 +281,12 @@ __global__ void __launch_bounds__(256) k_quant_128x128(const uint16_t *__restric
     for (int i = 1; i < 8; ++i) m = max(m, red[i]);
     if (m >= 0x7F80u && t == 0) set_status(status, FP8_ERR_NONFINITE);
     const float sc = scale_from_amax_bits(m, FMT);
-    const Divider d(sc);
+    const Divider2 d(sc);
     const int64_t ncb = cols / 128, nrb = rows / 128;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int row = rr + 16 * i;
-        const uint2 c = quant8<FMT>(v[i], d);
+        const uint2 c = quant8p<FMT>(v[i], d);
         *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = c;
         if (TRANS) {
             ct[row * 33 + 2 * g] = c.x;
@@ -321,15 +349,16 @@ static int quant_1x128_fmt(const void *x, int64_t rows, int64_t cols, int64_t ld
                 return FP8_ERR_CUDA;
             attr_done[dev & 63] = true;
         }
-        dim3 grid((unsigned)(cols / 128), (unsigned)(rows / 128));
-        k_quant_1x128_fused_t<FMT><<<grid, 256, kFusedSmem, st>>>(
+        const int64_t ntiles = (rows / 128) * (cols / 128);
+        const int64_t grid = std::min<int64_t>(ntiles, (int64_t)sm_count() * 4);
+        k_quant_1x128_fused_t<FMT><<<(unsigned)grid, 256, kFusedSmem, st>>>(
             static_cast<const uint16_t *>(x), rows, cols, ldx, static_cast<uint8_t *>(q), s,
             static_cast<uint8_t *>(qT), sT, status);
         return check_launch();
     }
-    constexpr int U = 4;
-    const int64_t ntiles = rows * (cols / 128);
-    int64_t blocks = (ntiles + 16 * U - 1) / (16 * U);
+    constexpr int U = 8;
+    const int64_t items = rows * ((cols / 128 + U - 1) / U);
+    int64_t blocks = (items + 15) / 16;
     const int64_t cap = (int64_t)sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;

@@ -173,8 +173,8 @@ FP8FG_API size_t fp8_pertensor_workspace_bytes(void);
  * amax_history[step % L], sets *scale = s_{t+1} = m * 2^margin / fmax with
  * m = max(history) (or this step's amax for FP8_AMAX_MOST_RECENT; unchanged
  * if m == 0) and increments *step -- all on the device, no host round trip.
- * x: BF16 [rows][ldx], cols % 16 == 0.  q: [rows][cols].  qT (optional, then
- * rows % 128 == 0 and cols % 128 == 0): [cols][rows] = q^T for the wgrad
+ * x: BF16 [rows][ldx], any rows, cols % 128 == 0.  q: [rows][cols].  qT
+ * (optional, then rows % 128 == 0): [cols][rows] = q^T for the wgrad
  * operand.  stats (optional): monitors with the whole tensor as one group.
  * workspace: fp8_pertensor_workspace_bytes() bytes, see above.  Calls that
  * share one workspace must not overlap on the GPU. */
@@ -241,8 +241,9 @@ FP8FG_API int fp8_grouped_gemm(int G, const int32_t *group_offsets, int64_t M_ca
  * row_token[r] = token, row_prob[r] = its probability (0 for padding),
  * row_is_pad[r] (optional) = 1 for padding.  Rows from group_offsets[E] to
  * M_capacity get row_token = -1, row_prob = 0.  The total must fit
- * M_capacity (else FP8_ERR_INVALID_ARG on the device); T*topk + E*(align-1)
- * always fits.  1 <= topk <= min(E, 8), align in {1..1024}. */
+ * M_capacity and every padded count must be reachable with distinct tokens
+ * (else FP8_ERR_INVALID_ARG on the device); T*topk + E*(align-1) always fits
+ * M_capacity.  1 <= topk <= min(E, 8), align in {1..1024}. */
 FP8FG_API int fp8_moe_route_pad(const float *logits, int64_t T, int E, int topk, int align,
                                 int64_t M_capacity, int32_t *topk_idx, float *topk_prob,
                                 int32_t *counts, int32_t *group_offsets, int32_t *row_token,

@@ -37,7 +37,8 @@
  *  R5  Delayed scaling: s_0 = 1; at step t quantize with s_t, write amax_t
  *      into history slot t mod L, s_{t+1} = max(history) * 2^margin / fmax
  *      (or the most recent amax for the "most recent" algorithm); if that
- *      amax is 0, s_{t+1} = s_t.
+ *      amax is 0, s_{t+1} = s_t.  A step whose tensor holds Inf/NaN is
+ *      reported and leaves history, scale and step unchanged.
  *  R6  Monitors: underflow = #(x != 0 and q is +-0) ; distortion is reported
  *      as a retention ratio distinct(q) / distinct(x) summed over scaling
  *      groups, +-0 counted as one value on both sides; saturated =
@@ -534,6 +535,9 @@ int orc_delayed_step(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx,
         float one_scale = s_t;
         orc_quant_stats(x, rows, cols, ldx, q, &one_scale, ORC_GRAN_TENSOR, fmt, stats);
     }
+    /* A step whose tensor holds Inf/NaN reports it and leaves the state as it
+     * was (reading R5: a non-finite amax must not enter the history). */
+    if (bad) return ORC_NONFINITE;
     /* 2. record this step's amax; 3. next scale from the history */
     hist[*step % hist_len] = amax;
     if (algo == ORC_ALGO_MOST_RECENT) {
@@ -545,7 +549,7 @@ int orc_delayed_step(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx,
     }
     if (m > 0.0f) *scale = ldexpf(m, margin) / (float)fmt_of(fmt).fmax;
     *step += 1;
-    return bad ? ORC_NONFINITE : ORC_OK;
+    return ORC_OK;
 }
 
 /* ---------------------------------------------------------------------------

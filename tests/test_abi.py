@@ -1,0 +1,95 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/fp8fg.h declares; host-side argument validation rejects bad calls
+with the documented status before touching the GPU (runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_fine_grained_x128_gb300 as fg
+from fp8_fine_grained_x128_gb300 import build as fgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fgbuild.build()
+    return fg.lib()
+
+
+def declared_symbols():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, f)).read()
+        names += re.findall(r"FP8FG_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_binding_covers_the_abi():
+    assert set(declared_symbols()) <= set(fg._SIGS), set(declared_symbols()) - set(fg._SIGS)
+
+
+def test_version_and_strings(lib):
+    assert lib.fp8_abi_version() == 1
+    assert fg.status_string(fg.ERR_SHAPE) == "FP8_ERR_SHAPE"
+    assert fg.status_string(fg.ERR_TIMEOUT) == "FP8_ERR_TIMEOUT"
+    assert fg.status_string(99) == "FP8_ERR_UNKNOWN"
+    assert fg.workspace_bytes() >= 8192
+
+
+def test_host_validation_without_launch(lib):
+    P = ctypes.c_void_p
+    good = P(4096)            # a 16-byte aligned (never dereferenced) address
+    odd = P(4097)
+    S = None
+    # quantizer: cols not a multiple of 128, bad format, misaligned, negative rows
+    assert lib.fp8_quant_1x128(good, 4, 100, 100, 0, good, good, None, None, S) == fg.ERR_SHAPE
+    assert lib.fp8_quant_1x128(good, 4, 128, 128, 7, good, good, None, None, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_quant_1x128(odd, 4, 128, 128, 0, good, good, None, None, S) == fg.ERR_ALIGNMENT
+    assert lib.fp8_quant_1x128(good, -1, 128, 128, 0, good, good, None, None, S) == fg.ERR_SHAPE
+    assert lib.fp8_quant_1x128(good, 100, 128, 128, 0, good, good, good, good, S) == fg.ERR_SHAPE  # T needs rows%128
+    assert lib.fp8_quant_1x128(good, 128, 128, 128, 0, good, good, good, None, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_quant_1x128(good, 0, 128, 128, 0, None, None, None, None, S) == fg.OK          # empty
+    assert lib.fp8_quant_128x128(good, 100, 128, 128, 0, good, good, None, None, S) == fg.ERR_SHAPE
+    assert lib.fp8_transpose_128x128(good, good, 128, 64, good, good, S) == fg.ERR_SHAPE
+    # GEMM: shapes, mixed TENSOR granularity, bad output dtype, misaligned ldD
+    g = lambda M, N, K, ga=0, gb=1, out=0, ld=None, A=good: lib.fp8_blockscaled_gemm(
+        M, N, K, A, 0, good, ga, good, 0, good, gb, good, out, N if ld is None else ld, S)
+    assert g(100, 128, 128) == fg.ERR_SHAPE
+    assert g(128, 128, 100) == fg.ERR_SHAPE
+    assert g(128, 128, 128, ga=2, gb=1) == fg.ERR_UNSUPPORTED
+    assert g(128, 128, 128, out=3) == fg.ERR_INVALID_ARG
+    assert g(128, 128, 128, ld=100) == fg.ERR_SHAPE
+    assert g(128, 128, 128, ld=132) == fg.ERR_ALIGNMENT
+    assert g(128, 128, 128, A=odd) == fg.ERR_ALIGNMENT
+    assert g(0, 128, 128) == fg.OK
+    # grouped GEMM and MoE glue
+    assert lib.fp8_grouped_gemm(0, good, 128, 128, 128, good, good, good, good, good, 0, 128, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_grouped_gemm(2, good, 100, 128, 128, good, good, good, good, good, 0, 128, S) == fg.ERR_SHAPE
+    assert lib.fp8_moe_route_pad(good, 16, 300, 8, 128, 1024, good, good, good, good, good, good, None, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_moe_route_pad(good, 16, 8, 9, 128, 1024, good, good, good, good, good, good, None, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_swiglu_fwd(good, 4, 12, good, S) == fg.ERR_SHAPE
+    # delayed scaling: recipe checks
+    rec = fg.DelayedRecipe(0, 0, 0, 0)
+    assert lib.fp8_quant_pertensor_delayed(good, 128, 128, 128, ctypes.byref(rec), good, good, good, good,
+                                           None, None, good, S) == fg.ERR_INVALID_ARG
+    rec = fg.DelayedRecipe(0, 16, 200, 0)
+    assert lib.fp8_quant_pertensor_delayed(good, 128, 128, 128, ctypes.byref(rec), good, good, good, good,
+                                           None, None, good, S) == fg.ERR_INVALID_ARG
+    rec = fg.DelayedRecipe(1, 16, 0, 1)
+    assert lib.fp8_quant_pertensor_delayed(good, 128, 100, 128, ctypes.byref(rec), good, good, good, good,
+                                           None, None, good, S) == fg.ERR_SHAPE
+    assert lib.fp8_selftest_wait_timeout(0, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_device_status(S, None) == fg.ERR_INVALID_ARG

@@ -50,7 +50,7 @@ def check_route(z, topk, align):
     return g, ref
 
 
-@pytest.mark.parametrize("T,E,topk,align", [(512, 16, 4, 128), (1000, 40, 3, 8), (256, 8, 8, 128), (96, 1, 1, 128)])
+@pytest.mark.parametrize("T,E,topk,align", [(512, 16, 4, 128), (1000, 40, 3, 8), (256, 8, 8, 128), (256, 1, 1, 128), (96, 2, 1, 32)])
 def test_route_pad_small(T, E, topk, align):
     z = synth.f32_normal((T, E), 5)
     z[3, :] = 0.25
@@ -61,6 +61,21 @@ def test_route_pad_small(T, E, topk, align):
 def test_route_pad_full_size():
     _, logits, _, _ = synth.moe_inputs()
     check_route(logits, 8, 128)
+
+
+def test_route_pad_impossible_padding_is_reported():
+    # 96 tokens all routed to the single expert cannot be padded to 128 distinct tokens
+    z = synth.f32_normal((96, 1), 5)
+    cap = 256
+    logits = dev_f32(z)
+    ti = torch.empty((96, 1), dtype=torch.int32, device="cuda")
+    tp = torch.empty((96, 1), dtype=torch.float32, device="cuda")
+    counts = torch.empty(1, dtype=torch.int32, device="cuda")
+    offs = torch.empty(2, dtype=torch.int32, device="cuda")
+    rt = torch.empty(cap, dtype=torch.int32, device="cuda")
+    rp = torch.empty(cap, dtype=torch.float32, device="cuda")
+    fg.moe_route_pad(logits, 1, 128, cap, ti, tp, counts, offs, rt, rp)
+    assert fg.device_status() == fg.ERR_INVALID_ARG
 
 
 def test_gather_bit_exact():

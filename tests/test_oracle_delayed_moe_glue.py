@@ -72,6 +72,17 @@ def test_checkpoint_split_invariant():
     assert np.array_equal(a.hist, c.hist) and a.scale[0] == c.scale[0] and a.step[0] == c.step[0]
 
 
+def test_nonfinite_step_leaves_state_unchanged():
+    st = oracle.DelayedState(4)
+    oracle.delayed_step(tensor_with_amax(3.0, 0), st, oracle.E4M3)
+    before = st.copy()
+    x = tensor_with_amax(5.0, 1)
+    x[0, 0] = 0x7FC0                      # NaN
+    _, _, _, code = oracle.delayed_step(x, st, oracle.E4M3)
+    assert code == oracle.NONFINITE
+    assert np.array_equal(st.hist, before.hist) and st.scale[0] == before.scale[0] and st.step[0] == before.step[0]
+
+
 def test_drift_saturates_then_recovers():
     # the scale is one step late: a x1.5 jump saturates the elements above the
     # old amax / 1.5 once, and the next step (same magnitude) saturates nothing
