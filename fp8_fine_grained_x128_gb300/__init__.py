@@ -71,6 +71,8 @@ _SIGS = {
     "fp8_pertensor_workspace_bytes": (ctypes.c_size_t, []),
     "fp8_quant_pertensor_delayed": (_INT, [_VP, _I64, _I64, _I64, ctypes.POINTER(DelayedRecipe),
                                            _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "fp8_quant_pertensor_delayed_noalloc": (_INT, [_VP, _I64, _I64, _I64, ctypes.POINTER(DelayedRecipe),
+                                                   _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "fp8_quant_stats": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _INT, _INT, _VP, _VP, _VP]),
     "fp8_blockscaled_gemm": (_INT, [_I64, _I64, _I64, _VP, _INT, _VP, _INT, _VP, _INT, _VP, _INT,
                                     _VP, _INT, _I64, _VP]),
@@ -183,6 +185,17 @@ def quant_pertensor_delayed(x, recipe: DelayedRecipe, hist, step, scale, q, work
            lib().fp8_quant_pertensor_delayed(_p(x), R, C, ld, ctypes.byref(recipe), _p(hist), _p(step),
                                              _p(scale), _p(q), _p(qT), _p(stats), _p(workspace),
                                              _stream(stream)))
+
+
+def quant_pertensor_delayed_noalloc(x, recipe: DelayedRecipe, hist, step, scale, q, qT=None, stats=None,
+                                    stream=None):
+    """The delayed-scaling step without a caller workspace, for callers that
+    cannot allocate device memory (the library's own scratch block is used;
+    calls that overlap on the GPU race on it)."""
+    R, C, ld = _rows_cols(x)
+    _check("fp8_quant_pertensor_delayed_noalloc",
+           lib().fp8_quant_pertensor_delayed_noalloc(_p(x), R, C, ld, ctypes.byref(recipe), _p(hist), _p(step),
+                                                     _p(scale), _p(q), _p(qT), _p(stats), _stream(stream)))
 
 
 def quant_stats(x, q, s, gran, fmt, stats, workspace=None, stream=None):

@@ -40,6 +40,8 @@ static int *status_ptr()
     return g_status_ptr[dev];
 }
 
+int *status_word_ptr() { return status_ptr(); }
+
 int sm_count()
 {
     const int dev = current_device();

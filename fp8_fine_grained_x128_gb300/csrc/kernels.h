@@ -10,6 +10,9 @@ namespace fp8fg {
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Device address of the current device's status word (nullptr on failure).
+int *status_word_ptr();
+
 // quant.cu
 int launch_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, void *q, float *s,
                        void *qT, float *sT, int *status, cudaStream_t st);

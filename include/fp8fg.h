@@ -183,6 +183,27 @@ FP8FG_API int fp8_quant_pertensor_delayed(const void *x, int64_t rows, int64_t c
                                           int32_t *step, float *scale, void *q, void *qT,
                                           fp8_stats_t *stats, void *workspace, void *stream);
 
+/* The same delayed-scaling step for callers that cannot allocate device
+ * memory -- for example code that runs inside another framework's fixed
+ * memory plan or arena, or a plugin that is handed buffers but no allocator.
+ * The pages have no counterpart: this is a library convenience.
+ * Instead of a caller-owned workspace it uses a 16 KiB scratch block that the
+ * library keeps in device memory for every GPU that loads it (until process
+ * exit); the step needs fp8_pertensor_workspace_bytes() of it whatever the
+ * tensor size, and a call returns FP8_ERR_UNSUPPORTED if that ever exceeded
+ * the block.  The caller still passes x, the state and the outputs exactly as
+ * for fp8_quant_pertensor_delayed, and results are identical.  The call
+ * allocates nothing; it clears the scratch on `stream` before the kernel
+ * (cudaMemsetAsync).  All calls share the one block, so calls that may run
+ * at the same time on the GPU (different streams without ordering) race on
+ * it.  The first call on each device looks up the block's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. */
+FP8FG_API int fp8_quant_pertensor_delayed_noalloc(const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                                                  const fp8_delayed_recipe_t *recipe, float *amax_history,
+                                                  int32_t *step, float *scale, void *q, void *qT,
+                                                  fp8_stats_t *stats, void *stream);
+
 /* Monitors of an existing quantization ([Ling] underflow / distortion
  * monitors), accumulated into *stats.  x: BF16 [rows][ldx]; q and s follow
  * `gran` (1x128, 128x128, TENSOR: q is [rows][cols]; 128x1: q is the
