@@ -65,6 +65,8 @@ __device__ __forceinline__ float scale_from_amax_bits(uint32_t amax_bf16_bits, i
 // e = x - q0*s is exact under FMA and RN(q0 + e*r) is the correctly rounded
 // quotient.  Valid while s and 1/s are normal and nothing overflows; callers
 // use it only when 2^-125 <= s <= 2^125 and fall back to __fdiv_rn otherwise.
+// A quotient that overflows (or x = +-Inf) turns q0 into +-Inf and q into NaN:
+// such a NaN from a non-NaN x is redone by __fdiv_rn.
 // The sign is forced from x so that -0 / s = -0 like the IEEE division.
 struct Divider {
     float s, r;
@@ -80,6 +82,7 @@ struct Divider {
             float q0 = __fmul_rn(x, r);
             float e = __fmaf_rn(-q0, s, x);
             float q = __fmaf_rn(e, r, q0);
+            if (q != q) return __fdiv_rn(x, s);
             return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
         }
         return __fdiv_rn(x, s);
@@ -90,7 +93,10 @@ struct Divider {
 // q0 = x*r, e = x - q0*s (exact), q = q0 + e*r, two lanes per instruction
 // (fma.rn.f32x2 rounds each lane like the scalar instruction).  For x = -0
 // it returns +0; callers restore the sign bit of zero quotients from x with
-// sign_bits4() on the codes.
+// sign_bits4() on the codes.  Like the scalar form it gives NaN where x / s
+// overflows or x = +-Inf; quantizers whose scale cannot make x / s overflow
+// (scales from the group's own amax) need no check, the others redo a group
+// whose codes hold a NaN with __fdiv_rn (has_nan_code).
 struct Divider2 {
     uint64_t r2, ns2;
     float s;
@@ -126,6 +132,17 @@ struct Divider2 {
 __device__ __forceinline__ uint32_t sign_bits4(uint32_t w0, uint32_t w1)
 {
     return __byte_perm(w0, w1, 0x7531) & 0x80808080u;
+}
+
+// True if one of the four codes in w is a NaN code (E4M3 S.1111.111, E5M2
+// S.11111.xx with xx != 0; satfinite conversion produces no E5M2 infinity, so
+// every code with an all-ones exponent is a NaN).
+template <int FMT>
+__device__ __forceinline__ bool has_nan_code(uint32_t w)
+{
+    constexpr uint32_t kMask = FMT == FP8_E4M3 ? 0x7F7F7F7Fu : 0x7C7C7C7Cu;
+    constexpr uint32_t kAdd = FMT == FP8_E4M3 ? 0x01010101u : 0x04040404u;
+    return (((w & kMask) + kAdd) & 0x80808080u) != 0;
 }
 
 // FP8 encode of two binary32 values (round to nearest even, saturating to

@@ -46,6 +46,7 @@ namespace fp8fg {
 constexpr int kGemmThreads = 384;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiWarp0 = 4;          // first epilogue warp (warpgroups 1 and 2)
+constexpr int kStageReleaseWarp = 7;  // epilogue warp that frees smem stages in promote mode
 constexpr int kCtrlRegs = 144;         // setmaxnreg of the control warpgroup
 constexpr int kEpiRegs = 176;         // setmaxnreg of the epilogue warpgroups
 // the split must fit the registers the CTA is launched with
@@ -290,10 +291,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         tc_mma_f8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
                                       (k > 0 || (!PROMOTE && kb > 0)) ? 1u : 0u);
                     }
-                    tc_commit(&empty[s]);
                     if (PROMOTE) {
+                        // one commit per chunk: when the accumulator is complete its
+                        // smem stage is no longer read, so the epilogue frees both
                         tc_commit(&tfull[buf]);
                         ++cc;
+                    } else {
+                        tc_commit(&empty[s]);
                     }
                     ++it;
                 }
@@ -376,6 +380,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     // 128x128 B: sA*sB of this thread's row and column half; 1x128 B: sA of the row
                     const float sr = sv[(SBG == SB_BLOCK ? (ew >> 2) * 128 : 0) + row];
                     if (!warp_wait_or_abort(&tfull[buf], (cc >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                    // the chunk's MMAs are complete, so its smem stage is no longer read
+                    if (warp == kStageReleaseWarp && lane == 0) mbar_arrive(&empty[cc % STAGES]);
                     tc_fence_after();
                     const uint64_t s2 = f2_pack(sr, sr);
                     if (SBG == SB_BLOCK) {

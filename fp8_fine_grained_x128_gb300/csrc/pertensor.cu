@@ -45,8 +45,11 @@ struct Counts {
 };
 
 // Quantize 8 BF16 values with one scale and (optionally) account the monitors.
+// The distinct-code count of a quantization done here needs no per-element
+// code bitmap: q = enc(x / s) is a function of x, so the distinct codes are the
+// image of the distinct inputs, which the last CTA encodes once.
 template <int FMT, bool STATS>
-__device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &c, uint32_t *bmx, uint32_t *bmq)
+__device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &c, uint32_t *bmx)
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float qv[8];
@@ -55,6 +58,17 @@ __device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &
     uint2 out;
     out.x = (cvt2<FMT>(qv[0], qv[1]) | (cvt2<FMT>(qv[2], qv[3]) << 16)) | sign_bits4(v.x, v.y);
     out.y = (cvt2<FMT>(qv[4], qv[5]) | (cvt2<FMT>(qv[6], qv[7]) << 16)) | sign_bits4(v.z, v.w);
+    if (has_nan_code<FMT>(out.x) || has_nan_code<FMT>(out.y)) {
+        // x NaN, x = +-Inf, or x / s overflowed in the fast division (the
+        // scale comes from earlier steps): the IEEE quotients decide
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            qv[2 * j] = __fdiv_rn(__uint_as_float(w[j] << 16), d.s);
+            qv[2 * j + 1] = __fdiv_rn(__uint_as_float(w[j] & 0xFFFF0000u), d.s);
+        }
+        out.x = (cvt2<FMT>(qv[0], qv[1]) | (cvt2<FMT>(qv[2], qv[3]) << 16)) | sign_bits4(v.x, v.y);
+        out.y = (cvt2<FMT>(qv[4], qv[5]) | (cvt2<FMT>(qv[6], qv[7]) << 16)) | sign_bits4(v.z, v.w);
+    }
     if (STATS) {
         const float fm = fmax_of(FMT);
 #pragma unroll
@@ -66,7 +80,6 @@ __device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &
             c.uf += nzero && ((code & 0x7Fu) == 0);
             c.sat += fabsf(qv[e]) > fm;
             bitmap_set(bmx, key_bf16(xb));
-            bitmap_set(bmq, key_fp8(code));
         }
     }
     return out;
@@ -125,6 +138,35 @@ __device__ bool merge_and_ticket(const Counts &c, uint32_t amax, const uint32_t 
     if (threadIdx.x == 0) *is_last = (atomicAdd(&ws->ticket, 1u) == gridDim.x - 1);
     __syncthreads();
     return *is_last != 0;
+}
+
+// In the last CTA of a delayed-scaling step: the codes of the distinct inputs
+// are marked in the workspace's code bitmap before the counts are taken.
+template <int FMT>
+__device__ void mark_codes_of_distinct_inputs(PtWorkspace *ws, const Divider2 &d)
+{
+    uint32_t m[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // this thread's 256-bit code set
+    for (int i = threadIdx.x; i < 2048; i += blockDim.x) {
+        uint32_t w = __ldcg(&ws->bmx[i]);
+        while (w) {
+            const int bit = __ffs(w) - 1;
+            w &= w - 1;
+            const uint32_t key = (uint32_t)i * 32 + bit;      // BF16 bits (+-0 folded to +0)
+            float lo, hi;
+            d(key, lo, hi);                                   // the key is the low half of the word
+            if (lo != lo) lo = __fdiv_rn(__uint_as_float(key << 16), d.s);   // overflow, Inf or NaN
+            const uint32_t code = key_fp8(cvt2<FMT>(lo, lo) & 0xFFu);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m[j] |= ((code >> 5) == (uint32_t)j) ? (1u << (code & 31)) : 0u;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m[j] |= __shfl_xor_sync(0xffffffffu, m[j], o);
+        if ((threadIdx.x & 31) == 0 && m[j]) atomicOr(&ws->bmq[j], m[j]);
+    }
+    __syncthreads();
 }
 
 // In the last CTA: distinct counts from the merged bitmaps, workspace reset.
@@ -196,7 +238,7 @@ __global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__res
             const int row = rr + 16 * i;
             if (r0 + row < rows) {
                 amax = max(amax, absmax8(v[i]));
-                const uint2 code = quant8_mon<FMT, STATS>(v[i], d, c, bmx, bmq);
+                const uint2 code = quant8_mon<FMT, STATS>(v[i], d, c, bmx);
                 *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = code;
                 if (TRANS) {
                     ct[row * 33 + 2 * g] = code.x;
@@ -231,6 +273,10 @@ __global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__res
     if (!merge_and_ticket<STATS>(c, amax, bmx, bmq, stats, ws, red, &is_last)) return;
 
     // ---- last CTA: state update (history slot, next scale, step) ----
+    if (STATS) {
+        __threadfence();
+        mark_codes_of_distinct_inputs<FMT>(ws, d);
+    }
     finalize_distinct_and_reset<STATS>(stats, ws, red);
     if (t == 0) {
         const uint32_t a = atomicExch(&ws->amax_bits, 0u);
@@ -259,71 +305,80 @@ __global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__res
 // Monitors of an existing quantization.
 // ---------------------------------------------------------------------------
 
-// Groups of 128 elements (1x128 tiles, or 128 rows of one column for the
-// transposed copy): one warp per group, 4 elements per lane; distinct values
-// by comparing every element with all earlier ones through shuffles.
-template <int FMT, bool COLS>
-__global__ void __launch_bounds__(256) k_stats_g128(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
-                                                    int64_t ldx, const uint8_t *__restrict__ q,
-                                                    const float *__restrict__ s, fp8_stats_t *stats)
-{
-    const int lane = threadIdx.x & 31;
-    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t ngroups = COLS ? (rows / 128) * cols : rows * (cols / 128);
-    const float fm = fmax_of(FMT);
-    uint32_t nz = 0, uf = 0, sat = 0, din = 0, dout = 0;
-    for (int64_t gi = warp0; gi < ngroups; gi += nwarps) {
-        uint32_t kx[4], kq[4];
-        float sc;
-        if (COLS) {
-            const int64_t mb = gi / cols, c = gi - mb * cols;
-            sc = s[mb * cols + c];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int64_t r = mb * 128 + j * 32 + lane;
-                kx[j] = x[r * ldx + c];
-                kq[j] = q[c * rows + r];
-            }
+// Saturation test |x / s| > fmax without a division for almost every element:
+// with t = fmax * s rounded, |x| <= t (1 - 2^-20) can only give a quotient below
+// fmax and |x| >= t (1 + 2^-20) only one above it (the quotient's and t's
+// roundings are each within 2^-24 relative, and the next binary32 above fmax is
+// far closer than 2^-21 fmax).  Between the two bounds, and for scales whose t
+// is not a normal number well inside the range, the exact quotient decides.
+struct SatTest {
+    float lo, hi, s;
+    __device__ __forceinline__ explicit SatTest(float s_, float fm) : s(s_)
+    {
+        const float t = __fmul_rn(fm, s_);
+        if (t >= 0x1p-100f && t <= 0x1p100f) {
+            lo = __fmul_rn(t, 1.0f - 0x1p-20f);
+            hi = __fmul_rn(t, 1.0f + 0x1p-20f);
         } else {
-            const int64_t ncb = cols / 128;
-            const int64_t r = gi / ncb, cb = gi - r * ncb;
-            sc = s[cb * rows + r];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                kx[j] = x[r * ldx + cb * 128 + j * 32 + lane];
-                kq[j] = q[r * cols + cb * 128 + j * 32 + lane];
-            }
+            lo = -1.0f;                          // every element takes the exact path
+            hi = __uint_as_float(0x7FC00000u);   // NaN: the fast "saturated" branch never fires
         }
-        const Divider d(sc);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const bool nzero = (kx[j] & 0x7FFFu) != 0;
-            nz += nzero;
-            uf += nzero && ((kq[j] & 0x7Fu) == 0);
-            sat += fabsf(d(__uint_as_float(kx[j] << 16))) > fm;
-            kx[j] = key_bf16(kx[j]);
-            kq[j] = key_fp8(kq[j]);
-        }
-        uint32_t dupx = 0, dupq = 0;   // bit j: element j*32+lane repeats an earlier one
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            for (int src = 0; src < 32; ++src) {
-                const uint32_t ox = __shfl_sync(0xffffffffu, kx[jj], src);
-                const uint32_t oq = __shfl_sync(0xffffffffu, kq[jj], src);
-                const int other = jj * 32 + src;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (other < j * 32 + lane) {
-                        dupx |= (uint32_t)(ox == kx[j]) << j;
-                        dupq |= (uint32_t)(oq == kq[j]) << j;
-                    }
-                }
-            }
-        }
-        din += 4 - __popc(dupx);
-        dout += 4 - __popc(dupq);
     }
+    __device__ __forceinline__ bool operator()(uint32_t xb, float fm) const
+    {
+        const float ax = __uint_as_float((xb & 0x7FFFu) << 16);
+        if (ax >= hi) return true;
+        if (!(ax > lo)) return false;
+        return fabsf(Divider(s)(__uint_as_float(xb << 16))) > fm;
+    }
+};
+
+// Per-warp scratch of the 128-element group monitors: a presence bitmap of the
+// 65536 BF16 keys and one flag byte per FP8 key.  Both are all zero between
+// groups: every group clears exactly what it set.
+struct GroupScratch {
+    uint32_t bx[2048];
+    uint32_t fq[64];
+};
+
+// Monitors of one group of 128 elements, 4 per lane (x as BF16 bits, q as FP8
+// codes, element e of the lane in half e of xv / byte e of qv).  The order of
+// the elements within the group does not matter.  A BF16 key counts as
+// distinct for the lane whose atomic OR set its bit first.
+template <int FMT>
+__device__ __forceinline__ void mon_group(uint2 xv, uint32_t qv, float sc, GroupScratch &g, int lane, uint32_t &nz,
+                                          uint32_t &uf, uint32_t &sat, uint32_t &din, uint32_t &dout)
+{
+    const float fm = fmax_of(FMT);
+    const SatTest st(sc, fm);
+    uint8_t *fqb = reinterpret_cast<uint8_t *>(g.fq);
+    const uint32_t xs[4] = {xv.x & 0xFFFFu, xv.x >> 16, xv.y & 0xFFFFu, xv.y >> 16};
+    uint32_t kx[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t code = (qv >> (8 * e)) & 0xFFu;
+        const bool nzero = (xs[e] & 0x7FFFu) != 0;
+        nz += nzero;
+        uf += nzero && ((code & 0x7Fu) == 0);
+        sat += st(xs[e], fm);
+        kx[e] = key_bf16(xs[e]);
+        const uint32_t bit = 1u << (kx[e] & 31);
+        din += (atomicOr(&g.bx[kx[e] >> 5], bit) & bit) == 0;
+        fqb[key_fp8(code)] = 1;
+    }
+    __syncwarp();
+    const uint32_t f0 = g.fq[lane], f1 = g.fq[lane + 32];
+    dout += __popc(f0) + __popc(f1);          // flag bytes are 0 or 1
+    g.fq[lane] = 0;
+    g.fq[lane + 32] = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) g.bx[kx[e] >> 5] = 0;
+    __syncwarp();
+}
+
+__device__ __forceinline__ void warp_stats_flush(fp8_stats_t *stats, int lane, uint32_t nz, uint32_t uf, uint32_t sat,
+                                                 uint32_t din, uint32_t dout)
+{
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         nz += __shfl_xor_sync(0xffffffffu, nz, o);
@@ -339,6 +394,98 @@ __global__ void __launch_bounds__(256) k_stats_g128(const uint16_t *__restrict__
         atomicAdd(reinterpret_cast<unsigned long long *>(&stats->distinct_in), (unsigned long long)din);
         atomicAdd(reinterpret_cast<unsigned long long *>(&stats->distinct_out), (unsigned long long)dout);
     }
+}
+
+constexpr int kG128Warps = 4;   // 128 threads, 33 KB of group scratch per CTA
+
+__device__ __forceinline__ void clear_group_scratch(GroupScratch &g, int lane)
+{
+    for (int i = lane; i < 2048; i += 32) g.bx[i] = 0;
+    for (int i = lane; i < 64; i += 32) g.fq[i] = 0;
+    __syncwarp();
+}
+
+// 1x128 groups (one row, 128 consecutive columns): one warp per group, four
+// groups loaded ahead of their processing.
+template <int FMT>
+__global__ void __launch_bounds__(kG128Warps * 32) k_stats_1x128(const uint16_t *__restrict__ x, int64_t rows,
+                                                                 int64_t cols, int64_t ldx,
+                                                                 const uint8_t *__restrict__ q,
+                                                                 const float *__restrict__ s, fp8_stats_t *stats)
+{
+    __shared__ GroupScratch scr[kG128Warps];
+    const int lane = threadIdx.x & 31;
+    GroupScratch &g = scr[threadIdx.x >> 5];
+    clear_group_scratch(g, lane);
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t ncb = cols / 128, ngroups = rows * ncb;
+    constexpr int U = 4;
+    uint32_t nz = 0, uf = 0, sat = 0, din = 0, dout = 0;
+    for (int64_t base = warp0; base < ngroups; base += U * nwarps) {
+        uint2 xv[U];
+        uint32_t qv[U];
+        float sc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t gi = base + u * nwarps;
+            if (gi < ngroups) {
+                const int64_t r = gi / ncb, cb = gi - r * ncb;
+                xv[u] = __ldcs(reinterpret_cast<const uint2 *>(x + r * ldx + cb * 128) + lane);
+                qv[u] = __ldcs(reinterpret_cast<const uint32_t *>(q + r * cols + cb * 128) + lane);
+                sc[u] = s[cb * rows + r];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + u * nwarps < ngroups) mon_group<FMT>(xv[u], qv[u], sc[u], g, lane, nz, uf, sat, din, dout);
+    }
+    warp_stats_flush(stats, lane, nz, uf, sat, din, dout);
+}
+
+// 128x1 groups (128 rows of one column; q is the transposed copy qT[C][R] and
+// s is S[R/128][C]).  A CTA stages 128 rows x 32 columns of x in shared
+// memory, transposed, so that every warp reads its columns contiguously.
+template <int FMT>
+__global__ void __launch_bounds__(kG128Warps * 32) k_stats_128x1(const uint16_t *__restrict__ x, int64_t rows,
+                                                                 int64_t cols, int64_t ldx,
+                                                                 const uint8_t *__restrict__ q,
+                                                                 const float *__restrict__ s, fp8_stats_t *stats)
+{
+    constexpr int kPitch = 65;                  // words per staged column: conflict-free transposing stores
+    __shared__ GroupScratch scr[kG128Warps];
+    __shared__ uint32_t xs[32 * kPitch];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    GroupScratch &g = scr[warp];
+    clear_group_scratch(g, lane);
+    uint16_t *xs16 = reinterpret_cast<uint16_t *>(xs);
+    const int64_t ncs = cols / 32, ntiles = (rows / 128) * ncs;
+    uint32_t nz = 0, uf = 0, sat = 0, din = 0, dout = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t mb = tile / ncs, c0 = (tile - mb * ncs) * 32;
+        uint4 v[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)                // row p*32 + t/4, columns (t%4)*8 .. +7
+            v[p] = ldg_stream(x + (mb * 128 + p * 32 + (t >> 2)) * ldx + c0 + (t & 3) * 8);
+        __syncthreads();                           // the previous tile's columns are consumed
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int r = p * 32 + (t >> 2), cc = (t & 3) * 8;
+            const uint32_t w[4] = {v[p].x, v[p].y, v[p].z, v[p].w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                xs16[(cc + k) * (2 * kPitch) + r] = (uint16_t)((k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu));
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 32 / kG128Warps; ++j) {
+            const int c = warp * (32 / kG128Warps) + j;
+            const uint2 xv = make_uint2(xs[c * kPitch + 2 * lane], xs[c * kPitch + 2 * lane + 1]);
+            const uint32_t qv = __ldcs(reinterpret_cast<const uint32_t *>(q + (c0 + c) * rows + mb * 128) + lane);
+            mon_group<FMT>(xv, qv, s[mb * cols + c0 + c], g, lane, nz, uf, sat, din, dout);
+        }
+    }
+    warp_stats_flush(stats, lane, nz, uf, sat, din, dout);
 }
 
 // 128x128 blocks (one CTA per block, shared presence bitmaps) and the whole
@@ -371,7 +518,7 @@ __global__ void __launch_bounds__(256) k_stats_blocks(const uint16_t *__restrict
             if (t < 8) bmq[t] = 0;
             __syncthreads();
         }
-        const Divider d(TENSOR ? s[0] : s[rb * ncb + cb]);
+        const SatTest sat_test(TENSOR ? s[0] : s[rb * ncb + cb], fm);
 #pragma unroll 2
         for (int i = 0; i < 8; ++i) {
             const int64_t r = rb * 128 + rr + 16 * i;
@@ -385,7 +532,7 @@ __global__ void __launch_bounds__(256) k_stats_blocks(const uint16_t *__restrict
                 const bool nzero = (xb & 0x7FFFu) != 0;
                 c.nz += nzero;
                 c.uf += nzero && ((code & 0x7Fu) == 0);
-                c.sat += fabsf(d(__uint_as_float(xb << 16))) > fm;
+                c.sat += sat_test(xb, fm);
                 bitmap_set(bmx, key_bf16(xb));
                 bitmap_set(bmq, key_fp8(code));
             }
@@ -481,19 +628,18 @@ int launch_quant_stats(const void *x, int64_t rows, int64_t cols, int64_t ldx, c
     auto Q = static_cast<const uint8_t *>(q);
     auto S = static_cast<fp8_stats_t *>(stats);
     auto W = static_cast<PtWorkspace *>(ws);
-    const int64_t cap = (int64_t)sm_count() * 8;
     if (gran == FP8_GRAN_1x128 || gran == FP8_GRAN_128x1) {
         const bool cols_mode = gran == FP8_GRAN_128x1;
-        const int64_t groups = cols_mode ? (rows / 128) * cols : rows * (cols / 128);
-        int64_t blocks = (groups + 7) / 8;
-        if (blocks > cap) blocks = cap;
-        const unsigned b = (unsigned)blocks;
+        const int64_t units = cols_mode ? (rows / 128) * (cols / 32) : (rows * (cols / 128) + kG128Warps * 4 - 1) /
+                                                                         (kG128Warps * 4);
+        const int64_t cap = (int64_t)sm_count() * (cols_mode ? 5 : 6);   // CTAs that fit an SM's shared memory
+        const unsigned b = (unsigned)std::max<int64_t>(1, std::min<int64_t>(units, cap));
         if (fmt == FP8_E5M2) {
-            if (cols_mode) k_stats_g128<FP8_E5M2, true><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S);
-            else k_stats_g128<FP8_E5M2, false><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S);
+            if (cols_mode) k_stats_128x1<FP8_E5M2><<<b, kG128Warps * 32, 0, st>>>(X, rows, cols, ldx, Q, s, S);
+            else k_stats_1x128<FP8_E5M2><<<b, kG128Warps * 32, 0, st>>>(X, rows, cols, ldx, Q, s, S);
         } else {
-            if (cols_mode) k_stats_g128<FP8_E4M3, true><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S);
-            else k_stats_g128<FP8_E4M3, false><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S);
+            if (cols_mode) k_stats_128x1<FP8_E4M3><<<b, kG128Warps * 32, 0, st>>>(X, rows, cols, ldx, Q, s, S);
+            else k_stats_1x128<FP8_E4M3><<<b, kG128Warps * 32, 0, st>>>(X, rows, cols, ldx, Q, s, S);
         }
         return check_launch();
     }

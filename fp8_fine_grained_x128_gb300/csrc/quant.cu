@@ -108,7 +108,7 @@ __device__ __forceinline__ uint32_t quant_pair_cols(uint32_t w, const ColDiv2 &c
 constexpr int kFusedSmem = 32768 + 4096 + 64 * sizeof(ColDiv2);
 
 template <int FMT>
-__global__ void __launch_bounds__(256) k_quant_1x128_fused_t(const uint16_t *__restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(256, 3) k_quant_1x128_fused_t(const uint16_t *__restrict__ x, int64_t rows,
                                                              int64_t cols, int64_t ldx, uint8_t *__restrict__ q,
                                                              float *__restrict__ s, uint8_t *__restrict__ qT,
                                                              float *__restrict__ sT, int *status)
@@ -350,7 +350,7 @@ static int quant_1x128_fmt(const void *x, int64_t rows, int64_t cols, int64_t ld
             attr_done[dev & 63] = true;
         }
         const int64_t ntiles = (rows / 128) * (cols / 128);
-        const int64_t grid = std::min<int64_t>(ntiles, (int64_t)sm_count() * 4);
+        const int64_t grid = std::min<int64_t>(ntiles, (int64_t)sm_count() * 3);   // 3 resident CTAs per SM
         k_quant_1x128_fused_t<FMT><<<(unsigned)grid, 256, kFusedSmem, st>>>(
             static_cast<const uint16_t *>(x), rows, cols, ldx, static_cast<uint8_t *>(q), s,
             static_cast<uint8_t *>(qT), sT, status);

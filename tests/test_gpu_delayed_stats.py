@@ -122,6 +122,44 @@ def test_delayed_nonfinite_leaves_state_untouched():
     check_against_oracle(g, st, xb, oracle.E4M3)
 
 
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_delayed_overflowing_quotients_saturate(fmt):
+    """A scale carried over from a step with a tiny amax can make x / s overflow
+    binary32 this step: such elements saturate like the IEEE quotient says
+    (Inf -> +-fmax), they are counted as saturated, and the step's state update
+    still follows the oracle."""
+    R, C = 256, 384
+    xb = synth.bf16_signed_lognormal((R, C), 17, 0.0, 2.0)      # |x| up to ~1e4
+    for s0 in (2.0 ** -124, 2.0 ** -118, 1e-30):
+        g = GpuDelayed(fmt)
+        g.scale.fill_(s0)
+        st = oracle.DelayedState(16)
+        st.scale[:] = np.float32(s0)
+        q_ref, _ = check_against_oracle(g, st, xb, fmt)
+        assert (q_ref & 0x7F == (0x7E if fmt == oracle.E4M3 else 0x7B)).sum() > 0
+
+
+def test_delayed_nonfinite_codes_follow_ieee_quotients():
+    """A step holding Inf and NaN still writes its codes and monitors like the
+    IEEE quotients say (Inf -> +-fmax, NaN -> the NaN code)."""
+    g = GpuDelayed(oracle.E4M3)
+    xb, _ = synth.delayed_step_inputs(0, m=256, hidden=256, n_out=256)
+    g.run(xb)
+    st = oracle.DelayedState(16)
+    oracle.delayed_step(xb, st, oracle.E4M3)
+    bad = xb.copy()
+    bad[3, 3], bad[7, 200], bad[100, 5] = 0x7F80, 0xFF80, 0x7FC1      # +Inf, -Inf, NaN
+    q = empty_u8(256, 256)
+    qT = empty_u8(256, 256)
+    stats = fg.new_stats()
+    fg.quant_pertensor_delayed(dev_bf16(bad), g.recipe, g.hist, g.step, g.scale, q, g.ws, qT, stats)
+    assert fg.device_status() == fg.ERR_NONFINITE
+    q_ref, _, stats_ref, code = oracle.delayed_step(bad, st, oracle.E4M3)
+    assert code == oracle.NONFINITE
+    assert np.array_equal(q.cpu().numpy(), q_ref) and np.array_equal(qT.cpu().numpy(), q_ref.T)
+    assert np.array_equal(stats.cpu().numpy().astype(np.uint64), stats_ref)
+
+
 def test_hybrid_per_tensor_gemms():
     """fprop E4M3 x E4M3, dgrad E5M2 x E4M3 (W^T), wgrad E5M2 x E4M3 (both transposed copies)."""
     M, H, N = 1024, 512, 384
@@ -183,6 +221,41 @@ def test_quant_stats_all_granularities(fmt):
         assert_status_ok()
         ref = oracle.quant_stats(xb, q, s, gran, fmt)
         assert np.array_equal(stats.cpu().numpy().astype(np.uint64), ref), (gran, stats, ref)
+
+
+@pytest.mark.parametrize("gran", [oracle.GRAN_1x128, oracle.GRAN_128x1, oracle.GRAN_128x128])
+def test_quant_stats_saturation_boundary_and_odd_scales(gran):
+    """Scales that put |x / s| within a few ulps of fmax (the saturation count
+    is decided by the exact binary32 quotient), and scales far outside the
+    normal range (0, subnormal, huge, 2^-125 where x / s overflows)."""
+    fmt = oracle.E4M3
+    R, C = 256, 512
+    rng = np.random.default_rng(5)
+    xb = synth.bf16_signed_lognormal((R, C), 23, 0.0, 1.5)
+    xf = synth.bf16_bits_to_f32(xb)
+    if gran == oracle.GRAN_1x128:
+        shape, pick = (C // 128, R), lambda i, j: xf[j, i * 128:(i + 1) * 128]
+    elif gran == oracle.GRAN_128x1:
+        shape, pick = (R // 128, C), lambda i, j: xf[i * 128:(i + 1) * 128, j]
+    else:
+        shape, pick = (R // 128, C // 128), lambda i, j: xf[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128]
+    s = np.empty(shape, np.float32)
+    for i in range(shape[0]):
+        for j in range(shape[1]):
+            grp = np.abs(pick(i, j)).ravel()
+            v = grp[rng.integers(0, grp.size)]                  # one element of the group at |x/s| ~ fmax
+            s[i, j] = np.float32(v) / np.float32(448.0)
+            s[i, j] = np.nextafter(s[i, j], np.float32(rng.choice([-1, 1]) * np.inf), dtype=np.float32) \
+                if rng.random() < 0.5 else s[i, j]
+    odd = np.float32([0.0, 1e-40, 2.0 ** -125, 2.0 ** -124, 3e37, np.float32(np.inf)])
+    s.ravel()[:len(odd)] = odd
+    q = rng.integers(0, 256, size=(C, R) if gran == oracle.GRAN_128x1 else (R, C), dtype=np.uint8)
+    stats = fg.new_stats()
+    fg.quant_stats(dev_bf16(xb), dev_u8(q), dev_f32(s), gran, fmt, stats)
+    assert_status_ok()
+    ref = oracle.quant_stats(xb, q, s, gran, fmt)
+    assert ref[2] > 0
+    assert np.array_equal(stats.cpu().numpy().astype(np.uint64), ref), (stats, ref)
 
 
 def test_quant_stats_full_size_1x128():
