@@ -377,7 +377,7 @@ class RowBench:
         if want("a4"):
             put(self.hbm("a4_fp8_transpose_on_demand", lambda: fg.transpose_128x128(qw, sw, qwT, swT), 2 * n,
                          "FP8 W_gu^T"))
-        if want("a5"):
+        if want("a5_gemm_fprop"):
             D = bf(8192, 28672)
             put(self.tensor("a5_gemm_fprop_8192x28672x4096", lambda: fg.blockscaled_gemm(
                 q, E, s, fg.GRAN_1x128, qw, E, sw, fg.GRAN_128x128, D), 2.0 * 8192 * 28672 * 4096,

@@ -47,10 +47,17 @@ constexpr int kGemmThreads = 384;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiWarp0 = 4;          // first epilogue warp (warpgroups 1 and 2)
 constexpr int kStageReleaseWarp = 7;  // epilogue warp that frees smem stages in promote mode
-constexpr int kCtrlRegs = 144;         // setmaxnreg of the control warpgroup
-constexpr int kEpiRegs = 176;         // setmaxnreg of the epilogue warpgroups
+// setmaxnreg of the control warpgroup and of the two epilogue warpgroups,
+// per scale mode (the 1x128 x 1x128 epilogue holds per-row and per-column
+// scales beside its accumulators)
+template <int SBG> struct RegSplit { static constexpr int kCtrl = 144, kEpi = 176; };
+template <> struct RegSplit<1> { static constexpr int kCtrl = 64, kEpi = 216; };
 // the split must fit the registers the CTA is launched with
-constexpr int kRegsNeededAtLaunch = (128 * kCtrlRegs + 256 * kEpiRegs + kGemmThreads - 1) / kGemmThreads;
+template <int SBG>
+constexpr int regs_needed_at_launch()
+{
+    return (128 * RegSplit<SBG>::kCtrl + 256 * RegSplit<SBG>::kEpi + kGemmThreads - 1) / kGemmThreads;
+}
 constexpr int kMaxGroups = 1024;
 
 struct GemmArgs {
@@ -163,6 +170,15 @@ __device__ __forceinline__ void store_row(void *D, int64_t ldD, int out_f32, int
     }
 }
 
+// Two adjacent output columns (row, col), (row, col + 1) from a packed pair.
+__device__ __forceinline__ void store_pair(void *D, int64_t ldD, int out_f32, int64_t row, int64_t col, uint64_t v)
+{
+    float lo, hi;
+    f2_unpack(v, lo, hi);
+    if (out_f32) *reinterpret_cast<float2 *>(static_cast<float *>(D) + row * ldD + col) = make_float2(lo, hi);
+    else *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(D) + row * ldD + col) = pack_bf16x2(lo, hi);
+}
+
 template <int BN, int STAGES, bool PROMOTE, int SBG, bool GROUPED>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, uint32_t idesc,
@@ -239,7 +255,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int nk = a.K / 128;
 
     if (warp < kEpiWarp0) {
-        regs_dec<kCtrlRegs>();
+        regs_dec<RegSplit<SBG>::kCtrl>();
         if (warp == 0 && lane == 0) {
             // -------------------------------------------------- TMA producer
             uint32_t it = 0;
@@ -310,8 +326,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // every MMA issued by this thread completes before the CTA frees TMEM
             tc_commit(mma_done);
             mbar_wait_bounded(mma_done, 0, nullptr);
-        } else if (PROMOTE && warp == 2) {
+        } else if (PROMOTE && warp == 2 && lane == 0) {
             // -------------------------------------------------- scale producer
+            // Slot layout: [0, 128) sA of the tile's rows (1x128 A) or [128]
+            // the tile's sA (128x128 A); [256, 256 + BN) sB of the tile's
+            // columns (1x128 B) or [256], [257] the sB of the two column halves
+            // (128x128 B).  Vectors arrive by bulk copy, scalars are loaded
+            // before the slot is free and stored after.
+            const bool a_rows = a.granA == FP8_GRAN_1x128;
             uint32_t cs = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
@@ -323,36 +345,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (GROUPED) sB += (int64_t)group_of_row(sh_off, a.G, m0) * a.sB_group_stride;
                 for (int kb = 0; kb < nk; ++kb, ++cs) {
                     const int slot = cs % kScaleDepth;
-                    if (!warp_wait_or_abort(&sc_empty[slot], ((cs / kScaleDepth) & 1) ^ 1, abort_flag, a.status)) {
+                    float b0 = 0.0f, b1 = 0.0f, av = 0.0f;
+                    if (SBG == SB_BLOCK) {
+                        b0 = sB[(int64_t)(n0 >> 7) * a.ldsB + kb];
+                        b1 = sB[(int64_t)((n0 + HALF) >> 7) * a.ldsB + kb];
+                    }
+                    if (!a_rows) av = a.sA[(int64_t)(m0 >> 7) * a.ldsA + kb];
+                    if (!wait_or_abort(&sc_empty[slot], ((cs / kScaleDepth) & 1) ^ 1, abort_flag, a.status)) {
                         ok = false;
                         break;
                     }
                     float *sv = scl + slot * L::kScaleSlotFloats;
-                    float4 sa4;
-                    if (a.granA == FP8_GRAN_1x128) {
-                        sa4 = *reinterpret_cast<const float4 *>(a.sA + (int64_t)kb * a.ldsA + m0 + 4 * lane);
-                    } else {
-                        const float v = a.sA[(int64_t)(m0 >> 7) * a.ldsA + kb];
-                        sa4 = make_float4(v, v, v, v);
-                    }
                     if (SBG == SB_BLOCK) {
-                        const float b0 = sB[(int64_t)(n0 >> 7) * a.ldsB + kb];
-                        const float b1 = sB[(int64_t)((n0 + HALF) >> 7) * a.ldsB + kb];
-                        *reinterpret_cast<float4 *>(sv + 4 * lane) = make_float4(sa4.x * b0, sa4.y * b0, sa4.z * b0, sa4.w * b0);
-                        *reinterpret_cast<float4 *>(sv + 128 + 4 * lane) = make_float4(sa4.x * b1, sa4.y * b1, sa4.z * b1, sa4.w * b1);
-                    } else {
-                        *reinterpret_cast<float4 *>(sv + 4 * lane) = sa4;
-                        const float4 *col = reinterpret_cast<const float4 *>(sB + (int64_t)kb * a.ldsB + n0);
-#pragma unroll
-                        for (int i = lane; i < BN / 4; i += 32) reinterpret_cast<float4 *>(sv + 256)[i] = col[i];
+                        sv[256] = b0;
+                        sv[257] = b1;
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sc_full[slot]);
+                    if (!a_rows) sv[128] = av;
+                    // the arrive releases the stores above; the copies complete the phase
+                    mbar_arrive_expect_tx(&sc_full[slot], (a_rows ? 512u : 0u) + (SBG == SB_ROW ? BN * 4u : 0u));
+                    if (a_rows) bulk_load(sv, a.sA + (int64_t)kb * a.ldsA + m0, 512, &sc_full[slot]);
+                    if (SBG == SB_ROW) bulk_load(sv + 256, sB + (int64_t)kb * a.ldsB + n0, BN * 4, &sc_full[slot]);
                 }
             }
+            // copies still in flight land before the CTA may exit
+            const uint32_t first = cs > (uint32_t)kScaleDepth ? cs - kScaleDepth : 0;
+            for (uint32_t j = first; j < cs; ++j)
+                mbar_wait_bounded(&sc_full[j % kScaleDepth], (j / kScaleDepth) & 1, nullptr);
         }
     } else {
-        regs_inc<kEpiRegs>();
+        regs_inc<RegSplit<SBG>::kEpi>();
         // ------------------------------------------------------ epilogue
         const int ew = warp - kEpiWarp0;
         const int lg = warp & 3;             // TMEM lane quarter this warp may access
@@ -378,7 +399,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (!warp_wait_or_abort(&sc_full[slot], (cc / kScaleDepth) & 1, abort_flag, a.status)) { ok = false; break; }
                     const float *sv = scl + slot * L::kScaleSlotFloats;
                     // 128x128 B: sA*sB of this thread's row and column half; 1x128 B: sA of the row
-                    const float sr = sv[(SBG == SB_BLOCK ? (ew >> 2) * 128 : 0) + row];
+                    float sr = sv[a.granA == FP8_GRAN_1x128 ? row : 128];
+                    if (SBG == SB_BLOCK) sr *= sv[256 + (ew >> 2)];
                     if (!warp_wait_or_abort(&tfull[buf], (cc >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
                     // the chunk's MMAs are complete, so its smem stage is no longer read
                     if (warp == kStageReleaseWarp && lane == 0) mbar_arrive(&empty[cc % STAGES]);
@@ -399,18 +421,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             }
                         }
                     } else {
-                        // per-column scales sB(n, kb): 32 columns per wait
+                        // per-column scales sB(n, kb).  16x256b fragments: each
+                        // thread holds rows {16h + q, 16h + q + 8} (q = lane / 4,
+                        // h = 0, 1) of its lane quarter and columns 8i + 2(lane % 4)
+                        // + {0, 1}, so it reads 1/4 of the column scales.
+                        uint64_t sa2[4];
 #pragma unroll
-                        for (int j = 0; j < HALF / 32; ++j) {
-                            uint32_t r0[32];
-                            tc_ld_32x32b_x32(tm_lane + buf * BN + colbase + j * 32, r0);
-                            tc_wait_ld();
-                            const float4 *sbv = reinterpret_cast<const float4 *>(sv + 256 + colbase + j * 32);
+                        for (int rr = 0; rr < 4; ++rr) {
+                            const float v = sv[a.granA == FP8_GRAN_1x128 ? lg * 32 + rr * 8 + (lane >> 2) : 128];
+                            sa2[rr] = f2_pack(v, v);
+                        }
 #pragma unroll
-                            for (int i4 = 0; i4 < 8; ++i4) {
-                                const float4 b4 = sbv[i4];
-                                acc[j * 16 + 2 * i4] = f2_fma(f2_mul_bits(r0[4 * i4], r0[4 * i4 + 1], f2_pack(b4.x, b4.y)), s2, acc[j * 16 + 2 * i4]);
-                                acc[j * 16 + 2 * i4 + 1] = f2_fma(f2_mul_bits(r0[4 * i4 + 2], r0[4 * i4 + 3], f2_pack(b4.z, b4.w)), s2, acc[j * 16 + 2 * i4 + 1]);
+                        for (int c = 0; c < HALF / 64; ++c) {
+                            uint64_t sbp[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                sbp[i] = *reinterpret_cast<const uint64_t *>(sv + 256 + colbase + 64 * c + 8 * i + 2 * (lane & 3));
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                uint32_t r0[32];
+                                tc_ld_16x256b_x8(tmem_base + ((uint32_t)(lg * 32 + 16 * h) << 16) + buf * BN + colbase + 64 * c, r0);
+                                tc_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+#pragma unroll
+                                    for (int ab = 0; ab < 2; ++ab) {
+                                        uint64_t &acc_e = acc[(2 * h + ab) * (HALF / 8) + 8 * c + i];
+                                        acc_e = f2_fma(f2_mul_bits(r0[4 * i + 2 * ab], r0[4 * i + 2 * ab + 1], sbp[i]), sa2[2 * h + ab], acc_e);
+                                    }
+                                }
                             }
                         }
                     }
@@ -423,10 +462,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     ++cc;
                 }
                 if (!ok) break;
-                float v[HALF];
+                if (SBG == SB_BLOCK) {
+                    float v[HALF];
 #pragma unroll
-                for (int i = 0; i < NP; ++i) f2_unpack(acc[i], v[2 * i], v[2 * i + 1]);
-                store_row<HALF>(a.D, a.ldD, a.out_f32, (int64_t)m0 + row, (int64_t)n0 + colbase, v);
+                    for (int i = 0; i < NP; ++i) f2_unpack(acc[i], v[2 * i], v[2 * i + 1]);
+                    store_row<HALF>(a.D, a.ldD, a.out_f32, (int64_t)m0 + row, (int64_t)n0 + colbase, v);
+                } else {
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr) {
+                        const int64_t orow = (int64_t)m0 + lg * 32 + rr * 8 + (lane >> 2);
+#pragma unroll
+                        for (int i = 0; i < HALF / 8; ++i)
+                            store_pair(a.D, a.ldD, a.out_f32, orow, (int64_t)n0 + colbase + 8 * i + 2 * (lane & 3),
+                                       acc[rr * (HALF / 8) + i]);
+                    }
+                }
             } else {
                 const uint32_t buf = cc & 1;
                 const float sab = a.sA[0] * a.sB[0];
@@ -509,7 +559,7 @@ static int run_gemm(const CUtensorMap &mA, const CUtensorMap &mB, uint32_t idesc
         // only completes if the CTA was launched with at least that many.
         cudaFuncAttributes fa;
         if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return FP8_ERR_CUDA;
-        if (fa.numRegs < kRegsNeededAtLaunch) return FP8_ERR_UNSUPPORTED;
+        if (fa.numRegs < regs_needed_at_launch<SBG>()) return FP8_ERR_UNSUPPORTED;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) != cudaSuccess)
             return FP8_ERR_CUDA;
         attr_done[dev & 63] = true;
