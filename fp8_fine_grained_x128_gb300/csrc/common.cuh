@@ -108,6 +108,13 @@ struct Divider2 {
         asm("mov.b64 %0, {%1, %1};" : "=l"(r2) : "f"(r));
         asm("mov.b64 %0, {%1, %1};" : "=l"(ns2) : "f"(-s_));
     }
+    // from a scale and its reciprocal computed elsewhere (r = 0: not fast)
+    __device__ __forceinline__ Divider2(float s_, float r) : s(s_)
+    {
+        fast = r != 0.0f;
+        asm("mov.b64 %0, {%1, %1};" : "=l"(r2) : "f"(r));
+        asm("mov.b64 %0, {%1, %1};" : "=l"(ns2) : "f"(-s_));
+    }
     // quotients of (lo, hi) BF16 halves of w
     __device__ __forceinline__ void operator()(uint32_t w, float &qlo, float &qhi) const
     {
@@ -125,6 +132,45 @@ struct Divider2 {
         }
     }
 };
+
+// Scales of 8 groups of 128 values spread over the 16 lanes of a half-warp
+// (each lane holds 8 values of every group; m[u] = the lane's amax bits of
+// group u).  The maxima are reduce-scattered (xor 8 and 4 split the groups,
+// xor 2 and 1 finish them, two 16-bit maxima per word), so the quad of lanes
+// 4p..4p+3 ends with groups 2p and 2p+1, and lane 4p+e (e = 0, 1) computes
+// the scale s of group 2p+e and its reciprocal r (0 where the packed
+// division must fall back to __fdiv_rn).  Group u's pair then lives in lane
+// half_group_lane(u) of the half-warp.  Every lane of the warp must call it.
+struct GroupScale {
+    float s, r;
+    uint32_t amax;   // BF16 magnitude bits of this lane's group
+    int u;           // the group this lane computed
+};
+
+__device__ __forceinline__ int half_group_lane(int u) { return 4 * (u >> 1) + (u & 1); }
+
+template <int FMT>
+__device__ __forceinline__ GroupScale half_warp_scales8(const uint32_t (&m)[8], int l16)
+{
+    const bool b3 = (l16 & 8) != 0, b2 = (l16 & 4) != 0;
+    const uint32_t M0 = m[0] | (m[1] << 16), M1 = m[2] | (m[3] << 16);
+    const uint32_t M2 = m[4] | (m[5] << 16), M3 = m[6] | (m[7] << 16);
+    uint32_t K0 = b3 ? M2 : M0, K1 = b3 ? M3 : M1;
+    const uint32_t S0 = b3 ? M0 : M2, S1 = b3 ? M1 : M3;
+    K0 = __vmaxu2(K0, __shfl_xor_sync(0xffffffffu, S0, 8));
+    K1 = __vmaxu2(K1, __shfl_xor_sync(0xffffffffu, S1, 8));
+    uint32_t K = b2 ? K1 : K0;
+    const uint32_t S = b2 ? K0 : K1;
+    K = __vmaxu2(K, __shfl_xor_sync(0xffffffffu, S, 4));
+    K = __vmaxu2(K, __shfl_xor_sync(0xffffffffu, K, 2));
+    K = __vmaxu2(K, __shfl_xor_sync(0xffffffffu, K, 1));
+    GroupScale g;
+    g.amax = (l16 & 1) ? (K >> 16) : (K & 0xFFFFu);
+    g.u = 2 * (l16 >> 2) + (l16 & 1);
+    g.s = scale_from_amax_bits(g.amax, FMT);
+    g.r = (g.s >= 0x1p-125f && g.s <= 0x1p125f) ? __frcp_rn(g.s) : 0.0f;
+    return g;
+}
 
 // Sign bits of the 4 BF16 values in (w0 = x0,x1 ; w1 = x2,x3) placed at bit 7
 // of bytes 0..3: OR-ed into the 4 codes this restores -0 -> 0x80 (every other

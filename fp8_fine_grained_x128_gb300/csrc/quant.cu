@@ -48,20 +48,24 @@ __global__ void __launch_bounds__(256) k_quant_1x128_rows(const uint16_t *__rest
 #pragma unroll
         for (int u = 0; u < U; ++u)
             v[u] = (c0 + u < ncb) ? ldg_stream(xr + (int64_t)(c0 + u) * 128) : make_uint4(0, 0, 0, 0);
+        uint32_t m[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) m[u] = absmax8(v[u]);
+        // each tile's scale is computed by one lane and shuffled to the others
+        const GroupScale gs = half_warp_scales8<FMT>(m, l16);
+        if (!(l16 & 2) && c0 + gs.u < ncb) {
+            if (gs.amax >= 0x7F80u) set_status(status, FP8_ERR_NONFINITE);
+            s[(int64_t)(c0 + gs.u) * rows + r] = gs.s;
+        }
+        const int hbase = threadIdx.x & 16;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            uint32_t m = absmax8(v[u]);
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            const float su = __shfl_sync(0xffffffffu, gs.s, hbase + half_group_lane(u));
+            const float ru = __shfl_sync(0xffffffffu, gs.r, hbase + half_group_lane(u));
             const uint32_t cb = c0 + u;
             if (cb < ncb) {
-                if (m >= 0x7F80u && l16 == 0) set_status(status, FP8_ERR_NONFINITE);
-                const float sc = scale_from_amax_bits(m, FMT);
-                const Divider2 d(sc);
+                const Divider2 d(su, ru);
                 *reinterpret_cast<uint2 *>(q + (int64_t)r * cols + (int64_t)cb * 128 + l16 * 8) = quant8p<FMT>(v[u], d);
-                if (l16 == 0) s[(int64_t)cb * rows + r] = sc;
             }
         }
     }
@@ -138,19 +142,24 @@ __global__ void __launch_bounds__(256, 3) k_quant_1x128_fused_t(const uint16_t *
         const int64_t r0 = mb * 128, c0 = cb * 128;
 
         uint32_t cm0 = 0, cm1 = 0, cm2 = 0, cm3 = 0;
+        GroupScale gs;
+        {
+            uint32_t m[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m[i] = absmax8(v[i]);
+            gs = half_warp_scales8<FMT>(m, g);   // the half-warp's 8 rows rr + 16i
+        }
+        if (!(g & 2)) {
+            if (gs.amax >= 0x7F80u) set_status(status, FP8_ERR_NONFINITE);
+            s[cb * rows + r0 + rr + 16 * gs.u] = gs.s;
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int row = rr + 16 * i;
-            uint32_t m = absmax8(v[i]);
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            if (m >= 0x7F80u && g == 0) set_status(status, FP8_ERR_NONFINITE);
-            const float sc = scale_from_amax_bits(m, FMT);
-            const Divider2 d(sc);
+            const float si = __shfl_sync(0xffffffffu, gs.s, (lane & 16) + half_group_lane(i));
+            const float ri = __shfl_sync(0xffffffffu, gs.r, (lane & 16) + half_group_lane(i));
+            const Divider2 d(si, ri);
             *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = quant8p<FMT>(v[i], d);
-            if (g == 0) s[cb * rows + r0 + row] = sc;
             *reinterpret_cast<uint4 *>(tile + row * 256 + ((g ^ ((row >> 2) & 7)) << 4)) = v[i];
             cm0 = bf16x2_absmax(cm0, bf16x2_abs(v[i].x));
             cm1 = bf16x2_absmax(cm1, bf16x2_abs(v[i].y));
