@@ -115,6 +115,17 @@ struct Divider2 {
         asm("mov.b64 %0, {%1, %1};" : "=l"(r2) : "f"(r));
         asm("mov.b64 %0, {%1, %1};" : "=l"(ns2) : "f"(-s_));
     }
+    // the packed Markstein quotients alone (callers have checked `fast`)
+    __device__ __forceinline__ void fast_div(uint32_t w, float &qlo, float &qhi) const
+    {
+        const float xlo = __uint_as_float(w << 16), xhi = __uint_as_float(w & 0xFFFF0000u);
+        uint64_t x2, q0, e, q;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "f"(xlo), "f"(xhi));
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(r2));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(ns2), "l"(x2));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(e), "l"(r2), "l"(q0));
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(qlo), "=f"(qhi) : "l"(q));
+    }
     // quotients of (lo, hi) BF16 halves of w
     __device__ __forceinline__ void operator()(uint32_t w, float &qlo, float &qhi) const
     {
@@ -214,20 +225,33 @@ __device__ __forceinline__ uint2 quant8(uint4 v, const Divider &d)
     return out;
 }
 
-// Same with the packed divider.
+// Same with the packed divider.  The fast path is inlined; a scale outside
+// its range (rare: an all-tiny or non-finite group) takes one out-of-line
+// call for the whole group, which keeps the unrolled loops small.
 template <int FMT>
-__device__ __forceinline__ uint32_t quant4p(uint32_t w0, uint32_t w1, const Divider2 &d)
+__device__ __forceinline__ uint32_t quant4p_fast(uint32_t w0, uint32_t w1, const Divider2 &d)
 {
     float a, b, c, e;
-    d(w0, a, b);
-    d(w1, c, e);
+    d.fast_div(w0, a, b);
+    d.fast_div(w1, c, e);
     return (cvt2<FMT>(a, b) | (cvt2<FMT>(c, e) << 16)) | sign_bits4(w0, w1);
+}
+
+template <int FMT>
+__device__ __noinline__ uint2 quant8p_slow(uint4 v, float s)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t c[4];
+    for (int j = 0; j < 4; ++j)
+        c[j] = cvt2<FMT>(__fdiv_rn(__uint_as_float(w[j] << 16), s), __fdiv_rn(__uint_as_float(w[j] & 0xFFFF0000u), s));
+    return make_uint2((c[0] | (c[1] << 16)) | sign_bits4(w[0], w[1]), (c[2] | (c[3] << 16)) | sign_bits4(w[2], w[3]));
 }
 
 template <int FMT>
 __device__ __forceinline__ uint2 quant8p(uint4 v, const Divider2 &d)
 {
-    return make_uint2(quant4p<FMT>(v.x, v.y, d), quant4p<FMT>(v.z, v.w, d));
+    if (!d.fast) return quant8p_slow<FMT>(v, d.s);
+    return make_uint2(quant4p_fast<FMT>(v.x, v.y, d), quant4p_fast<FMT>(v.z, v.w, d));
 }
 
 __device__ __forceinline__ uint32_t absmax8(uint4 v)

@@ -48,24 +48,44 @@ struct Counts {
 // The distinct-code count of a quantization done here needs no per-element
 // code bitmap: q = enc(x / s) is a function of x, so the distinct codes are the
 // image of the distinct inputs, which the last CTA encodes once.
+struct Quot8 {
+    float q[8];
+};
+
+// IEEE quotients of 8 BF16 values (out of line: the rare path).
+__device__ __noinline__ Quot8 quot8_ieee(uint4 v, float s)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    Quot8 r;
+    for (int j = 0; j < 4; ++j) {
+        r.q[2 * j] = __fdiv_rn(__uint_as_float(w[j] << 16), s);
+        r.q[2 * j + 1] = __fdiv_rn(__uint_as_float(w[j] & 0xFFFF0000u), s);
+    }
+    return r;
+}
+
 template <int FMT, bool STATS>
 __device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &c, uint32_t *bmx)
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float qv[8];
+    if (d.fast) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) d(w[j], qv[2 * j], qv[2 * j + 1]);
+        for (int j = 0; j < 4; ++j) d.fast_div(w[j], qv[2 * j], qv[2 * j + 1]);
+    } else {
+        const Quot8 r = quot8_ieee(v, d.s);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qv[e] = r.q[e];
+    }
     uint2 out;
     out.x = (cvt2<FMT>(qv[0], qv[1]) | (cvt2<FMT>(qv[2], qv[3]) << 16)) | sign_bits4(v.x, v.y);
     out.y = (cvt2<FMT>(qv[4], qv[5]) | (cvt2<FMT>(qv[6], qv[7]) << 16)) | sign_bits4(v.z, v.w);
     if (has_nan_code<FMT>(out.x) || has_nan_code<FMT>(out.y)) {
         // x NaN, x = +-Inf, or x / s overflowed in the fast division (the
         // scale comes from earlier steps): the IEEE quotients decide
+        const Quot8 r = quot8_ieee(v, d.s);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            qv[2 * j] = __fdiv_rn(__uint_as_float(w[j] << 16), d.s);
-            qv[2 * j + 1] = __fdiv_rn(__uint_as_float(w[j] & 0xFFFF0000u), d.s);
-        }
+        for (int e = 0; e < 8; ++e) qv[e] = r.q[e];
         out.x = (cvt2<FMT>(qv[0], qv[1]) | (cvt2<FMT>(qv[2], qv[3]) << 16)) | sign_bits4(v.x, v.y);
         out.y = (cvt2<FMT>(qv[4], qv[5]) | (cvt2<FMT>(qv[6], qv[7]) << 16)) | sign_bits4(v.z, v.w);
     }

@@ -28,7 +28,7 @@ namespace fp8fg {
 // loads in flight; the only division per run is the run -> (row, chunk) map.
 // ---------------------------------------------------------------------------
 template <int FMT, int U>
-__global__ void __launch_bounds__(256) k_quant_1x128_rows(const uint16_t *__restrict__ x, uint32_t rows,
+__global__ void __launch_bounds__(256, 4) k_quant_1x128_rows(const uint16_t *__restrict__ x, uint32_t rows,
                                                           uint32_t ncb, int64_t ldx, uint8_t *__restrict__ q,
                                                           float *__restrict__ s, int *status)
 {
@@ -90,23 +90,36 @@ struct ColDiv2 {
     int fast;
 };
 
+// Codes of the column pair (lo, hi) of w, each with its own column scale.
 template <int FMT>
-__device__ __forceinline__ uint32_t quant_pair_cols(uint32_t w, const ColDiv2 &c)
+__device__ __forceinline__ uint32_t quant_pair_cols_fast(uint32_t w, const ColDiv2 &c)
 {
     float qlo, qhi;
-    if (c.fast) {
-        const float xlo = __uint_as_float(w << 16), xhi = __uint_as_float(w & 0xFFFF0000u);
-        uint64_t x2, q0, e, qq;
-        asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "f"(xlo), "f"(xhi));
-        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(c.r2));
-        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(c.ns2), "l"(x2));
-        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(qq) : "l"(e), "l"(c.r2), "l"(q0));
-        asm("mov.b64 {%0, %1}, %2;" : "=f"(qlo), "=f"(qhi) : "l"(qq));
-    } else {
-        qlo = __fdiv_rn(__uint_as_float(w << 16), c.s0);
-        qhi = __fdiv_rn(__uint_as_float(w & 0xFFFF0000u), c.s1);
-    }
+    const float xlo = __uint_as_float(w << 16), xhi = __uint_as_float(w & 0xFFFF0000u);
+    uint64_t x2, q0, e, qq;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "f"(xlo), "f"(xhi));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(c.r2));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(c.ns2), "l"(x2));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(qq) : "l"(e), "l"(c.r2), "l"(q0));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(qlo), "=f"(qhi) : "l"(qq));
     return cvt2<FMT>(qlo, qhi);
+}
+
+// The same for 4 rows x 4 columns when a column scale is outside the fast
+// division's range (out of line: rare).
+template <int FMT>
+__device__ __noinline__ uint4 quant_cols4x4_slow(uint4 lo, uint4 hi, float s0, float s1, float s2, float s3)
+{
+    const uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w}, b[4] = {hi.x, hi.y, hi.z, hi.w};
+    uint32_t rw[4];
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t c01 = cvt2<FMT>(__fdiv_rn(__uint_as_float(a[i] << 16), s0),
+                                       __fdiv_rn(__uint_as_float(a[i] & 0xFFFF0000u), s1));
+        const uint32_t c23 = cvt2<FMT>(__fdiv_rn(__uint_as_float(b[i] << 16), s2),
+                                       __fdiv_rn(__uint_as_float(b[i] & 0xFFFF0000u), s3));
+        rw[i] = (c01 | (c23 << 16)) | sign_bits4(a[i], b[i]);
+    }
+    return make_uint4(rw[0], rw[1], rw[2], rw[3]);
 }
 
 constexpr int kFusedSmem = 32768 + 4096 + 64 * sizeof(ColDiv2);
@@ -205,17 +218,28 @@ __global__ void __launch_bounds__(256, 3) k_quant_1x128_fused_t(const uint16_t *
 
         const int cw = (lane >> 3) + 4 * warp;   // columns 4cw .. 4cw+3
         const ColDiv2 d01 = cdiv[2 * cw], d23 = cdiv[2 * cw + 1];
+        const bool cfast = d01.fast && d23.fast;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int mg = (lane & 7) + 8 * k;   // rows 4mg .. 4mg+3
-            uint32_t rw[4];                      // codes of row 4mg+i, columns 4cw..4cw+3
+            uint2 pr[4];                         // BF16 of row 4mg+i, columns 4cw..4cw+3
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int row = 4 * mg + i;
-                const uint2 pr = *reinterpret_cast<const uint2 *>(
+                pr[i] = *reinterpret_cast<const uint2 *>(
                     tile + row * 256 + (((cw >> 1) ^ ((row >> 2) & 7)) << 4) + ((cw & 1) << 3));
-                rw[i] = (quant_pair_cols<FMT>(pr.x, d01) | (quant_pair_cols<FMT>(pr.y, d23) << 16)) |
-                        sign_bits4(pr.x, pr.y);
+            }
+            uint32_t rw[4];                      // codes of row 4mg+i, columns 4cw..4cw+3
+            if (cfast) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    rw[i] = (quant_pair_cols_fast<FMT>(pr[i].x, d01) | (quant_pair_cols_fast<FMT>(pr[i].y, d23) << 16)) |
+                            sign_bits4(pr[i].x, pr[i].y);
+            } else {
+                const uint4 c = quant_cols4x4_slow<FMT>(make_uint4(pr[0].x, pr[1].x, pr[2].x, pr[3].x),
+                                                        make_uint4(pr[0].y, pr[1].y, pr[2].y, pr[3].y), d01.s0,
+                                                        d01.s1, d23.s0, d23.s1);
+                rw[0] = c.x; rw[1] = c.y; rw[2] = c.z; rw[3] = c.w;
             }
             const uint32_t t0 = __byte_perm(rw[0], rw[1], 0x5140), t1 = __byte_perm(rw[2], rw[3], 0x5140);
             const uint32_t t2 = __byte_perm(rw[0], rw[1], 0x7362), t3 = __byte_perm(rw[2], rw[3], 0x7362);
@@ -367,8 +391,10 @@ static int quant_1x128_fmt(const void *x, int64_t rows, int64_t cols, int64_t ld
     }
     constexpr int U = 8;
     const int64_t items = rows * ((cols / 128 + U - 1) / U);
+    // one run per half-warp: the block scheduler balances the load (a
+    // persistent grid leaves whole runs of imbalance at this size)
     int64_t blocks = (items + 15) / 16;
-    const int64_t cap = (int64_t)sm_count() * 8;
+    const int64_t cap = (int64_t)1 << 20;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     k_quant_1x128_rows<FMT, U><<<(unsigned)blocks, 256, 0, st>>>(
