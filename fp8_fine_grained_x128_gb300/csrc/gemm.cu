@@ -433,23 +433,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         }
 #pragma unroll
                         for (int c = 0; c < HALF / 64; ++c) {
-                            uint64_t sbp[8];
+                            // both 16-lane halves of the quarter in flight per wait
+                            uint32_t p0[32], p1[32];
+                            const uint32_t ta = tmem_base + ((uint32_t)(lg * 32) << 16) + buf * BN + colbase + 64 * c;
+                            tc_ld_16x256b_x8(ta, p0);
+                            tc_ld_16x256b_x8(ta + (16u << 16), p1);
+                            tc_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                sbp[i] = *reinterpret_cast<const uint64_t *>(sv + 256 + colbase + 64 * c + 8 * i + 2 * (lane & 3));
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                uint32_t r0[32];
-                                tc_ld_16x256b_x8(tmem_base + ((uint32_t)(lg * 32 + 16 * h) << 16) + buf * BN + colbase + 64 * c, r0);
-                                tc_wait_ld();
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-#pragma unroll
-                                    for (int ab = 0; ab < 2; ++ab) {
-                                        uint64_t &acc_e = acc[(2 * h + ab) * (HALF / 8) + 8 * c + i];
-                                        acc_e = f2_fma(f2_mul_bits(r0[4 * i + 2 * ab], r0[4 * i + 2 * ab + 1], sbp[i]), sa2[2 * h + ab], acc_e);
-                                    }
-                                }
+                            for (int i = 0; i < 8; ++i) {
+                                const uint64_t sb = *reinterpret_cast<const uint64_t *>(sv + 256 + colbase + 64 * c + 8 * i + 2 * (lane & 3));
+                                uint64_t *ac = acc + 8 * c + i;
+                                ac[0 * (HALF / 8)] = f2_fma(f2_mul_bits(p0[4 * i], p0[4 * i + 1], sb), sa2[0], ac[0 * (HALF / 8)]);
+                                ac[1 * (HALF / 8)] = f2_fma(f2_mul_bits(p0[4 * i + 2], p0[4 * i + 3], sb), sa2[1], ac[1 * (HALF / 8)]);
+                                ac[2 * (HALF / 8)] = f2_fma(f2_mul_bits(p1[4 * i], p1[4 * i + 1], sb), sa2[2], ac[2 * (HALF / 8)]);
+                                ac[3 * (HALF / 8)] = f2_fma(f2_mul_bits(p1[4 * i + 2], p1[4 * i + 3], sb), sa2[3], ac[3 * (HALF / 8)]);
                             }
                         }
                     }
