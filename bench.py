@@ -40,10 +40,12 @@ METRIC = "block-scaled FP8 GEMM TFLOPS and quantize GB/s at 1 GB300, as % of roo
 WORKLOAD = "dense SwiGLU MLP full step (fprop+dgrad+wgrad), M=8192 tokens, hidden 4096, FFN 14336, E4M3 1x128/128x128/128x1"
 M_TOK, HID, FFN = 8192, 4096, 14336
 
-# DRAM traffic per launch of the 8192x28672x4096 block-scaled GEMM from one
-# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum); None until a
-# capture of the current kernel exists (see profiles/).
-GEMM_TRAFFIC_BYTES = None
+# DRAM traffic per GEMM launch of the step (dram__bytes_read.sum +
+# dram__bytes_write.sum over the six GEMM launches of one step, divided by
+# six, from a one-pass ncu capture of the current kernel; the summary with
+# its command is profiles/k_gemm_step_dram_traffic.md).  Set to None when the
+# kernel changes until it is captured again.
+GEMM_TRAFFIC_BYTES = 738452565
 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
@@ -572,12 +574,21 @@ def run_ours(args):
     gemm_ms /= args.steps
     achieved = flops / (gemm_ms * 1e-3) / 1e12
     head = 2.0 * M_TOK * 2 * FFN * HID / (statistics.median(head_ms) * 1e-3) / 1e12
+    shapes = {"fprop_gate_up": (M_TOK, 2 * FFN, HID), "fprop_down": (M_TOK, HID, FFN),
+              "dgrad_down": (M_TOK, FFN, HID), "dgrad_gate_up": (M_TOK, HID, 2 * FFN),
+              "wgrad_down": (HID, FFN, M_TOK), "wgrad_gate_up": (2 * FFN, HID, M_TOK)}
+    per_gemm = {}
+    for name, (gm, gn, gk) in shapes.items():
+        t = statistics.median(e[name][0].elapsed_time(e[name][1]) for e in ev)
+        per_gemm[name] = {"MxNxK": f"{gm}x{gn}x{gk}", "us": round(t * 1e3, 1),
+                          "tflops": round(2.0 * gm * gn * gk / (t * 1e-3) / 1e12, 1)}
     roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak_sus, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak_sus, "traffic": GEMM_TRAFFIC_BYTES,
                 "kernel": "k_gemm (block-scaled, 6 shapes of the step)",
                 "peak_source": f"{pk['src']}: bf16 sustained {pk['bf16_sus']} TFLOP/s x {FP8_OVER_BF16} (FP8/BF16 nominal)",
                 "headline_shape_8192x28672x4096_tflops": head,
-                "headline_frac_of_burst": head / fp8_peak_burst}
+                "headline_frac_of_burst": head / fp8_peak_burst,
+                "per_gemm": per_gemm}
 
     # end to end: host buffers, H2D of the step's inputs and D2H of its results
     e2e = step.e2e(args.steps)
