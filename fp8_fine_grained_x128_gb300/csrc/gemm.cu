@@ -89,10 +89,12 @@ struct GemmSmem {
     // per scale slot: row values for the two column halves + BN column values
     static constexpr int kScaleSlotFloats = 2 * 128 + BN;
     static constexpr int kScaleBytes = kScaleDepth * kScaleSlotFloats * 4;
-    static constexpr int kBars = 2 * STAGES + 2 + 2 + 1 + 2 * kScaleDepth;
+    // TMEM accumulators of BN columns that alternate per chunk: all 512 columns
+    static constexpr int kNbuf = 512 / BN;
+    static constexpr int kBars = 2 * STAGES + 2 * kNbuf + 1 + 2 * kScaleDepth;
     static constexpr int kCtrl = kBars * 8 + 16;
     static constexpr int kBytes = 1024 + STAGES * kStage + kScaleBytes + kCtrl + 4 * (kMaxGroups + 1);
-    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kTmemCols = kNbuf * BN;
 };
 
 // Tiles are walked in bands of GM M-tiles, M fastest: a band's A rows stay in
@@ -193,8 +195,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * L::kStage + L::kScaleBytes);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
-    uint64_t *tempty = tfull + 2;
-    uint64_t *mma_done = tempty + 2;
+    uint64_t *tempty = tfull + L::kNbuf;
+    uint64_t *mma_done = tempty + L::kNbuf;
     uint64_t *sc_full = mma_done + 1;
     uint64_t *sc_empty = sc_full + kScaleDepth;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sc_empty + kScaleDepth);
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < L::kNbuf; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], kEpiWarps);
         }
@@ -284,17 +286,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t it = 0, cc = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                uint32_t buf = cc & 1;
+                uint32_t buf = cc % L::kNbuf;
                 if (!PROMOTE) {
-                    if (!wait_or_abort(&tempty[buf], ((cc >> 1) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+                    if (!wait_or_abort(&tempty[buf], ((cc / L::kNbuf) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
                 }
                 for (int kb = 0; kb < nk; ++kb) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (PROMOTE) {
-                        buf = cc & 1;
-                        if (!wait_or_abort(&tempty[buf], ((cc >> 1) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+                        buf = cc % L::kNbuf;
+                        if (!wait_or_abort(&tempty[buf], ((cc / L::kNbuf) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
                     }
                     if (!wait_or_abort(&full[s], ph, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
@@ -394,14 +396,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                 for (int i = 0; i < NP; ++i) acc[i] = 0ull;
                 for (int kb = 0; kb < nk; ++kb) {
-                    const uint32_t buf = cc & 1;
+                    const uint32_t buf = cc % L::kNbuf;
                     const int slot = cc % kScaleDepth;
                     if (!warp_wait_or_abort(&sc_full[slot], (cc / kScaleDepth) & 1, abort_flag, a.status)) { ok = false; break; }
                     const float *sv = scl + slot * L::kScaleSlotFloats;
                     // 128x128 B: sA*sB of this thread's row and column half; 1x128 B: sA of the row
                     float sr = sv[a.granA == FP8_GRAN_1x128 ? row : 128];
                     if (SBG == SB_BLOCK) sr *= sv[256 + (ew >> 2)];
-                    if (!warp_wait_or_abort(&tfull[buf], (cc >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                    if (!warp_wait_or_abort(&tfull[buf], (cc / L::kNbuf) & 1, abort_flag, a.status)) { ok = false; break; }
                     // the chunk's MMAs are complete, so its smem stage is no longer read
                     if (warp == kStageReleaseWarp && lane == 0) mbar_arrive(&empty[cc % STAGES]);
                     tc_fence_after();
@@ -475,9 +477,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             } else {
-                const uint32_t buf = cc & 1;
+                const uint32_t buf = cc % L::kNbuf;
                 const float sab = a.sA[0] * a.sB[0];
-                if (!warp_wait_or_abort(&tfull[buf], (cc >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                if (!warp_wait_or_abort(&tfull[buf], (cc / L::kNbuf) & 1, abort_flag, a.status)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int j = 0; j < HALF / 32; ++j) {
