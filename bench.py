@@ -332,18 +332,25 @@ class MlpStep:
 
 class RowBench:
     """Each hot-path row timed on its own: median of CUDA-event-timed launches,
-    L2 flushed (256 MB write) before every launch."""
+    L2 flushed before every launch.  The flush writes a 256 MB buffer and then
+    reads another 256 MB one, so the timed kernel finds none of its data in
+    L2 and does not pay the write-back of the flush's own dirty lines."""
 
     def __init__(self, dev, pk):
         import torch
         self.dev, self.pk = dev, pk
         self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.flush_read = torch.zeros(64 << 20, dtype=torch.int32, device=dev)
+
+    def flush(self):
+        self.flush_buf.zero_()
+        self.flush_read.max()
 
     def time(self, fn):
         import torch
         evs = []
         for i in range(self.iters + 2):
-            self.flush_buf.zero_()
+            self.flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -478,8 +485,10 @@ class RowBench:
             t_route = self.time(lambda: fg.moe_route_pad(Z, topk, 128, cap, ti, tp, cnt, offs, rt, rp, rpad))
             out["a9_moe_route_pad"] = {"time_us": t_route * 1e6, "bound": "latency",
                                        "note": "8192 tokens x 128 experts, top-8, pad to 128 (3 launches)"}
+            # algorithmic bytes: every token's codes and scales read once (its
+            # top-k repeats come from L2) and every dispatched row written once
             put(self.hbm("a9_moe_gather", lambda: fg.moe_gather(qx, sx, rt, offs, Ex, cap, qg, sg),
-                         2 * total * Hd + 2 * total * (Hd // 128) * 4, f"{total} dispatched rows x 2048"))
+                         (T + total) * (Hd + (Hd // 128) * 4), f"{total} dispatched rows x 2048 from 8192 tokens"))
         if want("a10"):
             qgu = u8(Ex, 2 * F, Hd).random_(0, 120)
             sgu = f32(Ex, 2 * F // 128, Hd // 128).fill_(1e-3)

@@ -11,6 +11,8 @@
 // ascending order -- all decided on the device, no host round trip.
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -74,26 +76,25 @@ __global__ void __launch_bounds__(256) k_moe_topk(const float *__restrict__ logi
 
 // ------------------------------------------------------------ per-expert count
 
-__device__ __forceinline__ bool routed_to(const int32_t *__restrict__ topk_idx, int64_t t, int topk, int e)
-{
-    bool r = false;
-    for (int k = 0; k < topk; ++k) r |= topk_idx[t * topk + k] == e;
-    return r;
-}
-
-__global__ void __launch_bounds__(256) k_moe_count(const int32_t *__restrict__ topk_idx, int64_t T, int topk,
+// Histogram of the top-k choices (each token's choices are distinct experts):
+// one pass over topk_idx, shared-memory counts merged into counts[], which
+// the launcher has zeroed.
+__global__ void __launch_bounds__(256) k_moe_count(const int32_t *__restrict__ topk_idx, int64_t n, int E,
                                                    int32_t *__restrict__ counts)
 {
-    const int e = blockIdx.x;
-    int total = 0;
-    for (int64_t t0 = 0; t0 < T; t0 += blockDim.x) {
-        const int64_t t = t0 + threadIdx.x;
-        total += __syncthreads_count(t < T && routed_to(topk_idx, t, topk, e));
+    __shared__ int hist[256];
+    for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int e = topk_idx[i];
+        if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
     }
-    if (threadIdx.x == 0) counts[e] = total;
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x)
+        if (hist[i]) atomicAdd(&counts[i], hist[i]);
 }
 
-// Block-wide exclusive prefix sum of a 0/1 flag (256 threads) and the total.
+// Block-wide exclusive prefix sum of a 0/1 flag (up to 1024 threads) and the total.
 __device__ __forceinline__ int block_excl_scan(int flag, int *warp_tot, int &total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -114,16 +115,19 @@ __device__ __forceinline__ int block_excl_scan(int flag, int *warp_tot, int &tot
 __device__ __forceinline__ int64_t padded_count(int c, int align) { return ((int64_t)c + align - 1) / align * align; }
 
 // One CTA per expert: offset from the padded counts of earlier experts, the
-// routing-map edit (first `need` free tokens), and the dispatch rows.
-__global__ void __launch_bounds__(256) k_moe_fill(const int32_t *__restrict__ topk_idx,
+// routing-map edit (first `need` free tokens), and the dispatch rows.  The
+// tokens are walked 1024 at a time (one per thread) in ascending order.
+constexpr int kFillThreads = 1024;
+
+__global__ void __launch_bounds__(kFillThreads) k_moe_fill(const int32_t *__restrict__ topk_idx,
                                                   const float *__restrict__ topk_prob, const int32_t *__restrict__ counts,
                                                   int64_t T, int E, int topk, int align, int64_t Mcap,
                                                   int32_t *__restrict__ offsets, int32_t *__restrict__ row_token,
                                                   float *__restrict__ row_prob, uint8_t *__restrict__ row_is_pad,
                                                   int *status)
 {
-    __shared__ int warp_tot[8];
-    __shared__ int64_t red[8];
+    __shared__ int warp_tot[kFillThreads / 32];
+    __shared__ int64_t red[kFillThreads / 32];
     const int e = blockIdx.x;
     // offset of this expert and the total, from the counts of all experts
     int64_t before = 0, all = 0;
@@ -140,12 +144,12 @@ __global__ void __launch_bounds__(256) k_moe_fill(const int32_t *__restrict__ to
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = before;
     __syncthreads();
     int64_t off = 0;
-    for (int w = 0; w < 8; ++w) off += red[w];
+    for (int w = 0; w < kFillThreads / 32; ++w) off += red[w];
     __syncthreads();
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = all;
     __syncthreads();
     int64_t total = 0;
-    for (int w = 0; w < 8; ++w) total += red[w];
+    for (int w = 0; w < kFillThreads / 32; ++w) total += red[w];
 
     const int c = counts[e];
     const int64_t need = padded_count(c, align) - c;
@@ -297,8 +301,13 @@ int launch_moe_route_pad(const float *logits, int64_t T, int E, int topk, int al
     else if (epl <= 2) k_moe_topk<2><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob);
     else if (epl <= 4) k_moe_topk<4><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob);
     else k_moe_topk<8><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob);
-    k_moe_count<<<E, 256, 0, st>>>(topk_idx, T, topk, counts);
-    k_moe_fill<<<E, 256, 0, st>>>(topk_idx, topk_prob, counts, T, E, topk, align, Mcap, offsets, row_token, row_prob,
+    if (cudaMemsetAsync(counts, 0, (size_t)E * sizeof(int32_t), st) != cudaSuccess) return FP8_ERR_CUDA;
+    const int64_t n = T * topk;
+    if (n > 0) {
+        const int64_t cb = std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 2);
+        k_moe_count<<<(unsigned)cb, 256, 0, st>>>(topk_idx, n, E, counts);
+    }
+    k_moe_fill<<<E, kFillThreads, 0, st>>>(topk_idx, topk_prob, counts, T, E, topk, align, Mcap, offsets, row_token, row_prob,
                                   row_is_pad, status);
     return check_launch();
 }
