@@ -484,7 +484,7 @@ class RowBench:
         if want("a9"):
             t_route = self.time(lambda: fg.moe_route_pad(Z, topk, 128, cap, ti, tp, cnt, offs, rt, rp, rpad))
             out["a9_moe_route_pad"] = {"time_us": t_route * 1e6, "bound": "latency",
-                                       "note": "8192 tokens x 128 experts, top-8, pad to 128 (3 launches)"}
+                                       "note": "8192 tokens x 128 experts, top-8, pad to 128 (3 kernels + a 512 B memset)"}
             # algorithmic bytes: every token's codes and scales read once (its
             # top-k repeats come from L2) and every dispatched row written once
             put(self.hbm("a9_moe_gather", lambda: fg.moe_gather(qx, sx, rt, offs, Ex, cap, qg, sg),

@@ -20,6 +20,20 @@ namespace fp8fg {
 
 // ---------------------------------------------------------------- top-k
 
+// Unsigned key with the order of the logits (-0 and +0 share one key so they
+// tie; NaN gets the lowest key and is chosen last).
+__device__ __forceinline__ uint32_t logit_key(float z)
+{
+    if (z != z) return 0u;
+    const uint32_t u = z == 0.0f ? 0u : __float_as_uint(z);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_logit(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 template <int EPL>
 __global__ void __launch_bounds__(256) k_moe_topk(const float *__restrict__ logits, int64_t T, int E, int topk,
                                                   int32_t *__restrict__ topk_idx, float *__restrict__ topk_prob)
@@ -44,32 +58,31 @@ __global__ void __launch_bounds__(256) k_moe_topk(const float *__restrict__ logi
             if (j * 32 + lane < E) sum += expf(z[j] - m);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        uint32_t taken = 0;
+        // each round: the largest remaining logit, ties to the lower expert
+        // index, by two warp reductions on an order-preserving key
+        uint32_t taken = 0, my_key = 0, my_idx = 0;   // lane k keeps round k's choice
         for (int k = 0; k < topk; ++k) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
+            uint32_t bk = 0, be = 0xffffffffu;
 #pragma unroll
             for (int j = 0; j < EPL; ++j) {
                 const int e = j * 32 + lane;
-                if (e < E && !((taken >> j) & 1u) && (z[j] > bv || (z[j] == bv && e < bi))) {
-                    bv = z[j];
-                    bi = e;
+                const uint32_t key = logit_key(z[j]);
+                if (e < E && !((taken >> j) & 1u) && key > bk) {
+                    bk = key;
+                    be = (uint32_t)e;
                 }
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (ov > bv || (ov == bv && oi < bi)) {
-                    bv = ov;
-                    bi = oi;
-                }
+            const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t bi = __reduce_min_sync(0xffffffffu, bk == mk ? be : 0xffffffffu);
+            if (bi < (uint32_t)E && (int)(bi & 31) == lane) taken |= 1u << (bi >> 5);
+            if (lane == k) {
+                my_key = mk;
+                my_idx = bi;
             }
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-            if (lane == 0) {
-                topk_idx[t * topk + k] = bi;
-                topk_prob[t * topk + k] = expf(bv - m) / sum;
-            }
+        }
+        if (lane < topk) {
+            topk_idx[t * topk + lane] = (int32_t)my_idx;
+            topk_prob[t * topk + lane] = expf(key_logit(my_key) - m) / sum;
         }
     }
 }
@@ -94,14 +107,18 @@ __global__ void __launch_bounds__(256) k_moe_count(const int32_t *__restrict__ t
         if (hist[i]) atomicAdd(&counts[i], hist[i]);
 }
 
-// Block-wide exclusive prefix sum of a 0/1 flag (up to 1024 threads) and the total.
-__device__ __forceinline__ int block_excl_scan(int flag, int *warp_tot, int &total)
+// Block-wide exclusive prefix sum of per-thread counts and the total.
+__device__ __forceinline__ int block_excl_scan_count(int v, int *warp_tot, int &total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t bal = __ballot_sync(0xffffffffu, flag);
-    const int within = __popc(bal & ((1u << lane) - 1u));
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
     __syncthreads();
-    if (lane == 0) warp_tot[warp] = __popc(bal);
+    if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     int before = 0;
     total = 0;
@@ -109,15 +126,17 @@ __device__ __forceinline__ int block_excl_scan(int flag, int *warp_tot, int &tot
         if (w < warp) before += warp_tot[w];
         total += warp_tot[w];
     }
-    return before + within;
+    return before + incl - v;
 }
 
 __device__ __forceinline__ int64_t padded_count(int c, int align) { return ((int64_t)c + align - 1) / align * align; }
 
 // One CTA per expert: offset from the padded counts of earlier experts, the
 // routing-map edit (first `need` free tokens), and the dispatch rows.  The
-// tokens are walked 1024 at a time (one per thread) in ascending order.
+// tokens are walked in ascending order, kFillTokens consecutive ones per
+// thread and round.
 constexpr int kFillThreads = 1024;
+constexpr int kFillTokens = 2;
 
 __global__ void __launch_bounds__(kFillThreads) k_moe_fill(const int32_t *__restrict__ topk_idx,
                                                   const float *__restrict__ topk_prob, const int32_t *__restrict__ counts,
@@ -160,35 +179,72 @@ __global__ void __launch_bounds__(kFillThreads) k_moe_fill(const int32_t *__rest
             if (total > Mcap) set_status(status, FP8_ERR_INVALID_ARG);
         }
     }
-    int64_t free_seen = 0, placed = 0;
-    for (int64_t t0 = 0; t0 < T; t0 += blockDim.x) {
-        const int64_t t = t0 + threadIdx.x;
-        const bool in = t < T;
-        int k_hit = -1;
-        if (in)
-            for (int k = 0; k < topk; ++k)
-                if (topk_idx[t * topk + k] == e) k_hit = k;
-        const bool routed = k_hit >= 0;
-        const bool fr = in && !routed;
-        int nfree = 0;
-        const int fpos = block_excl_scan(fr ? 1 : 0, warp_tot, nfree);
-        const bool pad = fr && (free_seen + fpos < need);
-        const bool member = routed || pad;
-        int nmem = 0;
-        const int mpos = block_excl_scan(member ? 1 : 0, warp_tot, nmem);
-        if (member) {
-            const int64_t r = off + placed + mpos;
-            if (r < Mcap) {
-                row_token[r] = (int32_t)t;
-                row_prob[r] = routed ? topk_prob[t * topk + k_hit] : 0.0f;
-                if (row_is_pad) row_is_pad[r] = pad ? 1 : 0;
-            }
+    // The padding entries are the first `need` tokens not routed to e, and the
+    // rows are the members in token order, so with r_t = tokens before t
+    // routed to e (and t - r_t free ones): a routed token's row is
+    // off + r_t + min(need, t - r_t), a free token is padding iff
+    // t - r_t < need, and then its row is off + t.  One block-wide scan of
+    // the routed counts per round of kFillThreads x kFillTokens tokens.
+    if (threadIdx.x == 0 && need > T - c) set_status(status, FP8_ERR_INVALID_ARG);   // too few free tokens
+    // which of token t's choices is e (-1: none); top-8 rows are read as two
+    // coalesced 16-byte loads when aligned
+    const bool vec8 = topk == 8 && (reinterpret_cast<uintptr_t>(topk_idx) & 15u) == 0;
+    auto choices = [&](int64_t t, int4 &a, int4 &b) {
+        if (t < T && vec8) {
+            a = __ldg(reinterpret_cast<const int4 *>(topk_idx + t * 8));
+            b = __ldg(reinterpret_cast<const int4 *>(topk_idx + t * 8) + 1);
+        } else if (t < T) {
+            int v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = k < topk ? __ldg(topk_idx + t * topk + k) : -1;
+            a = make_int4(v[0], v[1], v[2], v[3]);
+            b = make_int4(v[4], v[5], v[6], v[7]);
+        } else {
+            a = b = make_int4(-1, -1, -1, -1);
         }
-        free_seen += nfree;
-        placed += nmem;
+    };
+    int64_t r_prev = 0;
+    int4 cv[kFillTokens][2];
+#pragma unroll
+    for (int i = 0; i < kFillTokens; ++i) choices((int64_t)threadIdx.x * kFillTokens + i, cv[i][0], cv[i][1]);
+    for (int64_t t0 = 0; t0 < T; t0 += (int64_t)kFillThreads * kFillTokens) {
+        const int64_t tb = t0 + (int64_t)threadIdx.x * kFillTokens;
+        int k_hit[kFillTokens];
+#pragma unroll
+        for (int i = 0; i < kFillTokens; ++i) {
+            const int v[8] = {cv[i][0].x, cv[i][0].y, cv[i][0].z, cv[i][0].w,
+                              cv[i][1].x, cv[i][1].y, cv[i][1].z, cv[i][1].w};
+            k_hit[i] = -1;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (v[k] == e) k_hit[i] = k;
+        }
+        // the next round's loads fly during the scan
+#pragma unroll
+        for (int i = 0; i < kFillTokens; ++i)
+            choices(tb + (int64_t)kFillThreads * kFillTokens + i, cv[i][0], cv[i][1]);
+        int nr = 0;
+#pragma unroll
+        for (int i = 0; i < kFillTokens; ++i) nr += k_hit[i] >= 0;
+        int nround = 0;
+        int64_t rt = r_prev + block_excl_scan_count(nr, warp_tot, nround);
+#pragma unroll
+        for (int i = 0; i < kFillTokens; ++i) {
+            const int64_t t = tb + i;
+            const bool routed = k_hit[i] >= 0;
+            const int64_t ft = t - rt;
+            if (t < T && (routed || ft < need)) {
+                const int64_t r = off + (routed ? rt + (ft < need ? ft : need) : t);
+                if (r < Mcap) {
+                    row_token[r] = (int32_t)t;
+                    row_prob[r] = routed ? topk_prob[t * topk + k_hit[i]] : 0.0f;
+                    if (row_is_pad) row_is_pad[r] = routed ? 0 : 1;
+                }
+            }
+            rt += routed;
+        }
+        r_prev += nround;
     }
-    // fewer free tokens than padding needed: the edit is impossible
-    if (threadIdx.x == 0 && placed != padded_count(c, align)) set_status(status, FP8_ERR_INVALID_ARG);
     // rows past the last expert
     for (int64_t r = total + (int64_t)e * blockDim.x + threadIdx.x; r < Mcap; r += (int64_t)E * blockDim.x) {
         row_token[r] = -1;
