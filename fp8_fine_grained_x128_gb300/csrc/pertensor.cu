@@ -90,16 +90,29 @@ __device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &
         out.y = (cvt2<FMT>(qv[4], qv[5]) | (cvt2<FMT>(qv[6], qv[7]) << 16)) | sign_bits4(v.z, v.w);
     }
     if (STATS) {
-        const float fm = fmax_of(FMT);
+        // four elements at a time: bit 7 of byte i flags element i
+        constexpr uint32_t kMaxMag = (FMT == FP8_E4M3 ? 0x7Eu : 0x7Bu) * 0x01010101u;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const uint32_t xb = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
-            const uint32_t code = ((e < 4 ? out.x : out.y) >> (8 * (e & 3))) & 0xFFu;
-            const bool nzero = (xb & 0x7FFFu) != 0;
-            c.nz += nzero;
-            c.uf += nzero && ((code & 0x7Fu) == 0);
-            c.sat += fabsf(qv[e]) > fm;
-            bitmap_set(bmx, key_bf16(xb));
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t w0 = w[2 * h], w1 = w[2 * h + 1], cw = h ? out.y : out.x;
+            const uint32_t nzb = __byte_perm((w0 & 0x7FFF7FFFu) + 0x7FFF7FFFu, (w1 & 0x7FFF7FFFu) + 0x7FFF7FFFu,
+                                             0x7531) & 0x80808080u;                       // x != +-0
+            const uint32_t zc = ~((cw & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) & 0x80808080u;       // code +-0
+            c.nz += __popc(nzb);
+            c.uf += __popc(nzb & zc);
+            // |x/s| > fmax only where the code saturated to the largest magnitude
+            const uint32_t y = (cw & 0x7F7F7F7Fu) ^ kMaxMag;
+            if ((y - 0x01010101u) & ~y & 0x80808080u) {
+                const float fm = fmax_of(FMT);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) c.sat += fabsf(qv[4 * h + e]) > fm;
+            }
+        }
+        // presence of the raw BF16 patterns; +0 and -0 are merged in the count
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            bitmap_set(bmx, w[j] & 0xFFFFu);
+            bitmap_set(bmx, w[j] >> 16);
         }
     }
     return out;
@@ -196,6 +209,9 @@ __device__ void finalize_distinct_and_reset(fp8_stats_t *stats, PtWorkspace *ws,
     __threadfence();
     if (STATS) {
         uint32_t din = 0, dout = 0;
+        // +0 and -0 are one value: bit 0 of words 0 and 1024 (keys 0x0000, 0x8000)
+        if (threadIdx.x == 0 && (__ldcg(&ws->bmx[0]) & __ldcg(&ws->bmx[1024]) & 1u)) din = (uint32_t)-1;
+        __syncthreads();
         for (int i = threadIdx.x; i < 2048; i += blockDim.x) {
             din += __popc(__ldcg(&ws->bmx[i]));
             ws->bmx[i] = 0;
