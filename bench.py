@@ -464,7 +464,7 @@ class RowBench:
             del W7, D7
         if want("a6") or want("a7"):
             del X6, q6, q6T
-        if want("a9") or want("a10"):
+        if want("a9") or want("a10") or want("a12") or want("a13"):
             T, Hd, Ex, F, topk = 8192, 2048, 128, 768, 8
             xb, logits, _, _ = synth.moe_inputs()
             cap = T * topk + Ex * 127
@@ -502,6 +502,25 @@ class RowBench:
             put(self.tensor("a10_grouped_gemm_down", lambda: fg.grouped_gemm(offs, qh, sh, qdn, sdn, Yd),
                             2.0 * T * topk * Hd * F, "unpadded FLOPs; N=2048, K=768"))
             del qgu, qdn, GU, Yd, qh
+        if want("a12"):
+            # MoE weight gradients over each expert's dispatch rows (E5M2 gradient x E4M3
+            # activation, transposed copies with 1x128 scales along the rows, FP32 out):
+            # dW_down[e] = dY_e^T . H_e and dW_gu[e] = dGU_e^T . X_e
+            for name, n_, k_ in (("a12_grouped_wgrad_down", Hd, F), ("a12_grouped_wgrad_gate_up", 2 * F, Hd)):
+                at, bt = u8(n_, cap).random_(0, 120), u8(k_, cap).random_(0, 120)
+                sa_, sb_ = f32(cap // 128, n_).fill_(1e-3), f32(cap // 128, k_).fill_(1e-2)
+                dW = f32(Ex * n_, k_)
+                put(self.tensor(name, lambda: fg.grouped_gemm_wgrad(offs, at, fg.E5M2, sa_, bt, E, sb_, dW),
+                                2.0 * T * topk * n_ * k_,
+                                f"unpadded FLOPs; {Ex} experts of {n_}x{k_} over {total} dispatch rows"))
+                del at, bt, dW
+        if want("a13"):
+            qe = u8(Ex, 2 * F, Hd).random_(0, 120)
+            se = f32(Ex, 2 * F // 128, Hd // 128).fill_(1e-3)
+            qeT, seT = u8(Ex, Hd, 2 * F), f32(Ex, Hd // 128, 2 * F // 128)
+            put(self.hbm("a13_expert_weights_transpose", lambda: fg.transpose_128x128_batched(qe, se, qeT, seT),
+                         2 * Ex * 2 * F * Hd, f"{Ex} experts x {2 * F}x{Hd} FP8"))
+            del qe, qeT
         if want("a11"):
             GU2 = bf(8192, 28672).normal_()
             H2, dH2, dGU2 = bf(8192, 14336), bf(8192, 14336).normal_(), bf(8192, 28672)

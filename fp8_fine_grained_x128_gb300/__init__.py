@@ -68,6 +68,7 @@ _SIGS = {
     "fp8_quant_1x128": (_INT, [_VP, _I64, _I64, _I64, _INT, _VP, _VP, _VP, _VP, _VP]),
     "fp8_quant_128x128": (_INT, [_VP, _I64, _I64, _I64, _INT, _VP, _VP, _VP, _VP, _VP]),
     "fp8_transpose_128x128": (_INT, [_VP, _VP, _I64, _I64, _VP, _VP, _VP]),
+    "fp8_transpose_128x128_batched": (_INT, [_VP, _VP, _INT, _I64, _I64, _VP, _VP, _VP]),
     "fp8_pertensor_workspace_bytes": (ctypes.c_size_t, []),
     "fp8_quant_pertensor_delayed": (_INT, [_VP, _I64, _I64, _I64, ctypes.POINTER(DelayedRecipe),
                                            _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
@@ -78,6 +79,8 @@ _SIGS = {
                                     _VP, _INT, _I64, _VP]),
     "fp8_grouped_gemm": (_INT, [_INT, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _INT, _I64,
                                 _VP]),
+    "fp8_grouped_gemm_wgrad": (_INT, [_INT, _VP, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _INT, _VP, _VP, _INT,
+                                      _I64, _VP]),
     "fp8_moe_route_pad": (_INT, [_VP, _I64, _INT, _INT, _INT, _I64, _VP, _VP, _VP, _VP, _VP, _VP,
                                  _VP, _VP]),
     "fp8_moe_gather": (_INT, [_VP, _VP, _I64, _I64, _VP, _VP, _INT, _I64, _VP, _VP, _VP]),
@@ -178,6 +181,13 @@ def transpose_128x128(q, s, qT, sT, stream=None):
                                                                 _stream(stream)))
 
 
+def transpose_128x128_batched(q, s, qT, sT, stream=None):
+    """q [B, R, C] codes with scales [B, R/128, C/128] -> qT [B, C, R], sT [B, C/128, R/128]."""
+    B, R, C = q.shape
+    _check("fp8_transpose_128x128_batched",
+           lib().fp8_transpose_128x128_batched(_p(q), _p(s), B, R, C, _p(qT), _p(sT), _stream(stream)))
+
+
 def quant_pertensor_delayed(x, recipe: DelayedRecipe, hist, step, scale, q, workspace, qT=None,
                             stats=None, stream=None):
     R, C, ld = _rows_cols(x)
@@ -222,6 +232,17 @@ def grouped_gemm(offsets, A, sA, B, sB, D, stream=None):
     _check("fp8_grouped_gemm",
            lib().fp8_grouped_gemm(G, _p(offsets), Mcap, N, K, _p(A), _p(sA), _p(B), _p(sB), _p(D), out,
                                   D.stride(0), _stream(stream)))
+
+
+def grouped_gemm_wgrad(offsets, AT, fmtA, sAT, BT, fmtB, sBT, D, stream=None):
+    """D [G*N, ldD]: expert g's AT[:, rows_g] . BT[:, rows_g]^T (transposed copies, 1x128 scales)."""
+    G = offsets.numel() - 1
+    N, Mcap = AT.shape
+    K = BT.shape[0]
+    out = OUT_F32 if D.dtype == torch.float32 else OUT_BF16
+    _check("fp8_grouped_gemm_wgrad",
+           lib().fp8_grouped_gemm_wgrad(G, _p(offsets), Mcap, N, K, _p(AT), fmtA, _p(sAT), _p(BT), fmtB, _p(sBT),
+                                        _p(D), out, D.stride(0), _stream(stream)))
 
 
 # ------------------------------------------------------------------ MoE glue

@@ -155,6 +155,18 @@ FP8FG_API int fp8_transpose_128x128(const void *q, const float *s, int64_t rows,
     return launch_transpose_128x128(q, s, rows, cols, qT, sT, S(stream));
 }
 
+FP8FG_API int fp8_transpose_128x128_batched(const void *q, const float *s, int batch, int64_t rows, int64_t cols,
+                                            void *qT, float *sT, void *stream)
+{
+    if (batch < 0 || batch > 65535) return FP8_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || rows % 128 != 0 || cols % 128 != 0) return FP8_ERR_SHAPE;
+    if (rows / 128 >= 65536 || cols / 128 >= ((int64_t)1 << 31)) return FP8_ERR_SHAPE;
+    if (batch == 0 || rows == 0 || cols == 0) return FP8_OK;
+    if (!q || !s || !qT || !sT) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(qT)) return FP8_ERR_ALIGNMENT;
+    return launch_transpose_128x128(q, s, rows, cols, qT, sT, S(stream), batch);
+}
+
 FP8FG_API size_t fp8_pertensor_workspace_bytes(void) { return pertensor_workspace_bytes(); }
 
 FP8FG_API int fp8_quant_pertensor_delayed(const void *x, int64_t rows, int64_t cols, int64_t ldx,
@@ -240,6 +252,31 @@ FP8FG_API int fp8_grouped_gemm(int G, const int32_t *group_offsets, int64_t M_ca
         return FP8_ERR_ALIGNMENT;
     FP8FG_STATUS_OR_RETURN(st);
     return launch_grouped_gemm(G, group_offsets, M_capacity, N, K, A, sA, B, sB, D, out_dtype, ldD, st, S(stream));
+}
+
+FP8FG_API int fp8_grouped_gemm_wgrad(int G, const int32_t *group_offsets, int64_t M_capacity, int64_t N, int64_t K,
+                                     const void *AT, int fmtA, const float *sAT, const void *BT, int fmtB,
+                                     const float *sBT, void *D, int out_dtype, int64_t ldD, void *stream)
+{
+    if (G < 1 || G > 1024) return FP8_ERR_INVALID_ARG;
+    if (!fmt_ok(fmtA) || !fmt_ok(fmtB)) return FP8_ERR_INVALID_ARG;
+    if (out_dtype != FP8_OUT_BF16 && out_dtype != FP8_OUT_F32) return FP8_ERR_INVALID_ARG;
+    if (M_capacity < 0 || N < 0 || K < 0 || M_capacity % 128 != 0 || N % 128 != 0 || K % 128 != 0)
+        return FP8_ERR_SHAPE;
+    if (M_capacity >= ((int64_t)1 << 31) || (int64_t)G * N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31))
+        return FP8_ERR_SHAPE;
+    if (N == 0 || K == 0) return FP8_OK;
+    if (!D) return FP8_ERR_INVALID_ARG;
+    if (ldD < K) return FP8_ERR_SHAPE;
+    const int64_t esz = out_dtype == FP8_OUT_F32 ? 4 : 2;
+    if (!aligned16(D) || (ldD * esz) % 16 != 0) return FP8_ERR_ALIGNMENT;
+    if (M_capacity > 0) {
+        if (!group_offsets || !AT || !sAT || !BT || !sBT) return FP8_ERR_INVALID_ARG;
+        if (!aligned16(AT) || !aligned16(BT) || !aligned16(sAT) || !aligned16(sBT)) return FP8_ERR_ALIGNMENT;
+    }
+    FP8FG_STATUS_OR_RETURN(st);
+    return launch_grouped_wgrad(G, group_offsets, M_capacity, N, K, AT, fmtA, sAT, BT, fmtB, sBT, D, out_dtype, ldD,
+                                st, S(stream));
 }
 
 FP8FG_API int fp8_moe_route_pad(const float *logits, int64_t T, int E, int topk, int align, int64_t M_capacity,

@@ -82,6 +82,10 @@ struct GemmArgs {
 };
 
 enum { SB_BLOCK = 0, SB_ROW = 1 };
+// Grouping of the tiles: none; by rows of A (MoE forward/dgrad: each M tile
+// belongs to one expert, whose B it uses); by K (MoE wgrad: each expert's
+// output is a full M x N matrix contracted over that expert's K chunks only).
+enum { G_NONE = 0, G_ROWS = 1, G_K = 2 };
 
 constexpr int kScaleDepth = 4;     // chunks of scales staged ahead of the epilogue
 
@@ -125,6 +129,54 @@ __device__ __forceinline__ int group_of_row(const int32_t *off, int G, int row)
         else hi = mid - 1;
     }
     return lo;
+}
+
+// What one output tile reads and writes; every role decodes tiles with it.
+struct TileInfo {
+    int a_row;        // first row of the A tile
+    int b_row;        // first row of the B tile (in the stacked B for G_ROWS)
+    int n0;           // first output column
+    int kg0;          // first K chunk (global index into K and the scale arrays)
+    int nk;           // K chunks of this tile (0 for an empty group in G_K)
+    int grp;          // group
+    int64_t out_row;  // first output row
+};
+
+template <int BN, int GMODE>
+__device__ __forceinline__ TileInfo tile_info(int tile, int num_mt, int num_nt, const GemmArgs &a,
+                                              const int32_t *off)
+{
+    TileInfo t;
+    int mt, nt;
+    if (GMODE == G_K) {
+        const int per = num_mt * num_nt;
+        t.grp = tile / per;
+        const int rem = tile - t.grp * per;
+        mt = rem / num_nt;
+        nt = rem - mt * num_nt;
+        t.kg0 = off[t.grp] >> 7;
+        t.nk = (off[t.grp + 1] - off[t.grp]) >> 7;
+        t.out_row = (int64_t)t.grp * a.M + mt * 128;
+        t.b_row = nt * BN;
+    } else if (GMODE == G_ROWS) {
+        mt = tile / num_nt;
+        nt = tile - mt * num_nt;
+        t.grp = group_of_row(off, a.G, mt * 128);
+        t.kg0 = 0;
+        t.nk = a.K / 128;
+        t.out_row = mt * 128;
+        t.b_row = t.grp * a.N + nt * BN;
+    } else {
+        tile_coords_raster(tile, num_mt, num_nt, a.raster_gm, mt, nt);
+        t.grp = 0;
+        t.kg0 = 0;
+        t.nk = a.K / 128;
+        t.out_row = mt * 128;
+        t.b_row = nt * BN;
+    }
+    t.a_row = mt * 128;
+    t.n0 = nt * BN;
+    return t;
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
@@ -187,7 +239,7 @@ __device__ __forceinline__ void store_pair(void *D, int64_t ldD, int out_f32, in
     else *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(D) + row * ldD + col) = pack_bf16x2(lo, hi);
 }
 
-template <int BN, int STAGES, bool PROMOTE, int SBG, bool GROUPED, bool TSTORE>
+template <int BN, int STAGES, bool PROMOTE, int SBG, int GMODE, bool TSTORE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmD, uint32_t idesc, GemmArgs a)
@@ -232,7 +284,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *bad_offsets = 0;
         fence_barrier_init();
     }
-    if (GROUPED) {
+    if (GMODE != G_NONE) {
         for (int i = threadIdx.x; i <= a.G; i += blockDim.x) sh_off[i] = a.offsets[i];
     }
     if (warp == 1) {
@@ -249,21 +301,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (GROUPED && threadIdx.x == 0) {
+    if (GMODE != G_NONE && threadIdx.x == 0) {
         bool ok = sh_off[0] == 0;
         for (int i = 0; i < a.G; ++i) ok = ok && (sh_off[i] <= sh_off[i + 1]) && ((sh_off[i + 1] & 127) == 0);
-        ok = ok && sh_off[a.G] <= a.M;
+        ok = ok && sh_off[a.G] <= (GMODE == G_K ? a.K : a.M);   // the grouped extent's capacity
         if (!ok) {
             *bad_offsets = 1;
             set_status(a.status, FP8_ERR_INVALID_ARG);
         }
     }
-    if (GROUPED) __syncthreads();
+    if (GMODE != G_NONE) __syncthreads();
 
     const int num_nt = a.N / BN;
-    const int num_mt = GROUPED ? (*bad_offsets ? 0 : sh_off[a.G] / 128) : a.M / 128;
-    const int ntiles = num_mt * num_nt;
-    const int nk = a.K / 128;
+    const int num_mt = GMODE == G_ROWS ? sh_off[a.G] / 128 : a.M / 128;
+    int ntiles = GMODE == G_K ? a.G * num_mt * num_nt : num_mt * num_nt;
+    if (GMODE != G_NONE && *bad_offsets) ntiles = 0;
 
     if (warp < kEpiWarp0) {
         regs_dec<RegSplit<SBG>::kCtrl>();
@@ -272,18 +324,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                int mt, nt;
-                if (GROUPED) { mt = tile / num_nt; nt = tile - mt * num_nt; }
-                else tile_coords_raster(tile, num_mt, num_nt, a.raster_gm, mt, nt);
-                const int brow = nt * BN + (GROUPED ? group_of_row(sh_off, a.G, mt * 128) * a.N : 0);
-                for (int kb = 0; kb < nk; ++kb) {
+                const TileInfo ti = tile_info<BN, GMODE>(tile, num_mt, num_nt, a, sh_off);
+                for (int kb = 0; kb < ti.nk; ++kb) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!wait_or_abort(&empty[s], ph ^ 1, abort_flag, a.status)) { ok = false; break; }
                     uint8_t *st = smem + s * L::kStage;
                     mbar_arrive_expect_tx(&full[s], L::kStage);
-                    tma_load_2d(st, &tmA, &full[s], kb * 128, mt * 128);
-                    tma_load_2d(st + L::kA, &tmB, &full[s], kb * 128, brow);
+                    tma_load_2d(st, &tmA, &full[s], (ti.kg0 + kb) * 128, ti.a_row);
+                    tma_load_2d(st + L::kA, &tmB, &full[s], (ti.kg0 + kb) * 128, ti.b_row);
                     ++it;
                 }
             }
@@ -295,6 +344,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t it = 0, cc = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const int nk = tile_info<BN, GMODE>(tile, num_mt, num_nt, a, sh_off).nk;
                 uint32_t buf = cc % L::kNbuf;
                 if (!PROMOTE) {
                     if (!wait_or_abort(&tempty[buf], ((cc / L::kNbuf) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
@@ -348,13 +398,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t cs = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                int mt, nt;
-                if (GROUPED) { mt = tile / num_nt; nt = tile - mt * num_nt; }
-                else tile_coords_raster(tile, num_mt, num_nt, a.raster_gm, mt, nt);
-                const int m0 = mt * 128, n0 = nt * BN;
+                const TileInfo ti = tile_info<BN, GMODE>(tile, num_mt, num_nt, a, sh_off);
+                const int m0 = ti.a_row, n0 = ti.n0;
                 const float *sB = a.sB;
-                if (GROUPED) sB += (int64_t)group_of_row(sh_off, a.G, m0) * a.sB_group_stride;
-                for (int kb = 0; kb < nk; ++kb, ++cs) {
+                if (GMODE == G_ROWS) sB += (int64_t)ti.grp * a.sB_group_stride;
+                for (int kb = ti.kg0; kb < ti.kg0 + ti.nk; ++kb, ++cs) {
                     const int slot = cs % kScaleDepth;
                     float b0 = 0.0f, b1 = 0.0f, av = 0.0f;
                     if (SBG == SB_BLOCK) {
@@ -394,15 +442,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t cc = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            int mt, nt;
-            if (GROUPED) { mt = tile / num_nt; nt = tile - mt * num_nt; }
-            else tile_coords_raster(tile, num_mt, num_nt, a.raster_gm, mt, nt);
-            const int m0 = mt * 128, n0 = nt * BN;
+            const TileInfo ti = tile_info<BN, GMODE>(tile, num_mt, num_nt, a, sh_off);
+            const int64_t m0 = ti.out_row;   // output row of the tile
+            const int n0 = ti.n0;
             if (PROMOTE) {
                 uint64_t acc[NP];
 #pragma unroll
                 for (int i = 0; i < NP; ++i) acc[i] = 0ull;
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = 0; kb < ti.nk; ++kb) {
                     const uint32_t buf = cc % L::kNbuf;
                     const int slot = cc % kScaleDepth;
                     if (!warp_wait_or_abort(&sc_full[slot], (cc / kScaleDepth) & 1, abort_flag, a.status)) { ok = false; break; }
@@ -496,7 +543,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         *tile_go = go;
                         if (go) {
 #pragma unroll
-                            for (int b = 0; b < BN / 64; ++b) tma_store_2d(&tmD, stg + b * 16384, n0 + 64 * b, m0);
+                            for (int b = 0; b < BN / 64; ++b) tma_store_2d(&tmD, stg + b * 16384, n0 + 64 * b, (int)m0);
                             bulk_commit_group();
                         }
                     }
@@ -609,13 +656,13 @@ static bool make_out_map(CUtensorMap *map, void *ptr, uint64_t cols, uint64_t ro
            CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, bool PROMOTE, int SBG, bool GROUPED, bool TSTORE = false>
+template <int BN, int STAGES, bool PROMOTE, int SBG, int GMODE, bool TSTORE = false>
 static int run_gemm(const CUtensorMap &mA, const CUtensorMap &mB, const CUtensorMap &mD, uint32_t idesc,
                     const GemmArgs &args, int grid, cudaStream_t st)
 {
     using L = GemmSmem<BN, STAGES, TSTORE>;
     static_assert(L::kBytes <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
-    auto kern = k_gemm<BN, STAGES, PROMOTE, SBG, GROUPED, TSTORE>;
+    auto kern = k_gemm<BN, STAGES, PROMOTE, SBG, GMODE, TSTORE>;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -672,21 +719,21 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const 
     const bool tensor = granA == FP8_GRAN_TENSOR;
     if (BN == 256) {
         const uint32_t idesc = idesc_f8f6f4(fmtA, fmtB, 128, 256);
-        if (tensor) return run_gemm<256, 4, false, SB_BLOCK, false>(mA, mB, mA, idesc, g, grid, st);
-        if (granB == FP8_GRAN_1x128) return run_gemm<256, 4, true, SB_ROW, false>(mA, mB, mA, idesc, g, grid, st);
+        if (tensor) return run_gemm<256, 4, false, SB_BLOCK, G_NONE>(mA, mB, mA, idesc, g, grid, st);
+        if (granB == FP8_GRAN_1x128) return run_gemm<256, 4, true, SB_ROW, G_NONE>(mA, mB, mA, idesc, g, grid, st);
         if (!g.out_f32 && K <= kTmaStoreMaxK) {
             // BF16 output leaves through shared memory and TMA stores (one
             // operand stage fewer makes room for the staged tile)
             CUtensorMap mD;
             if (!make_out_map(&mD, D, (uint64_t)N, (uint64_t)M, (uint64_t)ldD)) return FP8_ERR_CUDA;
-            return run_gemm<256, 3, true, SB_BLOCK, false, true>(mA, mB, mD, idesc, g, grid, st);
+            return run_gemm<256, 3, true, SB_BLOCK, G_NONE, true>(mA, mB, mD, idesc, g, grid, st);
         }
-        return run_gemm<256, 4, true, SB_BLOCK, false>(mA, mB, mA, idesc, g, grid, st);
+        return run_gemm<256, 4, true, SB_BLOCK, G_NONE>(mA, mB, mA, idesc, g, grid, st);
     } else {
         const uint32_t idesc = idesc_f8f6f4(fmtA, fmtB, 128, 128);
-        if (tensor) return run_gemm<128, 6, false, SB_BLOCK, false>(mA, mB, mA, idesc, g, grid, st);
-        if (granB == FP8_GRAN_1x128) return run_gemm<128, 6, true, SB_ROW, false>(mA, mB, mA, idesc, g, grid, st);
-        return run_gemm<128, 6, true, SB_BLOCK, false>(mA, mB, mA, idesc, g, grid, st);
+        if (tensor) return run_gemm<128, 6, false, SB_BLOCK, G_NONE>(mA, mB, mA, idesc, g, grid, st);
+        if (granB == FP8_GRAN_1x128) return run_gemm<128, 6, true, SB_ROW, G_NONE>(mA, mB, mA, idesc, g, grid, st);
+        return run_gemm<128, 6, true, SB_BLOCK, G_NONE>(mA, mB, mA, idesc, g, grid, st);
     }
 }
 
@@ -724,12 +771,52 @@ int launch_grouped_gemm(int G, const int32_t *offsets, int64_t Mcap, int64_t N, 
         if (!g.out_f32 && K <= kTmaStoreMaxK) {
             CUtensorMap mD;
             if (!make_out_map(&mD, D, (uint64_t)N, (uint64_t)Mcap, (uint64_t)ldD)) return FP8_ERR_CUDA;
-            return run_gemm<256, 3, true, SB_BLOCK, true, true>(mA, mB, mD, idesc, g, grid, st);
+            return run_gemm<256, 3, true, SB_BLOCK, G_ROWS, true>(mA, mB, mD, idesc, g, grid, st);
         }
-        return run_gemm<256, 4, true, SB_BLOCK, true>(mA, mB, mA, idesc, g, grid, st);
+        return run_gemm<256, 4, true, SB_BLOCK, G_ROWS>(mA, mB, mA, idesc, g, grid, st);
     }
-    return run_gemm<128, 6, true, SB_BLOCK, true>(mA, mB, mA, idesc_f8f6f4(FP8_E4M3, FP8_E4M3, 128, 128), g, grid,
+    return run_gemm<128, 6, true, SB_BLOCK, G_ROWS>(mA, mB, mA, idesc_f8f6f4(FP8_E4M3, FP8_E4M3, 128, 128), g, grid,
                                                   st);
+}
+
+// MoE wgrad: expert g's D[g] [N][K] contracts the transposed copies AT [N][Mcap]
+// and BT [K][Mcap] over the dispatch rows [off[g], off[g+1]) only.
+int launch_grouped_wgrad(int G, const int32_t *offsets, int64_t Mcap, int64_t N, int64_t K, const void *AT, int fmtA,
+                         const float *sAT, const void *BT, int fmtB, const float *sBT, void *D, int out_dtype,
+                         int64_t ldD, int *status, cudaStream_t st)
+{
+    if (N == 0 || K == 0) return FP8_OK;
+    if (Mcap == 0) {   // every expert is empty: D = 0
+        const size_t esz = out_dtype == FP8_OUT_F32 ? 4 : 2;
+        return cudaMemset2DAsync(D, (size_t)ldD * esz, 0, (size_t)K * esz, (size_t)G * N, st) == cudaSuccess
+                   ? FP8_OK
+                   : FP8_ERR_CUDA;
+    }
+    const int BN = (K % 256 == 0) ? 256 : 128;
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, AT, (uint64_t)Mcap, (uint64_t)N, 128) || !make_map(&mB, BT, (uint64_t)Mcap, (uint64_t)K, BN))
+        return FP8_ERR_CUDA;
+    GemmArgs g{};
+    g.M = (int)N;        // rows of each expert's output
+    g.N = (int)K;        // columns of each expert's output
+    g.K = (int)Mcap;     // contraction capacity; expert g uses [off[g], off[g+1])
+    g.sA = sAT;
+    g.granA = FP8_GRAN_1x128;
+    g.ldsA = N;
+    g.sB = sBT;
+    g.ldsB = K;
+    g.D = D;
+    g.ldD = ldD;
+    g.out_f32 = out_dtype == FP8_OUT_F32;
+    g.offsets = offsets;
+    g.G = G;
+    g.status = status;
+    g.raster_gm = 1;
+    const int64_t ntiles = (int64_t)G * (N / 128) * (K / BN);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ntiles, sm_count()));
+    const uint32_t idesc = idesc_f8f6f4(fmtA, fmtB, 128, BN);
+    if (BN == 256) return run_gemm<256, 4, true, SB_ROW, G_K>(mA, mB, mA, idesc, g, grid, st);
+    return run_gemm<128, 6, true, SB_ROW, G_K>(mA, mB, mA, idesc, g, grid, st);
 }
 
 }  // namespace fp8fg

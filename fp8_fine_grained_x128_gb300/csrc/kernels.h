@@ -18,8 +18,9 @@ int launch_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, i
                        void *qT, float *sT, int *status, cudaStream_t st);
 int launch_quant_128x128(const void *w, int64_t rows, int64_t cols, int64_t ldw, int fmt, void *q, float *s,
                          void *qT, float *sT, int *status, cudaStream_t st);
+// batch matrices of [rows][cols] stored back to back (scales likewise)
 int launch_transpose_128x128(const void *q, const float *s, int64_t rows, int64_t cols, void *qT, float *sT,
-                             cudaStream_t st);
+                             cudaStream_t st, int batch = 1);
 
 // pertensor.cu
 size_t pertensor_workspace_bytes();
@@ -37,6 +38,9 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const 
 int launch_grouped_gemm(int G, const int32_t *offsets, int64_t Mcap, int64_t N, int64_t K, const void *A,
                         const float *sA, const void *B, const float *sB, void *D, int out_dtype, int64_t ldD,
                         int *status, cudaStream_t st);
+int launch_grouped_wgrad(int G, const int32_t *offsets, int64_t Mcap, int64_t N, int64_t K, const void *AT, int fmtA,
+                         const float *sAT, const void *BT, int fmtB, const float *sBT, void *D, int out_dtype,
+                         int64_t ldD, int *status, cudaStream_t st);
 
 // moe.cu
 int launch_moe_route_pad(const float *logits, int64_t T, int E, int topk, int align, int64_t Mcap,

@@ -347,6 +347,11 @@ __global__ void __launch_bounds__(256) k_transpose_128x128(const uint8_t *__rest
     const int t = threadIdx.x;
     const int64_t cb = blockIdx.x, rb = blockIdx.y;
     const int64_t r0 = rb * 128, c0 = cb * 128;
+    // blockIdx.z: matrix of a batch of equally shaped ones, stored back to back
+    q += (int64_t)blockIdx.z * rows * cols;
+    qT += (int64_t)blockIdx.z * rows * cols;
+    s += (int64_t)blockIdx.z * (rows / 128) * (cols / 128);
+    sT += (int64_t)blockIdx.z * (rows / 128) * (cols / 128);
     // 128 rows x 8 chunks of 16 B: 4 chunks per thread
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -430,10 +435,10 @@ int launch_quant_128x128(const void *w, int64_t rows, int64_t cols, int64_t ldw,
 }
 
 int launch_transpose_128x128(const void *q, const float *s, int64_t rows, int64_t cols, void *qT, float *sT,
-                             cudaStream_t st)
+                             cudaStream_t st, int batch)
 {
-    if (rows == 0 || cols == 0) return FP8_OK;
-    dim3 grid((unsigned)(cols / 128), (unsigned)(rows / 128));
+    if (rows == 0 || cols == 0 || batch == 0) return FP8_OK;
+    dim3 grid((unsigned)(cols / 128), (unsigned)(rows / 128), (unsigned)batch);
     k_transpose_128x128<<<grid, 256, 0, st>>>(static_cast<const uint8_t *>(q), s, rows, cols,
                                               static_cast<uint8_t *>(qT), sT);
     return check_launch();

@@ -159,6 +159,13 @@ FP8FG_API int fp8_quant_128x128(const void *w, int64_t rows, int64_t cols, int64
 FP8FG_API int fp8_transpose_128x128(const void *q, const float *s, int64_t rows, int64_t cols,
                                     void *qT, float *sT, void *stream);
 
+/* The same for `batch` matrices stored back to back (e.g. the weights of the
+ * MoE experts before their grouped dgrad): q [batch][rows][cols], s
+ * [batch][rows/128][cols/128] -> qT [batch][cols][rows], sT
+ * [batch][cols/128][rows/128].  0 <= batch <= 65535. */
+FP8FG_API int fp8_transpose_128x128_batched(const void *q, const float *s, int batch, int64_t rows,
+                                            int64_t cols, void *qT, float *sT, void *stream);
+
 /* Bytes of the caller-owned workspace used by fp8_quant_pertensor_delayed and
  * by fp8_quant_stats(FP8_GRAN_TENSOR).  Zero it once (cudaMemset) before the
  * first use; every call that completes leaves it zeroed again. */
@@ -247,6 +254,25 @@ FP8FG_API int fp8_grouped_gemm(int G, const int32_t *group_offsets, int64_t M_ca
                                int64_t N, int64_t K, const void *A, const float *sA,
                                const void *B, const float *sB, void *D, int out_dtype,
                                int64_t ldD, void *stream);
+
+/* Grouped MoE weight gradient ([FP8-RL]: FP8 on the MoE expert layers; [Ling]
+ * monitor table "grad (transpose)": the wgrad operands are the copies
+ * quantized 128x1 along the token dimension).  Expert g's dispatch rows are
+ * [off[g], off[g+1]) of two dispatch-ordered tensors; AT and BT are their
+ * transposed copies (fp8_quant_1x128 with qT, sT), so
+ *   D[g] = AT[:, off[g]:off[g+1]] . BT[:, off[g]:off[g+1]]^T, [N][K],
+ * promoted per 128 rows with both operands' scales; an expert without rows
+ * gets D[g] = 0.
+ * group_offsets: DEVICE int32[G+1], 0 = off[0] <= ... <= off[G] <= M_capacity,
+ *   multiples of 128 (checked on the device: FP8_ERR_INVALID_ARG).
+ * AT [N][M_capacity] (fmtA) with scales S[M_capacity/128][N];
+ * BT [K][M_capacity] (fmtB) with scales S[M_capacity/128][K];
+ * D [G*N][ldD] (expert g at rows g*N ..), FP8_OUT_F32 or FP8_OUT_BF16.
+ * N, K, M_capacity % 128 == 0, 1 <= G <= 1024. */
+FP8FG_API int fp8_grouped_gemm_wgrad(int G, const int32_t *group_offsets, int64_t M_capacity,
+                                     int64_t N, int64_t K, const void *AT, int fmtA, const float *sAT,
+                                     const void *BT, int fmtB, const float *sBT, void *D,
+                                     int out_dtype, int64_t ldD, void *stream);
 
 /* -------------------------------------------------------------- MoE glue */
 

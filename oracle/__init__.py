@@ -91,6 +91,8 @@ def lib():
                                                    ctypes.c_int, i64, i64, vp, vp, vp]),
                 "orc_grouped_gemm_points": (ctypes.c_int, [ctypes.c_int, vp, i64, i64, vp, vp, i64,
                                                            vp, vp, i64, vp, vp, vp]),
+                "orc_grouped_wgrad_points": (ctypes.c_int, [ctypes.c_int, vp, i64, i64, i64, vp, ctypes.c_int,
+                                                            vp, vp, ctypes.c_int, vp, i64, vp, vp, vp, vp]),
                 "orc_moe_route": (ctypes.c_int, [i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
                                                  vp, vp, vp, vp, vp, i64, vp, vp, vp, vp]),
                 "orc_moe_gather": (None, [vp, vp, i64, i64, vp, i64, i64, vp, vp]),
@@ -300,6 +302,32 @@ def grouped_gemm_points(offsets, A, sA, ldsA, B, sB, pm, pn):
     if st != OK:
         raise ValueError(f"orc_grouped_gemm_points status {st}")
     return out
+
+
+def grouped_wgrad_points(offsets, AT, fmtA, sA, BT, fmtB, sB, pg, pn, pk):
+    """MoE grouped wgrad at points (g, n, k): D_g = AT[:, rows of g] . BT[:, rows of g]^T
+    with 1x128 scales along the rows, S[ldt/128][N] and S[ldt/128][K]; 0 for an empty group."""
+    off = _c(offsets, np.int32)
+    AT = _c(AT, np.uint8)
+    BT = _c(BT, np.uint8)
+    N, ldt = AT.shape
+    K = BT.shape[0]
+    sA = _c(sA, np.float32)
+    sB = _c(sB, np.float32)
+    pg, pn, pk = (_c(np.ravel(v), np.int64) for v in (pg, pn, pk))
+    out = np.empty(pg.size, np.float64)
+    st = lib().orc_grouped_wgrad_points(len(off) - 1, _ptr(off), N, K, ldt, _ptr(AT), fmtA, _ptr(sA), _ptr(BT),
+                                        fmtB, _ptr(sB), pg.size, _ptr(pg), _ptr(pn), _ptr(pk), _ptr(out))
+    if st != OK:
+        raise ValueError(f"orc_grouped_wgrad_points status {st}")
+    return out
+
+
+def grouped_wgrad_full(offsets, AT, fmtA, sA, BT, fmtB, sB):
+    """All of D [G][N][K] of grouped_wgrad_points."""
+    G, N, K = len(offsets) - 1, AT.shape[0], BT.shape[0]
+    gg, nn, kk = np.meshgrid(np.arange(G), np.arange(N), np.arange(K), indexing="ij")
+    return grouped_wgrad_points(offsets, AT, fmtA, sA, BT, fmtB, sB, gg, nn, kk).reshape(G, N, K)
 
 
 # ---------------------------------------------------------------------------

@@ -638,6 +638,43 @@ int orc_grouped_gemm_points(int G, const int32_t *off, int64_t N, int64_t K,
     return ORC_OK;
 }
 
+/* Grouped wgrad of the MoE expert layers ([FP8-RL] MoE expert layers in FP8;
+ * [Ling] "grad (transpose)": the wgrad operands are the transposed copies
+ * quantized along the token dimension).  The dispatch rows of expert g are
+ * [off[g], off[g+1]); the operands are the transposed copies AT [N][ldt] and
+ * BT [K][ldt] of two dispatch-ordered tensors, with 1x128 scales along the
+ * rows, S[ldt/128][N] and S[ldt/128][K].  Expert g's output is
+ *   D_g[n][k] = sum over its 128-row chunks c of sA[c][n] * sB[c][k] *
+ *               (sum over the chunk's rows r of AT[n][r] * BT[k][r]),
+ * zero for an expert without rows.  Points (g, n, k); unrounded FP64. */
+int orc_grouped_wgrad_points(int G, const int32_t *off, int64_t N, int64_t K, int64_t ldt,
+                             const uint8_t *AT, int fmtA, const float *sA,
+                             const uint8_t *BT, int fmtB, const float *sB,
+                             int64_t npts, const int64_t *pg, const int64_t *pn, const int64_t *pk,
+                             double *out)
+{
+    double decA[256], decB[256];
+    int64_t i;
+    int c;
+    if (ldt % 128 != 0) return ORC_BADARG;
+    for (c = 0; c < 256; ++c) {
+        decA[c] = orc_fp8_decode((uint8_t)c, fmtA);
+        decB[c] = orc_fp8_decode((uint8_t)c, fmtB);
+    }
+#pragma omp parallel for schedule(dynamic, 256)
+    for (i = 0; i < npts; ++i) {
+        int64_t g = pg[i], n = pn[i], k = pk[i], r0, rows;
+        if (g < 0 || g >= G || n < 0 || n >= N || k < 0 || k >= K) { out[i] = NAN; continue; }
+        r0 = off[g];
+        rows = off[g + 1] - off[g];
+        if (rows < 0 || r0 % 128 != 0 || rows % 128 != 0 || r0 + rows > ldt) { out[i] = NAN; continue; }
+        /* the group's slice: its chunks start at chunk r0/128 of the scale arrays */
+        out[i] = gemm_point(rows, AT + n * ldt + r0, fmtA, sA + (r0 / 128) * N, ORC_GRAN_1x128, N, n,
+                            BT + k * ldt + r0, fmtB, sB + (r0 / 128) * K, ORC_GRAN_1x128, K, k, decA, decB);
+    }
+    return ORC_OK;
+}
+
 /* ---------------------------------------------------------------------------
  * MoE routing with the padded routing map ([Ling] "FP8 padding routing map";
  * [FP8-RL] MoE expert layers in FP8) -- R8.

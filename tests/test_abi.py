@@ -78,6 +78,19 @@ def test_host_validation_without_launch(lib):
     # grouped GEMM and MoE glue
     assert lib.fp8_grouped_gemm(0, good, 128, 128, 128, good, good, good, good, good, 0, 128, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_grouped_gemm(2, good, 100, 128, 128, good, good, good, good, good, 0, 128, S) == fg.ERR_SHAPE
+    w = lambda G=2, cap=256, N=128, K=128, fa=1, out=1, ld=128, D=good: lib.fp8_grouped_gemm_wgrad(
+        G, good, cap, N, K, good, fa, good, good, 0, good, D, out, ld, S)
+    assert w(G=0) == fg.ERR_INVALID_ARG
+    assert w(fa=5) == fg.ERR_INVALID_ARG
+    assert w(cap=200) == fg.ERR_SHAPE
+    assert w(K=100) == fg.ERR_SHAPE
+    assert w(ld=64) == fg.ERR_SHAPE
+    assert w(out=0, ld=132) == fg.ERR_ALIGNMENT
+    assert w(D=odd) == fg.ERR_ALIGNMENT
+    assert w(N=0) == fg.OK
+    assert lib.fp8_transpose_128x128_batched(good, good, 2, 128, 64, good, good, S) == fg.ERR_SHAPE
+    assert lib.fp8_transpose_128x128_batched(good, good, -1, 128, 128, good, good, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_transpose_128x128_batched(good, good, 0, 128, 128, good, good, S) == fg.OK
     assert lib.fp8_moe_route_pad(good, 16, 300, 8, 128, 1024, good, good, good, good, good, good, None, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_moe_route_pad(good, 16, 8, 9, 128, 1024, good, good, good, good, good, good, None, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_swiglu_fwd(good, 4, 12, good, S) == fg.ERR_SHAPE

@@ -145,3 +145,30 @@ def test_grouped_equals_per_group_gemm():
         ref = a @ b.T
         assert np.all(np.abs(got[lo:hi] - ref) <= 1e-12 * (np.abs(a) @ np.abs(b).T) + 1e-300)
     assert np.all(np.isnan(got[offs[-1]:]))
+
+
+def test_grouped_wgrad_matches_dequantize_then_multiply():
+    """MoE wgrad per expert: D_g = dequant(AT[:, rows_g]) . dequant(BT[:, rows_g])^T with the
+    1x128 scales of the transposed copies (one per 128 rows and per column of the copy);
+    an expert without rows gets exactly zero."""
+    offs = np.array([0, 256, 256, 640, 768], np.int32)    # expert 1 has no rows
+    ldt, N, K = 896, 256, 384                              # capacity past the last expert
+    fa, fb = oracle.E5M2, oracle.E4M3                      # gradient x activation
+    AT = rand_codes((N, ldt), 41, fa)
+    BT = rand_codes((K, ldt), 42, fb)
+    sA = rand_scales((ldt // 128, N), 43)
+    sB = rand_scales((ldt // 128, K), 44)
+    got = oracle.grouped_wgrad_full(offs, AT, fa, sA, BT, fb, sB)
+    deqA = tdec(AT, fa) * np.repeat(sA.astype(np.float64).T, 128, axis=1)   # [N, ldt]
+    deqB = tdec(BT, fb) * np.repeat(sB.astype(np.float64).T, 128, axis=1)   # [K, ldt]
+    for g in range(len(offs) - 1):
+        lo, hi = offs[g], offs[g + 1]
+        if hi == lo:
+            assert np.all(got[g] == 0.0)
+            continue
+        ref = deqA[:, lo:hi] @ deqB[:, lo:hi].T
+        bound = 1e-12 * (np.abs(deqA[:, lo:hi]) @ np.abs(deqB[:, lo:hi]).T) + 1e-300
+        assert np.all(np.abs(got[g] - ref) <= bound)
+    # reading the scales with the row index instead of the chunk index is caught
+    wrong = oracle.grouped_wgrad_full(offs, AT, fa, np.ascontiguousarray(sA[::-1]), BT, fb, sB)
+    assert not np.allclose(wrong[3], got[3])
