@@ -510,9 +510,13 @@ class RowBench:
                 at, bt = u8(n_, cap).random_(0, 120), u8(k_, cap).random_(0, 120)
                 sa_, sb_ = f32(cap // 128, n_).fill_(1e-3), f32(cap // 128, k_).fill_(1e-2)
                 dW = f32(Ex * n_, k_)
-                put(self.tensor(name, lambda: fg.grouped_gemm_wgrad(offs, at, fg.E5M2, sa_, bt, E, sb_, dW),
-                                2.0 * T * topk * n_ * k_,
-                                f"unpadded FLOPs; {Ex} experts of {n_}x{k_} over {total} dispatch rows"))
+                # bound by its FP32 outputs (Ex x n_ x k_ x 4 B) rather than by its FLOPs:
+                # algorithmic bytes = both transposed operands read once + the outputs
+                nbytes = (n_ + k_) * total + (n_ + k_) * (total // 128) * 4 + Ex * n_ * k_ * 4
+                row = self.hbm(name, lambda: fg.grouped_gemm_wgrad(offs, at, fg.E5M2, sa_, bt, E, sb_, dW), nbytes,
+                               f"{Ex} experts of {n_}x{k_} FP32 over {total} dispatch rows")
+                row[1]["tflops_unpadded"] = 2.0 * T * topk * n_ * k_ / (row[1]["time_us"] * 1e-6) / 1e12
+                put(row)
                 del at, bt, dW
         if want("a13"):
             qe = u8(Ex, 2 * F, Hd).random_(0, 120)
