@@ -93,6 +93,7 @@ def lib():
                                                            vp, vp, i64, vp, vp, vp]),
                 "orc_grouped_wgrad_points": (ctypes.c_int, [ctypes.c_int, vp, i64, i64, i64, vp, ctypes.c_int,
                                                             vp, vp, ctypes.c_int, vp, i64, vp, vp, vp, vp]),
+                "orc_adam_fp8_step": (ctypes.c_int, [i64, vp, vp, vp, vp, vp, vp] + [ctypes.c_float] * 9),
                 "orc_moe_route": (ctypes.c_int, [i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
                                                  vp, vp, vp, vp, vp, i64, vp, vp, vp, vp]),
                 "orc_moe_gather": (None, [vp, vp, i64, i64, vp, i64, i64, vp, vp]),
@@ -384,3 +385,27 @@ def swiglu_bwd(gu_bits, dh_bits):
     dgu = np.empty((R, F2), np.uint16)
     lib().orc_swiglu_bwd(_ptr(gu), _ptr(dh), R, F2 // 2, _ptr(dgu))
     return dgu
+
+
+# ---------------------------------------------------------------------------
+# FP8 optimizer states
+# ---------------------------------------------------------------------------
+
+def adam_hyper(lr, beta1, beta2, eps, wd, step):
+    """The binary32 constants of one AdamW step (bias corrections from the step number)."""
+    f = np.float32
+    return dict(lr=f(lr), b1=f(beta1), b2=f(beta2), omb1=f(1.0 - beta1), omb2=f(1.0 - beta2), eps=f(eps), wd=f(wd),
+                bc1=f(1.0 - beta1 ** step), bc2=f(1.0 - beta2 ** step))
+
+
+def adam_fp8_step(p, g_bits, qm, sm, qv, sv, h):
+    """One AdamW step with FP8 moments (in place on copies): returns (p, qm, sm, qv, sv)."""
+    p = np.array(p, np.float32, copy=True)
+    qm, qv = np.array(qm, np.uint8, copy=True), np.array(qv, np.uint8, copy=True)
+    sm, sv = np.array(sm, np.float32, copy=True), np.array(sv, np.float32, copy=True)
+    g = _c(g_bits, np.uint16)
+    st = lib().orc_adam_fp8_step(p.size, _ptr(p), _ptr(g), _ptr(qm), _ptr(sm), _ptr(qv), _ptr(sv), h["lr"], h["b1"],
+                                 h["b2"], h["omb1"], h["omb2"], h["eps"], h["wd"], h["bc1"], h["bc2"])
+    if st != OK:
+        raise ValueError(f"orc_adam_fp8_step status {st}")
+    return p, qm, sm, qv, sv

@@ -49,6 +49,10 @@
  *      expert index; pad every expert to a multiple of `align` with the
  *      lowest-index tokens not already routed to it, router prob 0; the rows
  *      of an expert are its tokens in ascending order.
+ *  R12 FP8 optimizer states: Adam's m in E4M3 and v in E5M2 (v holds squared
+ *      gradients, the widest-ranged quantity), one R2 scale per 128
+ *      consecutive parameters; the AdamW update in binary32 in a fixed order
+ *      (see orc_adam_fp8_step).
  */
 #include <math.h>
 #include <stdint.h>
@@ -671,6 +675,67 @@ int orc_grouped_wgrad_points(int G, const int32_t *off, int64_t N, int64_t K, in
         /* the group's slice: its chunks start at chunk r0/128 of the scale arrays */
         out[i] = gemm_point(rows, AT + n * ldt + r0, fmtA, sA + (r0 / 128) * N, ORC_GRAN_1x128, N, n,
                             BT + k * ldt + r0, fmtB, sB + (r0 / 128) * K, ORC_GRAN_1x128, K, k, decA, decB);
+    }
+    return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * AdamW step with the moments kept in FP8 ([Ling] "FP8 Optimizer": both Adam
+ * moments in FP8 with fine-grained compression / decompression; [FP8-LM]
+ * "Level 2: FP8 optimizer": momentum and variance in FP8) -- R12.
+ * m is E4M3 and v is E5M2, each with one binary32 scale per 128 consecutive
+ * parameters (R2's rule).  Every step below is one IEEE binary32 operation,
+ * in this order (Adam as published by Kingma and Ba, with the decoupled
+ * weight decay of Loshchilov and Hutter's AdamW):
+ *   m  = dec(qm) * sm                 v  = dec(qv) * sv
+ *   m  = b1 * m + omb1 * g            v  = b2 * v + omb2 * (g * g)
+ *   mh = m / bc1                      vh = v / bc2
+ *   u  = mh / (sqrt(vh) + eps)
+ *   p  = p - lr * (u + wd * p)
+ * then per 128-block s = amax / fmax (1 if amax = 0) and q = enc(x / s) for
+ * the new m and v.  omb1 = 1 - b1, omb2 = 1 - b2, bc1 = 1 - b1^t and
+ * bc2 = 1 - b2^t are given as binary32 numbers.
+ * ------------------------------------------------------------------------- */
+int orc_adam_fp8_step(int64_t n, float *p, const uint16_t *g, uint8_t *qm, float *sm, uint8_t *qv, float *sv,
+                      float lr, float b1, float b2, float omb1, float omb2, float eps, float wd, float bc1,
+                      float bc2)
+{
+    int64_t blk;
+    if (n % 128 != 0) return ORC_BADARG;
+#pragma omp parallel for schedule(static)
+    for (blk = 0; blk < n / 128; ++blk) {
+        float mn[128], vn[128], am = 0.0f, av = 0.0f, s_m, s_v;
+        int i;
+        for (i = 0; i < 128; ++i) {
+            const int64_t k = blk * 128 + i;
+            const float gi = orc_bf16_to_f32(g[k]);
+            float m = (float)orc_fp8_decode(qm[k], ORC_E4M3) * sm[blk];
+            float v = (float)orc_fp8_decode(qv[k], ORC_E5M2) * sv[blk];
+            float gg, mh, vh, den, u, t;
+            m = b1 * m + omb1 * gi;
+            gg = gi * gi;
+            v = b2 * v + omb2 * gg;
+            mh = m / bc1;
+            vh = v / bc2;
+            den = sqrtf(vh) + eps;
+            u = mh / den;
+            t = wd * p[k];
+            t = u + t;
+            t = lr * t;
+            p[k] = p[k] - t;
+            mn[i] = m;
+            vn[i] = v;
+            if (fabsf(m) > am) am = fabsf(m);
+            if (fabsf(v) > av) av = fabsf(v);
+        }
+        s_m = am == 0.0f ? 1.0f : am / 448.0f;
+        s_v = av == 0.0f ? 1.0f : av / 57344.0f;
+        for (i = 0; i < 128; ++i) {
+            qm[blk * 128 + i] = orc_fp8_encode(mn[i] / s_m, ORC_E4M3);
+            qv[blk * 128 + i] = orc_fp8_encode(vn[i] / s_v, ORC_E5M2);
+        }
+        sm[blk] = s_m;
+        sv[blk] = s_v;
     }
     return ORC_OK;
 }
