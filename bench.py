@@ -525,6 +525,20 @@ class RowBench:
             put(self.hbm("a13_expert_weights_transpose", lambda: fg.transpose_128x128_batched(qe, se, qeT, seT),
                          2 * Ex * 2 * F * Hd, f"{Ex} experts x {2 * F}x{Hd} FP8"))
             del qe, qeT
+        if want("a14"):
+            # AdamW with FP8 moments over the 117M parameters of W_gu: parameters read and
+            # written (FP32), BF16 gradient, E4M3 m and E5M2 v codes read and written,
+            # their block scales read and written
+            npar = 28672 * 4096
+            P = f32(npar).normal_(0, 0.02)
+            Gd = bf(npar).normal_(0, 1e-3)
+            Mq, Vq = u8(npar).zero_(), u8(npar).zero_()
+            Ms, Vs = f32(npar // 128).fill_(1.0), f32(npar // 128).fill_(1.0)
+            hp = fg.adamw_hparams(1e-3, 0.9, 0.95, 1e-8, 0.1, 1)
+            fg.adamw_step_fp8_states(P, Gd, Mq, Ms, Vq, Vs, hp)          # non-trivial moment codes
+            put(self.hbm("a14_adamw_fp8_states", lambda: fg.adamw_step_fp8_states(P, Gd, Mq, Ms, Vq, Vs, hp),
+                         npar * (4 + 4 + 2 + 2 + 2) + (npar // 128) * 16, "117M parameters (W_gu)"))
+            del P, Gd, Mq, Vq
         if want("a11"):
             GU2 = bf(8192, 28672).normal_()
             H2, dH2, dGU2 = bf(8192, 14336), bf(8192, 14336).normal_(), bf(8192, 28672)

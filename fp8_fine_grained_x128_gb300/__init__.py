@@ -59,6 +59,11 @@ class DelayedRecipe(ctypes.Structure):
                 ("margin", ctypes.c_int32), ("algo", ctypes.c_int32)]
 
 
+class AdamWHparams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_float) for n in ("lr", "beta1", "beta2", "one_minus_beta1", "one_minus_beta2", "eps",
+                                              "weight_decay", "bias_correction1", "bias_correction2")]
+
+
 _I64, _I32, _VP, _INT = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int
 _SIGS = {
     "fp8_abi_version": (_INT, []),
@@ -81,6 +86,7 @@ _SIGS = {
                                 _VP]),
     "fp8_grouped_gemm_wgrad": (_INT, [_INT, _VP, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _INT, _VP, _VP, _INT,
                                       _I64, _VP]),
+    "fp8_adamw_step_fp8_states": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, ctypes.POINTER(AdamWHparams), _VP]),
     "fp8_moe_route_pad": (_INT, [_VP, _I64, _INT, _INT, _INT, _I64, _VP, _VP, _VP, _VP, _VP, _VP,
                                  _VP, _VP]),
     "fp8_moe_gather": (_INT, [_VP, _VP, _I64, _I64, _VP, _VP, _INT, _I64, _VP, _VP, _VP]),
@@ -243,6 +249,22 @@ def grouped_gemm_wgrad(offsets, AT, fmtA, sAT, BT, fmtB, sBT, D, stream=None):
     _check("fp8_grouped_gemm_wgrad",
            lib().fp8_grouped_gemm_wgrad(G, _p(offsets), Mcap, N, K, _p(AT), fmtA, _p(sAT), _p(BT), fmtB, _p(sBT),
                                         _p(D), out, D.stride(0), _stream(stream)))
+
+
+# ------------------------------------------------------------------ FP8 optimizer states
+
+def adamw_hparams(lr, beta1, beta2, eps, weight_decay, step) -> AdamWHparams:
+    """The binary32 hyper-parameters of AdamW step ``step`` (>= 1)."""
+    return AdamWHparams(lr, beta1, beta2, 1.0 - beta1, 1.0 - beta2, eps, weight_decay, 1.0 - beta1 ** step,
+                        1.0 - beta2 ** step)
+
+
+def adamw_step_fp8_states(param, grad, m, m_scales, v, v_scales, hparams: AdamWHparams, stream=None):
+    """In place: FP32 ``param`` [n], BF16 ``grad`` [n], E4M3 ``m`` / E5M2 ``v`` codes [n] with
+    scales [n/128]."""
+    _check("fp8_adamw_step_fp8_states",
+           lib().fp8_adamw_step_fp8_states(_p(param), _p(grad), _p(m), _p(m_scales), _p(v), _p(v_scales),
+                                           param.numel(), ctypes.byref(hparams), _stream(stream)))
 
 
 # ------------------------------------------------------------------ MoE glue

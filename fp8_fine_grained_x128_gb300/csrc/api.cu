@@ -279,6 +279,17 @@ FP8FG_API int fp8_grouped_gemm_wgrad(int G, const int32_t *group_offsets, int64_
                                 st, S(stream));
 }
 
+FP8FG_API int fp8_adamw_step_fp8_states(float *param, const void *grad, uint8_t *m, float *m_scales, uint8_t *v,
+                                        float *v_scales, int64_t n, const fp8_adamw_hparams_t *hparams, void *stream)
+{
+    if (!hparams) return FP8_ERR_INVALID_ARG;
+    if (n < 0 || n % 128 != 0) return FP8_ERR_SHAPE;
+    if (n == 0) return FP8_OK;
+    if (!param || !grad || !m || !m_scales || !v || !v_scales) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(param) || !aligned16(grad) || !aligned16(m) || !aligned16(v)) return FP8_ERR_ALIGNMENT;
+    return launch_adamw_fp8(param, grad, m, m_scales, v, v_scales, n, *hparams, S(stream));
+}
+
 FP8FG_API int fp8_moe_route_pad(const float *logits, int64_t T, int E, int topk, int align, int64_t M_capacity,
                                 int32_t *topk_idx, float *topk_prob, int32_t *counts, int32_t *group_offsets,
                                 int32_t *row_token, float *row_prob, uint8_t *row_is_pad, void *stream)

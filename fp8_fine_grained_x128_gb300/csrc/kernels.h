@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/fp8fg.h"
+
 namespace fp8fg {
 
 // Number of SMs of the current device (cached per device).
@@ -41,6 +43,10 @@ int launch_grouped_gemm(int G, const int32_t *offsets, int64_t Mcap, int64_t N, 
 int launch_grouped_wgrad(int G, const int32_t *offsets, int64_t Mcap, int64_t N, int64_t K, const void *AT, int fmtA,
                          const float *sAT, const void *BT, int fmtB, const float *sBT, void *D, int out_dtype,
                          int64_t ldD, int *status, cudaStream_t st);
+
+// optim.cu
+int launch_adamw_fp8(float *p, const void *g, uint8_t *qm, float *sm, uint8_t *qv, float *sv, int64_t n,
+                     const fp8_adamw_hparams_t &h, cudaStream_t st);
 
 // moe.cu
 int launch_moe_route_pad(const float *logits, int64_t T, int E, int topk, int align, int64_t Mcap,

@@ -274,6 +274,33 @@ FP8FG_API int fp8_grouped_gemm_wgrad(int G, const int32_t *group_offsets, int64_
                                      const void *BT, int fmtB, const float *sBT, void *D,
                                      int out_dtype, int64_t ldD, void *stream);
 
+/* ------------------------------------------------------ FP8 optimizer states */
+
+/* Hyper-parameters of one AdamW step, as binary32 numbers; the bias
+ * corrections are the caller's roundings of 1 - beta^t for step t >= 1. */
+typedef struct {
+    float lr, beta1, beta2, one_minus_beta1, one_minus_beta2, eps, weight_decay;
+    float bias_correction1, bias_correction2;
+} fp8_adamw_hparams_t;
+
+/* One AdamW step with the moments kept in FP8 ([Ling] "FP8 Optimizer": both
+ * Adam moments in FP8 with fine-grained compression / decompression; [FP8-LM]
+ * "Level 2: FP8 optimizer").  m: E4M3 codes [n] with scales m_scales[n/128],
+ * v: E5M2 codes [n] with scales v_scales[n/128] (one scale per 128 consecutive
+ * parameters, s = amax / fmax, 1 for an all-zero block; start from zero codes
+ * and unit scales).  With g the BF16 gradient, every operation a correctly
+ * rounded binary32 one in this order:
+ *   m = dec(m) * sm;  m = beta1 * m + one_minus_beta1 * g
+ *   v = dec(v) * sv;  v = beta2 * v + one_minus_beta2 * (g * g)
+ *   u = (m / bias_correction1) / (sqrt(v / bias_correction2) + eps)
+ *   param = param - lr * (u + weight_decay * param)
+ * and m, v are re-quantized with their blocks' new scales -- all in place, one
+ * pass.  param: FP32 master weights [n].  n % 128 == 0; param, grad, m, v
+ * 16-byte aligned. */
+FP8FG_API int fp8_adamw_step_fp8_states(float *param, const void *grad, uint8_t *m, float *m_scales,
+                                        uint8_t *v, float *v_scales, int64_t n,
+                                        const fp8_adamw_hparams_t *hparams, void *stream);
+
 /* -------------------------------------------------------------- MoE glue */
 
 /* Router + padded routing map ([Ling] "FP8 padding routing map").

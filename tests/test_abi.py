@@ -91,6 +91,11 @@ def test_host_validation_without_launch(lib):
     assert lib.fp8_transpose_128x128_batched(good, good, 2, 128, 64, good, good, S) == fg.ERR_SHAPE
     assert lib.fp8_transpose_128x128_batched(good, good, -1, 128, 128, good, good, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_transpose_128x128_batched(good, good, 0, 128, 128, good, good, S) == fg.OK
+    hp = fg.adamw_hparams(1e-3, 0.9, 0.95, 1e-8, 0.1, 1)
+    assert lib.fp8_adamw_step_fp8_states(good, good, good, good, good, good, 100, ctypes.byref(hp), S) == fg.ERR_SHAPE
+    assert lib.fp8_adamw_step_fp8_states(good, good, good, good, good, good, 128, None, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_adamw_step_fp8_states(odd, good, good, good, good, good, 128, ctypes.byref(hp), S) == fg.ERR_ALIGNMENT
+    assert lib.fp8_adamw_step_fp8_states(None, None, None, None, None, None, 0, ctypes.byref(hp), S) == fg.OK
     assert lib.fp8_moe_route_pad(good, 16, 300, 8, 128, 1024, good, good, good, good, good, good, None, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_moe_route_pad(good, 16, 8, 9, 128, 1024, good, good, good, good, good, good, None, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_swiglu_fwd(good, 4, 12, good, S) == fg.ERR_SHAPE
