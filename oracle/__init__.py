@@ -93,6 +93,7 @@ def lib():
                                                            vp, vp, i64, vp, vp, vp]),
                 "orc_grouped_wgrad_points": (ctypes.c_int, [ctypes.c_int, vp, i64, i64, i64, vp, ctypes.c_int,
                                                             vp, vp, ctypes.c_int, vp, i64, vp, vp, vp, vp]),
+                "orc_quant_pertensor_current": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp]),
                 "orc_adam_fp8_step": (ctypes.c_int, [i64, vp, vp, vp, vp, vp, vp] + [ctypes.c_float] * 9),
                 "orc_moe_route": (ctypes.c_int, [i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
                                                  vp, vp, vp, vp, vp, i64, vp, vp, vp, vp]),
@@ -409,3 +410,13 @@ def adam_fp8_step(p, g_bits, qm, sm, qv, sv, h):
     if st != OK:
         raise ValueError(f"orc_adam_fp8_step status {st}")
     return p, qm, sm, qv, sv
+
+
+def quant_pertensor_current(x_bits, fmt=E4M3):
+    """Per-tensor current scaling (the whole tensor one group): returns (q, scale, status)."""
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8)
+    s = np.zeros(1, np.float32)
+    st = lib().orc_quant_pertensor_current(_ptr(x), R, C, C, fmt, _ptr(s), _ptr(q))
+    return q, s[0], st

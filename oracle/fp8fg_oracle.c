@@ -506,6 +506,38 @@ int orc_quant_stats(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx,
 }
 
 /* ---------------------------------------------------------------------------
+ * Per-tensor current scaling ([FP8-RL] "KV cache compression": the scaling
+ * factor of the FP8 KV cache is recomputed from the current tensor after every
+ * model update, "inference-side calibration").  One group, the whole tensor:
+ * s = fp32(amax / fmax) (1 if amax = 0), q = enc(fp32(x) / s).  A tensor that
+ * holds Inf/NaN is reported (its outputs unspecified).
+ * ------------------------------------------------------------------------- */
+int orc_quant_pertensor_current(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                                float *scale, uint8_t *q)
+{
+    float amax = 0.0f, sc;
+    int64_t r;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(max : amax) reduction(| : bad)
+    for (r = 0; r < rows; ++r) {
+        int64_t c;
+        for (c = 0; c < cols; ++c) {
+            const float v = orc_bf16_to_f32(x[r * ldx + c]);
+            if (!isfinite(v)) bad = 1;
+            else if (fabsf(v) > amax) amax = fabsf(v);
+        }
+    }
+    sc = scale_of(amax, fmt);
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; ++r) {
+        int64_t c;
+        for (c = 0; c < cols; ++c) q[r * cols + c] = quant_one(orc_bf16_to_f32(x[r * ldx + c]), sc, fmt);
+    }
+    *scale = sc;
+    return bad ? ORC_NONFINITE : ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------
  * Per-tensor delayed scaling ([Infra] "Transformer Engine", "Scaling
  * strategies: delayed scaling") -- one step of the state machine (R5).
  * ------------------------------------------------------------------------- */

@@ -238,3 +238,25 @@ def test_stats_match_numpy_recount_all_granularities(fmt):
     assert code == oracle.OK and used == np.float32(0.01)
     assert list(map(int, stats)) == numpy_counts(x.reshape(1, -1), qt.reshape(1, -1),
                                                  np.float32([used]), fm)
+
+
+def test_pertensor_current_reduces_to_the_tile_and_block_quantizers():
+    """Per-tensor current scaling of a tensor that is one 1x128 tile (or one 128x128
+    block) is that tile's (block's) quantization; scaling x by 2 doubles s and keeps
+    the codes; an all-zero tensor gets s = 1 and zero codes."""
+    for fmt in (oracle.E4M3, oracle.E5M2):
+        t = synth.bf16_normal((1, 128), 51, 1.0, 0.01, 30.0)
+        q, s, st = oracle.quant_pertensor_current(t, fmt)
+        q1, s1, _ = oracle.quant_1x128(t, fmt)
+        assert st == oracle.OK and np.array_equal(q, q1) and np.float32(s) == s1.ravel()[0]
+        b = synth.bf16_normal((128, 128), 52, 1.0, 0.01, 30.0)
+        q, s, _ = oracle.quant_pertensor_current(b, fmt)
+        q2, s2, _ = oracle.quant_128x128(b, fmt)
+        assert np.array_equal(q, q2) and np.float32(s) == s2.ravel()[0]
+        x = synth.bf16_normal((300, 256), 53, 1e-2, 0.001, 100.0)
+        x2 = (x.astype(np.uint32) + (1 << 7)).astype(np.uint16)        # exponent + 1: x * 2 (no overflow here)
+        qa, sa, _ = oracle.quant_pertensor_current(x, fmt)
+        qb, sb, _ = oracle.quant_pertensor_current(x2, fmt)
+        assert np.array_equal(qa, qb) and np.float32(sb) == np.float32(2 * sa)
+        qz, sz, _ = oracle.quant_pertensor_current(np.zeros((3, 128), np.uint16), fmt)
+        assert sz == 1.0 and not qz.any()
