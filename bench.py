@@ -539,6 +539,14 @@ class RowBench:
             put(self.hbm("a14_adamw_fp8_states", lambda: fg.adamw_step_fp8_states(P, Gd, Mq, Ms, Vq, Vs, hp),
                          npar * (4 + 4 + 2 + 2 + 2) + (npar // 128) * 16, "117M parameters (W_gu)"))
             del P, Gd, Mq, Vq
+        if want("a15"):
+            # FP8 KV-cache calibration of one layer's K cache: 32768 tokens x 8 heads x 128, E4M3;
+            # algorithmic bytes = x read once + codes written (the second pass re-reads x, from L2)
+            KV = bf(32768, 1024).normal_(0, 1.0)
+            qkv, skv, wkv = u8(32768, 1024), f32(1), fg.new_workspace(dev)
+            put(self.hbm("a15_kv_cache_current_scaling", lambda: fg.quant_pertensor_current(KV, E, skv, qkv, wkv),
+                         3 * 32768 * 1024, "K cache 32768 tokens x 1024 (two passes, the second from L2)"))
+            del KV, qkv
         if want("a11"):
             GU2 = bf(8192, 28672).normal_()
             H2, dH2, dGU2 = bf(8192, 14336), bf(8192, 14336).normal_(), bf(8192, 28672)

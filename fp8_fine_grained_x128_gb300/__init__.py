@@ -79,6 +79,7 @@ _SIGS = {
                                            _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "fp8_quant_pertensor_delayed_noalloc": (_INT, [_VP, _I64, _I64, _I64, ctypes.POINTER(DelayedRecipe),
                                                    _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "fp8_quant_pertensor_current": (_INT, [_VP, _I64, _I64, _I64, _INT, _VP, _VP, _VP, _VP]),
     "fp8_quant_stats": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _INT, _INT, _VP, _VP, _VP]),
     "fp8_blockscaled_gemm": (_INT, [_I64, _I64, _I64, _VP, _INT, _VP, _INT, _VP, _INT, _VP, _INT,
                                     _VP, _INT, _I64, _VP]),
@@ -212,6 +213,14 @@ def quant_pertensor_delayed_noalloc(x, recipe: DelayedRecipe, hist, step, scale,
     _check("fp8_quant_pertensor_delayed_noalloc",
            lib().fp8_quant_pertensor_delayed_noalloc(_p(x), R, C, ld, ctypes.byref(recipe), _p(hist), _p(step),
                                                      _p(scale), _p(q), _p(qT), _p(stats), _stream(stream)))
+
+
+def quant_pertensor_current(x, fmt, scale, q, workspace, stream=None):
+    """Per-tensor current scaling: scale (device float[1]) = amax / fmax of x, q = codes."""
+    R, C, ld = _rows_cols(x)
+    _check("fp8_quant_pertensor_current",
+           lib().fp8_quant_pertensor_current(_p(x), R, C, ld, fmt, _p(scale), _p(q), _p(workspace),
+                                             _stream(stream)))
 
 
 def quant_stats(x, q, s, gran, fmt, stats, workspace=None, stream=None):

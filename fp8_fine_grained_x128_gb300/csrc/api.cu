@@ -190,6 +190,19 @@ FP8FG_API int fp8_quant_pertensor_delayed(const void *x, int64_t rows, int64_t c
                                     recipe->algo, amax_history, step, scale, q, qT, stats, workspace, st, S(stream));
 }
 
+FP8FG_API int fp8_quant_pertensor_current(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                                          float *scale, void *q, void *workspace, void *stream)
+{
+    if (!fmt_ok(fmt)) return FP8_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || cols % 8 != 0 || ldx < cols) return FP8_ERR_SHAPE;
+    if (!scale || !workspace) return FP8_ERR_INVALID_ARG;
+    if (rows > 0 && cols > 0 && (!x || !q)) return FP8_ERR_INVALID_ARG;
+    if ((x && !aligned16(x)) || (q && (reinterpret_cast<uintptr_t>(q) & 7u)) || ldx % 8 != 0 || !aligned16(workspace))
+        return FP8_ERR_ALIGNMENT;
+    FP8FG_STATUS_OR_RETURN(st);
+    return launch_pertensor_current(x, rows, cols, ldx, fmt, scale, q, workspace, st, S(stream));
+}
+
 FP8FG_API int fp8_quant_stats(const void *x, int64_t rows, int64_t cols, int64_t ldx, const void *q, const float *s,
                               int gran, int fmt, fp8_stats_t *stats, void *workspace, void *stream)
 {

@@ -31,6 +31,8 @@ int launch_pertensor_delayed(const void *x, int64_t rows, int64_t cols, int64_t 
                              void *stats, void *ws, int *status, cudaStream_t st);
 int launch_quant_stats(const void *x, int64_t rows, int64_t cols, int64_t ldx, const void *q, const float *s,
                        int gran, int fmt, void *stats, void *ws, int *status, cudaStream_t st);
+int launch_pertensor_current(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, float *scale, void *q,
+                             void *ws, int *status, cudaStream_t st);
 int launch_selftest_wait(int timeout_ms, int *status, cudaStream_t st);
 
 // gemm.cu

@@ -600,6 +600,82 @@ __global__ void __launch_bounds__(256) k_stats_blocks(const uint16_t *__restrict
 }
 
 // ---------------------------------------------------------------------------
+// Per-tensor current scaling (FP8-RL article, "KV cache compression": the
+// scaling factor of the FP8 KV cache is recomputed from the current tensor
+// after every model update).  Pass 1 reduces the tensor's amax and its last
+// CTA writes s = amax / fmax to the device (no host round trip); pass 2
+// quantizes with that s.
+// ---------------------------------------------------------------------------
+template <int FMT>
+__global__ void __launch_bounds__(256) k_amax_scale(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
+                                                    int64_t ldx, float *scale, PtWorkspace *ws, int *status)
+{
+    __shared__ uint32_t red[32];
+    __shared__ int is_last;
+    const int64_t vpr = cols / 8, nvec = rows * vpr;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    uint32_t m = 0;
+    if (ldx == cols) {   // contiguous: flat 16-byte vectors, eight loads in flight
+        constexpr int U = 8;
+        int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+        for (; i + (U - 1) * stride < nvec; i += U * stride) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) v[u] = ldg_stream(x + (i + u * stride) * 8);
+#pragma unroll
+            for (int u = 0; u < U; ++u) m = max(m, absmax8(v[u]));
+        }
+        for (; i < nvec; i += stride) m = max(m, absmax8(ldg_stream(x + i * 8)));
+    } else {
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+            const int64_t r = i / vpr, c = (i - r * vpr) * 8;
+            m = max(m, absmax8(ldg_stream(x + r * ldx + c)));
+        }
+    }
+    const uint32_t a = block_reduce_max(m, red);
+    if (threadIdx.x == 0) atomicMax(&ws->amax_bits, a);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(&ws->ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (is_last && threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t am = __ldcg(&ws->amax_bits);
+        if (am >= 0x7F80u) set_status(status, FP8_ERR_NONFINITE);
+        *scale = scale_from_amax_bits(am, FMT);
+        ws->amax_bits = 0;
+        ws->ticket = 0;
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(256) k_quant_scale(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
+                                                     int64_t ldx, const float *scale, uint8_t *__restrict__ q)
+{
+    const Divider2 d(*scale);
+    const int64_t vpr = cols / 8, nvec = rows * vpr;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    if (ldx == cols) {   // contiguous: flat 16-byte vectors, four loads in flight
+        constexpr int U = 4;
+        int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+        for (; i + (U - 1) * stride < nvec; i += U * stride) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) v[u] = ldg_stream(x + (i + u * stride) * 8);
+#pragma unroll
+            for (int u = 0; u < U; ++u) *reinterpret_cast<uint2 *>(q + (i + u * stride) * 8) = quant8p<FMT>(v[u], d);
+        }
+        for (; i < nvec; i += stride)
+            *reinterpret_cast<uint2 *>(q + i * 8) = quant8p<FMT>(ldg_stream(x + i * 8), d);
+    } else {
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+            const int64_t r = i / vpr, c = (i - r * vpr) * 8;
+            *reinterpret_cast<uint2 *>(q + r * cols + c) = quant8p<FMT>(ldg_stream(x + r * ldx + c), d);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Bounded-wait self-test: one thread waits on a barrier nothing arrives at.
 // ---------------------------------------------------------------------------
 __global__ void k_selftest_wait(uint64_t timeout_ns, int *status)
@@ -688,6 +764,25 @@ int launch_quant_stats(const void *x, int64_t rows, int64_t cols, int64_t ldx, c
     } else {
         if (gran == FP8_GRAN_TENSOR) k_stats_blocks<FP8_E4M3, true><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S, W);
         else k_stats_blocks<FP8_E4M3, false><<<b, 256, 0, st>>>(X, rows, cols, ldx, Q, s, S, W);
+    }
+    return check_launch();
+}
+
+int launch_pertensor_current(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, float *scale, void *q,
+                             void *ws, int *status, cudaStream_t st)
+{
+    const int64_t nvec = rows * (cols / 8);
+    const unsigned ba = (unsigned)std::max<int64_t>(1, std::min<int64_t>((nvec + 255) / 256, (int64_t)sm_count() * 4));
+    const unsigned bq = (unsigned)std::max<int64_t>(1, std::min<int64_t>((nvec + 255) / 256, (int64_t)sm_count() * 8));
+    auto X = static_cast<const uint16_t *>(x);
+    auto W = static_cast<PtWorkspace *>(ws);
+    auto Q = static_cast<uint8_t *>(q);
+    if (fmt == FP8_E5M2) {
+        k_amax_scale<FP8_E5M2><<<ba, 256, 0, st>>>(X, rows, cols, ldx, scale, W, status);
+        if (nvec > 0) k_quant_scale<FP8_E5M2><<<bq, 256, 0, st>>>(X, rows, cols, ldx, scale, Q);
+    } else {
+        k_amax_scale<FP8_E4M3><<<ba, 256, 0, st>>>(X, rows, cols, ldx, scale, W, status);
+        if (nvec > 0) k_quant_scale<FP8_E4M3><<<bq, 256, 0, st>>>(X, rows, cols, ldx, scale, Q);
     }
     return check_launch();
 }

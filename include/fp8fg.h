@@ -190,6 +190,19 @@ FP8FG_API int fp8_quant_pertensor_delayed(const void *x, int64_t rows, int64_t c
                                           int32_t *step, float *scale, void *q, void *qT,
                                           fp8_stats_t *stats, void *workspace, void *stream);
 
+/* Per-tensor current scaling ([FP8-RL] "KV cache compression": after every
+ * model update the FP8 KV cache's scaling factor is recomputed from the
+ * current tensor, "inference-side calibration").  One group, the whole
+ * tensor: *scale = s = fp32(amax / fmax) (1 if amax = 0), written on the
+ * device, and q = RNE_satfinite(x / s).  x: BF16 [rows][ldx], cols % 8 == 0,
+ * x 16-byte and q 8-byte aligned.  q: [rows][cols].  scale: DEVICE float.
+ * workspace: fp8_pertensor_workspace_bytes() bytes, zeroed once and left
+ * zeroed (calls sharing one workspace must not overlap on the GPU).  A tensor
+ * holding Inf/NaN records FP8_ERR_NONFINITE (outputs unspecified). */
+FP8FG_API int fp8_quant_pertensor_current(const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                                          int fmt, float *scale, void *q, void *workspace,
+                                          void *stream);
+
 /* The same delayed-scaling step for callers that cannot allocate device
  * memory -- for example code that runs inside another framework's fixed
  * memory plan or arena, or a plugin that is handed buffers but no allocator.
