@@ -94,6 +94,7 @@ def lib():
                 "orc_grouped_wgrad_points": (ctypes.c_int, [ctypes.c_int, vp, i64, i64, i64, vp, ctypes.c_int,
                                                             vp, vp, ctypes.c_int, vp, i64, vp, vp, vp, vp]),
                 "orc_quant_pertensor_current": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp]),
+                "orc_wgrad_recompute_error": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, i64, vp]),
                 "orc_adam_fp8_step": (ctypes.c_int, [i64, vp, vp, vp, vp, vp, vp] + [ctypes.c_float] * 9),
                 "orc_moe_route": (ctypes.c_int, [i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
                                                  vp, vp, vp, vp, vp, i64, vp, vp, vp, vp]),
@@ -420,3 +421,15 @@ def quant_pertensor_current(x_bits, fmt=E4M3):
     s = np.zeros(1, np.float32)
     st = lib().orc_quant_pertensor_current(_ptr(x), R, C, C, fmt, _ptr(s), _ptr(q))
     return q, s[0], st
+
+
+def wgrad_recompute_error(dY_bits, X_bits, D):
+    """High-precision dw recompute monitor: {sum (D-R)^2, sum R^2, max|D-R|, max|R|} with
+    R = dY^T . X of the BF16 operands (exact products, FP64 sums)."""
+    dY, X = _c(dY_bits, np.uint16), _c(X_bits, np.uint16)
+    D = _c(D, np.float32)
+    M, N = dY.shape
+    K = X.shape[1]
+    out = np.zeros(4, np.float64)
+    lib().orc_wgrad_recompute_error(M, N, K, _ptr(dY), _ptr(X), _ptr(D), D.shape[1], _ptr(out))
+    return out

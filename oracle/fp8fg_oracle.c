@@ -712,6 +712,41 @@ int orc_grouped_wgrad_points(int G, const int32_t *off, int64_t N, int64_t K, in
 }
 
 /* ---------------------------------------------------------------------------
+ * High-precision dw recompute monitor ([Ling] "Where does the error come
+ * from?": tensors flagged by the underflow / distortion monitors get their dw
+ * recomputed in high precision and compared).  The reference is
+ *   R[n][k] = sum_m dY[m][n] * X[m][k]
+ * over the BF16 operands (token-major dY [M][N], X [M][K]), exact products
+ * summed in FP64; against the FP8 wgrad D [N][ldD] the monitor reports
+ *   out = { sum (D - R)^2, sum R^2, max |D - R|, max |R| }  (FP64).
+ * ------------------------------------------------------------------------- */
+int orc_wgrad_recompute_error(int64_t M, int64_t N, int64_t K, const uint16_t *dY, const uint16_t *X,
+                              const float *D, int64_t ldD, double *out)
+{
+    double sdd = 0.0, srr = 0.0, mdd = 0.0, mrr = 0.0;
+    int64_t n;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : sdd, srr) reduction(max : mdd, mrr)
+    for (n = 0; n < N; ++n) {
+        int64_t k, m;
+        for (k = 0; k < K; ++k) {
+            double r = 0.0, d;
+            for (m = 0; m < M; ++m)
+                r += (double)orc_bf16_to_f32(dY[m * N + n]) * (double)orc_bf16_to_f32(X[m * K + k]);
+            d = (double)D[n * ldD + k] - r;
+            sdd += d * d;
+            srr += r * r;
+            if (fabs(d) > mdd) mdd = fabs(d);
+            if (fabs(r) > mrr) mrr = fabs(r);
+        }
+    }
+    out[0] = sdd;
+    out[1] = srr;
+    out[2] = mdd;
+    out[3] = mrr;
+    return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------
  * AdamW step with the moments kept in FP8 ([Ling] "FP8 Optimizer": both Adam
  * moments in FP8 with fine-grained compression / decompression; [FP8-LM]
  * "Level 2: FP8 optimizer": momentum and variance in FP8) -- R12.

@@ -172,3 +172,26 @@ def test_grouped_wgrad_matches_dequantize_then_multiply():
     # reading the scales with the row index instead of the chunk index is caught
     wrong = oracle.grouped_wgrad_full(offs, AT, fa, np.ascontiguousarray(sA[::-1]), BT, fb, sB)
     assert not np.allclose(wrong[3], got[3])
+
+
+def test_wgrad_recompute_error_closed_forms():
+    """With small-integer BF16 operands R = dY^T X is an exact integer matrix: D = R gives
+    zero error; one entry off by delta gives delta^2 and delta; D = 0 gives sum (D-R)^2 =
+    sum R^2 and max |D-R| = max |R|; D = 2R gives the same."""
+    rng = np.random.default_rng(7)
+    M, N, K = 64, 24, 40
+    dyi = rng.integers(-8, 9, size=(M, N))
+    xi = rng.integers(-8, 9, size=(M, K))
+    to_bf16 = lambda a: (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)   # exact for small ints
+    dy, x = to_bf16(dyi), to_bf16(xi)
+    R = (dyi.T @ xi).astype(np.float64)                      # integer matmul
+    out = oracle.wgrad_recompute_error(dy, x, R.astype(np.float32))
+    assert out[0] == 0.0 and out[2] == 0.0
+    assert out[1] == float((R * R).sum()) and out[3] == float(np.abs(R).max())
+    D = R.astype(np.float32).copy()
+    D[3, 5] += 0.5
+    out = oracle.wgrad_recompute_error(dy, x, D)
+    assert out[0] == 0.25 and out[2] == 0.5
+    for D in (np.zeros_like(R, np.float32), (2 * R).astype(np.float32)):
+        out = oracle.wgrad_recompute_error(dy, x, D)
+        assert out[0] == out[1] and out[2] == out[3]
