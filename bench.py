@@ -547,6 +547,20 @@ class RowBench:
             put(self.hbm("a15_kv_cache_current_scaling", lambda: fg.quant_pertensor_current(KV, E, skv, qkv, wkv),
                          3 * 32768 * 1024, "K cache 32768 tokens x 1024 (two passes, the second from L2)"))
             del KV, qkv
+        if want("a16"):
+            # high-precision dw recompute of the down projection's wgrad (dW_down [4096, 14336]
+            # from dY [8192, 4096] and H [8192, 14336]): a cuBLAS BF16 GEMM plus this
+            # library's comparison kernel; reported against the measured bf16 peak
+            Md, Nd, Kd = 8192, 4096, 14336
+            dYm, Hm = bf(Md, Nd).normal_(0, 1e-3), bf(Md, Kd).normal_(0, 1.0)
+            Dm, Rm, em = f32(Nd, Kd).normal_(0, 1.0), f32(Nd, Kd), fg.new_wgrad_err(dev)
+            t = self.time(lambda: fg.wgrad_recompute_error(dYm, Hm, Dm, Rm, em))
+            tf = 2.0 * Md * Nd * Kd / t / 1e12
+            out["a16_dw_recompute_monitor"] = {"time_us": t * 1e6, "achieved": tf, "unit": "TFLOP/s",
+                                               "peak": self.pk["bf16"], "frac": tf / self.pk["bf16"],
+                                               "bound": "tensor (bf16, cuBLAS) + HBM (comparison)",
+                                               "note": "dW_down 4096x14336 over 8192 tokens"}
+            del dYm, Hm, Dm, Rm
         if want("a11"):
             GU2 = bf(8192, 28672).normal_()
             H2, dH2, dGU2 = bf(8192, 14336), bf(8192, 14336).normal_(), bf(8192, 28672)

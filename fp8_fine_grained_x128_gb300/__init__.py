@@ -87,6 +87,7 @@ _SIGS = {
                                 _VP]),
     "fp8_grouped_gemm_wgrad": (_INT, [_INT, _VP, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _INT, _VP, _VP, _INT,
                                       _I64, _VP]),
+    "fp8_wgrad_recompute_error": (_INT, [_I64, _I64, _I64, _VP, _VP, _VP, _I64, _VP, _VP, _VP]),
     "fp8_adamw_step_fp8_states": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, ctypes.POINTER(AdamWHparams), _VP]),
     "fp8_moe_route_pad": (_INT, [_VP, _I64, _INT, _INT, _INT, _I64, _VP, _VP, _VP, _VP, _VP, _VP,
                                  _VP, _VP]),
@@ -258,6 +259,30 @@ def grouped_gemm_wgrad(offsets, AT, fmtA, sAT, BT, fmtB, sBT, D, stream=None):
     _check("fp8_grouped_gemm_wgrad",
            lib().fp8_grouped_gemm_wgrad(G, _p(offsets), Mcap, N, K, _p(AT), fmtA, _p(sAT), _p(BT), fmtB, _p(sBT),
                                         _p(D), out, D.stride(0), _stream(stream)))
+
+
+# ------------------------------------------------------------------ high-precision dw monitor
+
+def wgrad_recompute_error(dY, X, D, ref_workspace, err, stream=None):
+    """err (device float64[3] view of fp8_wgrad_err_t: see new_wgrad_err) <- statistics of the FP8
+    wgrad D [N, K] against R = dY^T . X recomputed from the BF16 operands into ref_workspace."""
+    M, N = dY.shape
+    K = X.shape[1]
+    _check("fp8_wgrad_recompute_error",
+           lib().fp8_wgrad_recompute_error(M, N, K, _p(dY), _p(X), _p(D), D.stride(0), _p(ref_workspace), _p(err),
+                                           _stream(stream)))
+
+
+def new_wgrad_err(device="cuda") -> torch.Tensor:
+    """Storage for fp8_wgrad_err_t (24 bytes)."""
+    return torch.zeros(3, dtype=torch.float64, device=device)
+
+
+def wgrad_err_values(err: torch.Tensor):
+    """(sum_sq_diff, sum_sq_ref, max_abs_diff, max_abs_ref) from new_wgrad_err storage."""
+    h = err.cpu()
+    f = h[2:3].view(torch.float32)
+    return float(h[0]), float(h[1]), float(f[0]), float(f[1])
 
 
 # ------------------------------------------------------------------ FP8 optimizer states

@@ -292,6 +292,22 @@ FP8FG_API int fp8_grouped_gemm_wgrad(int G, const int32_t *group_offsets, int64_
                                 st, S(stream));
 }
 
+FP8FG_API int fp8_wgrad_recompute_error(int64_t M, int64_t N, int64_t K, const void *dY, const void *X, const float *D,
+                                        int64_t ldD, float *ref_workspace, fp8_wgrad_err_t *err, void *stream)
+{
+    if (M < 0 || N < 0 || K < 0 || M >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31))
+        return FP8_ERR_SHAPE;
+    if (!err) return FP8_ERR_INVALID_ARG;
+    if (N > 0 && K > 0) {
+        if (ldD < K) return FP8_ERR_SHAPE;
+        if (!D || !ref_workspace || (M > 0 && (!dY || !X))) return FP8_ERR_INVALID_ARG;
+        if ((M > 0 && (!aligned16(dY) || !aligned16(X))) || (reinterpret_cast<uintptr_t>(D) & 3u) ||
+            (reinterpret_cast<uintptr_t>(ref_workspace) & 3u) || (reinterpret_cast<uintptr_t>(err) & 7u))
+            return FP8_ERR_ALIGNMENT;
+    }
+    return launch_wgrad_recompute_error(M, N, K, dY, X, D, ldD, ref_workspace, err, S(stream));
+}
+
 FP8FG_API int fp8_adamw_step_fp8_states(float *param, const void *grad, uint8_t *m, float *m_scales, uint8_t *v,
                                         float *v_scales, int64_t n, const fp8_adamw_hparams_t *hparams, void *stream)
 {

@@ -287,6 +287,30 @@ FP8FG_API int fp8_grouped_gemm_wgrad(int G, const int32_t *group_offsets, int64_
                                      const void *BT, int fmtB, const float *sBT, void *D,
                                      int out_dtype, int64_t ldD, void *stream);
 
+/* ------------------------------------------------ high-precision dw monitor */
+
+/* Error statistics of an FP8 wgrad D against its high-precision recompute R. */
+typedef struct {
+    double sum_sq_diff;   /* sum (D - R)^2 */
+    double sum_sq_ref;    /* sum R^2 */
+    float max_abs_diff;   /* max |D - R| */
+    float max_abs_ref;    /* max |R| */
+} fp8_wgrad_err_t;
+
+/* High-precision dw recompute monitor ([Ling] "Where does the error come
+ * from?": tensors flagged by the underflow / distortion monitors get their dw
+ * recomputed in high precision and compared).  R = dY^T . X from the BF16
+ * operands, token-major dY [M][N] and X [M][K], FP32 accumulation (a plain
+ * BF16 GEMM, run by cuBLAS, which is loaded on the first call: without it
+ * the call returns FP8_ERR_UNSUPPORTED), written to ref_workspace [N][K]
+ * (caller-owned, N*K floats); then *err (DEVICE) = the statistics of D
+ * [N][ldD] (FP32, e.g. fp8_blockscaled_gemm's wgrad output) against R.
+ * The relative Frobenius error is sqrt(sum_sq_diff / sum_sq_ref).
+ * dY, X 16-byte aligned; M, N, K < 2^31. */
+FP8FG_API int fp8_wgrad_recompute_error(int64_t M, int64_t N, int64_t K, const void *dY, const void *X,
+                                        const float *D, int64_t ldD, float *ref_workspace,
+                                        fp8_wgrad_err_t *err, void *stream);
+
 /* ------------------------------------------------------ FP8 optimizer states */
 
 /* Hyper-parameters of one AdamW step, as binary32 numbers; the bias

@@ -95,6 +95,10 @@ def test_host_validation_without_launch(lib):
     assert lib.fp8_quant_pertensor_current(good, 4, 16, 16, 9, good, good, good, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_quant_pertensor_current(good, 4, 16, 16, 0, good, good, None, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_quant_pertensor_current(odd, 4, 16, 16, 0, good, good, good, S) == fg.ERR_ALIGNMENT
+    assert lib.fp8_wgrad_recompute_error(-1, 128, 128, good, good, good, 128, good, good, S) == fg.ERR_SHAPE
+    assert lib.fp8_wgrad_recompute_error(128, 128, 128, good, good, good, 100, good, good, S) == fg.ERR_SHAPE
+    assert lib.fp8_wgrad_recompute_error(128, 128, 128, good, good, good, 128, good, None, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_wgrad_recompute_error(128, 128, 128, odd, good, good, 128, good, good, S) == fg.ERR_ALIGNMENT
     hp = fg.adamw_hparams(1e-3, 0.9, 0.95, 1e-8, 0.1, 1)
     assert lib.fp8_adamw_step_fp8_states(good, good, good, good, good, good, 100, ctypes.byref(hp), S) == fg.ERR_SHAPE
     assert lib.fp8_adamw_step_fp8_states(good, good, good, good, good, good, 128, None, S) == fg.ERR_INVALID_ARG
