@@ -65,7 +65,7 @@ __device__ __noinline__ Quot8 quot8_ieee(uint4 v, float s)
 }
 
 template <int FMT, bool STATS>
-__device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &c, uint32_t *bmx)
+__device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &c, uint8_t *seen)
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float qv[8];
@@ -108,11 +108,12 @@ __device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &
                 for (int e = 0; e < 4; ++e) c.sat += fabsf(qv[4 * h + e]) > fm;
             }
         }
-        // presence of the raw BF16 patterns; +0 and -0 are merged in the count
+        // presence of the raw BF16 patterns, one byte each (a plain store, no
+        // read or branch); +0 and -0 are merged in the count
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            bitmap_set(bmx, w[j] & 0xFFFFu);
-            bitmap_set(bmx, w[j] >> 16);
+            seen[w[j] & 0xFFFFu] = 1;
+            seen[w[j] >> 16] = 1;
         }
     }
     return out;
@@ -245,11 +246,12 @@ __global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__res
     __shared__ uint32_t bmq[8];
     __shared__ uint32_t red[32];
     __shared__ int is_last;
+    extern __shared__ __align__(16) uint8_t seen[];   // STATS: one byte per BF16 pattern (64 KB)
 
     const int t = threadIdx.x;
     const int g = t & 15, rr = t >> 4;
     if (STATS) {
-        for (int i = t; i < 2048; i += 256) bmx[i] = 0;
+        for (int i = t; i < 65536 / 16; i += 256) reinterpret_cast<uint4 *>(seen)[i] = make_uint4(0, 0, 0, 0);
         if (t < 8) bmq[t] = 0;
     }
     const float s_t = *scale;   // chosen from the amax of earlier steps
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__res
             const int row = rr + 16 * i;
             if (r0 + row < rows) {
                 amax = max(amax, absmax8(v[i]));
-                const uint2 code = quant8_mon<FMT, STATS>(v[i], d, c, bmx);
+                const uint2 code = quant8_mon<FMT, STATS>(v[i], d, c, seen);
                 *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = code;
                 if (TRANS) {
                     ct[row * 33 + 2 * g] = code.x;
@@ -306,6 +308,19 @@ __global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__res
         }
     }
 
+    if (STATS) {
+        // presence bytes -> presence bits (bytes are 0 or 1)
+        __syncthreads();
+        for (int i = t; i < 2048; i += 256) {
+            const uint4 a = reinterpret_cast<const uint4 *>(seen)[2 * i], b = reinterpret_cast<const uint4 *>(seen)[2 * i + 1];
+            const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            uint32_t bits = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                bits |= ((wv[j] & 1u) | ((wv[j] >> 7) & 2u) | ((wv[j] >> 14) & 4u) | ((wv[j] >> 21) & 8u)) << (4 * j);
+            bmx[i] = bits;
+        }
+    }
     if (!merge_and_ticket<STATS>(c, amax, bmx, bmq, stats, ws, red, &is_last)) return;
 
     // ---- last CTA: state update (history slot, next scale, step) ----
@@ -703,7 +718,18 @@ static void delayed_launch(int blocks, cudaStream_t st, const void *x, int64_t r
                            int hist_len, int margin, int algo, float *hist, int32_t *step, float *scale, void *q,
                            void *qT, void *stats, void *ws, int *status)
 {
-    k_pertensor_delayed<FMT, TRANS, STATS><<<blocks, 256, 0, st>>>(
+    constexpr int kSeen = STATS ? 65536 : 0;
+    if (STATS) {
+        static bool attr_done[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (!attr_done[dev & 63]) {
+            cudaFuncSetAttribute(k_pertensor_delayed<FMT, TRANS, STATS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSeen);
+            attr_done[dev & 63] = true;
+        }
+    }
+    k_pertensor_delayed<FMT, TRANS, STATS><<<blocks, 256, kSeen, st>>>(
         static_cast<const uint16_t *>(x), rows, cols, ldx, hist_len, margin, algo, hist, step, scale,
         static_cast<uint8_t *>(q), static_cast<uint8_t *>(qT), static_cast<fp8_stats_t *>(stats),
         static_cast<PtWorkspace *>(ws), status);
@@ -714,7 +740,8 @@ int launch_pertensor_delayed(const void *x, int64_t rows, int64_t cols, int64_t 
                              void *stats, void *ws, int *status, cudaStream_t st)
 {
     const int64_t ntiles = ((rows + 127) / 128) * (cols / 128);
-    int64_t blocks = (int64_t)sm_count() * 4;
+    // with monitors a CTA holds 64 KB of presence bytes: two per SM
+    int64_t blocks = (int64_t)sm_count() * (stats ? 2 : 4);
     if (blocks > ntiles) blocks = ntiles;
     if (blocks < 1) blocks = 1;   // an empty tensor still runs the state update
     const int b = (int)blocks;
