@@ -116,6 +116,22 @@ def cpu_sample_time(budget_s: float, seed: int = 0):
     return t_step, cores, sample
 
 
+def slowest_rank_ms(ms: float, world: int, device) -> float:
+    """The job's time per step is its slowest rank's (max over ranks)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -622,13 +638,9 @@ def run_ours(args):
     barrier()
     clocks.mark("end")
     clk = clocks.stop()
-    ms = t_start.elapsed_time(t_end) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank_ms(t_start.elapsed_time(t_end) / args.steps, world, dev)
     flops = step_flops()
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_tflops(world, flops, ms)
 
     # dominant kernel: the block-scaled GEMM (all six shapes of the step)
     gemm_ms = 0.0
@@ -660,7 +672,7 @@ def run_ours(args):
 
     # end to end: host buffers, H2D of the step's inputs and D2H of its results
     e2e = step.e2e(args.steps)
-    e2e_val = world * flops / (e2e["ms"] * 1e-3) / 1e12
+    e2e_val = job_tflops(world, flops, slowest_rank_ms(e2e["ms"], world, dev))
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
