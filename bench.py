@@ -45,7 +45,7 @@ M_TOK, HID, FFN = 8192, 4096, 14336
 # six, from a one-pass ncu capture of the current kernel; the summary with
 # its command is profiles/k_gemm_step_dram_traffic.md).  Set to None when the
 # kernel changes until it is captured again.
-GEMM_TRAFFIC_BYTES = 727842731
+GEMM_TRAFFIC_BYTES = 730479445
 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
@@ -240,14 +240,14 @@ class MlpStep:
         self.qWgu, self.sWgu, self.qWguT, self.sWguT = u8(f2, h), f32(f2 // 128, h // 128), u8(h, f2), f32(h // 128, f2 // 128)
         self.qWd, self.sWd, self.qWdT, self.sWdT = u8(h, f), f32(h // 128, f // 128), u8(f, h), f32(f // 128, h // 128)
         self.qX, self.sX, self.qXT, self.sXT = u8(m, h), f32(h // 128, m), u8(h, m), f32(m // 128, h)
-        self.GU, self.H = bf(m, f2), bf(m, f)
+        self.GU = bf(m, f2)
         self.qH, self.sH, self.qHT, self.sHT = u8(m, f), f32(f // 128, m), u8(f, m), f32(m // 128, f)
         self.Y = bf(m, h)
         self.qdY, self.sdY, self.qdYT, self.sdYT = u8(m, h), f32(h // 128, m), u8(h, m), f32(m // 128, h)
-        self.dH, self.dGU = bf(m, f), bf(m, f2)
+        self.dH = bf(m, f)
         self.qdGU, self.sdGU, self.qdGUT, self.sdGUT = u8(m, f2), f32(f2 // 128, m), u8(f2, m), f32(m // 128, f2)
         self.dX, self.dWd, self.dWgu = bf(m, h), f32(h, f), f32(f2, h)
-        self.launches_per_step = 16
+        self.launches_per_step = 14
 
     def run(self, timed=False):
         import torch
@@ -272,15 +272,14 @@ class MlpStep:
         # fprop
         fg.quant_1x128(self.X, E, self.qX, self.sX, self.qXT, self.sXT)
         gemm("fprop_gate_up", self.qX, self.sX, B1, self.qWgu, self.sWgu, BB, self.GU)
-        fg.swiglu_fwd(self.GU, self.H)
-        fg.quant_1x128(self.H, E, self.qH, self.sH, self.qHT, self.sHT)
+        # H = SwiGLU(GU), quantized 1x128 and 128x1 as it is computed (H never stored)
+        fg.swiglu_quant_fwd(self.GU, E, self.qH, self.sH, self.qHT, self.sHT)
         gemm("fprop_down", self.qH, self.sH, B1, self.qWd, self.sWd, BB, self.Y)
         # dgrad (W^T on demand)
         fg.quant_1x128(self.dY, E, self.qdY, self.sdY, self.qdYT, self.sdYT)
         fg.transpose_128x128(self.qWd, self.sWd, self.qWdT, self.sWdT)
         gemm("dgrad_down", self.qdY, self.sdY, B1, self.qWdT, self.sWdT, BB, self.dH)
-        fg.swiglu_bwd(self.GU, self.dH, self.dGU)
-        fg.quant_1x128(self.dGU, E, self.qdGU, self.sdGU, self.qdGUT, self.sdGUT)
+        fg.swiglu_bwd_quant(self.GU, self.dH, E, self.qdGU, self.sdGU, self.qdGUT, self.sdGUT)
         fg.transpose_128x128(self.qWgu, self.sWgu, self.qWguT, self.sWguT)
         gemm("dgrad_gate_up", self.qdGU, self.sdGU, B1, self.qWguT, self.sWguT, BB, self.dX)
         # wgrad from the 128x1 (transposed) copies
@@ -583,6 +582,15 @@ class RowBench:
             nf = 8192 * 14336
             put(self.hbm("a11_swiglu_fwd", lambda: fg.swiglu_fwd(GU2, H2), 6 * nf, "GU 8192x28672 -> H"))
             put(self.hbm("a11_swiglu_bwd", lambda: fg.swiglu_bwd(GU2, dH2, dGU2), 10 * nf, "GU, dH -> dGU"))
+            # fused with the 1x128 + 128x1 quantizer: BF16 in; codes, transposed codes and
+            # both FP32 scale sets out (scale bytes = 2 x 4 bytes per 128 outputs)
+            qa, sa, qb, sb = u8(8192, 14336), f32(112, 8192), u8(14336, 8192), f32(64, 14336)
+            put(self.hbm("a11_swiglu_quant_fwd", lambda: fg.swiglu_quant_fwd(GU2, E, qa, sa, qb, sb),
+                         4 * nf + 2 * nf + nf // 16, "GU 8192x28672 -> H codes + H^T codes"))
+            qa, sa, qb, sb = u8(8192, 28672), f32(224, 8192), u8(28672, 8192), f32(64, 28672)
+            put(self.hbm("a11_swiglu_bwd_quant", lambda: fg.swiglu_bwd_quant(GU2, dH2, E, qa, sa, qb, sb),
+                         6 * nf + 4 * nf + nf // 8, "GU, dH -> dGU codes + dGU^T codes"))
+            del qa, sa, qb, sb
         st = fg.device_status()
         out["device_status"] = fg.status_string(st)
         return out

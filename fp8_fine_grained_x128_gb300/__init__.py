@@ -94,6 +94,8 @@ _SIGS = {
     "fp8_moe_gather": (_INT, [_VP, _VP, _I64, _I64, _VP, _VP, _INT, _I64, _VP, _VP, _VP]),
     "fp8_swiglu_fwd": (_INT, [_VP, _I64, _I64, _VP, _VP]),
     "fp8_swiglu_bwd": (_INT, [_VP, _VP, _I64, _I64, _VP, _VP]),
+    "fp8_swiglu_quant_fwd": (_INT, [_VP, _I64, _I64, _INT, _VP, _VP, _VP, _VP, _VP]),
+    "fp8_swiglu_bwd_quant": (_INT, [_VP, _VP, _I64, _I64, _INT, _VP, _VP, _VP, _VP, _VP]),
 }
 
 
@@ -326,3 +328,17 @@ def swiglu_fwd(gu, h, stream=None):
 def swiglu_bwd(gu, dh, dgu, stream=None):
     R, F2 = gu.shape
     _check("fp8_swiglu_bwd", lib().fp8_swiglu_bwd(_p(gu), _p(dh), R, F2 // 2, _p(dgu), _stream(stream)))
+
+
+def swiglu_quant_fwd(gu, fmt, q, s, qT, sT, stream=None):
+    """H = SwiGLU(gu) quantized 1x128 (q [R, F], s [F/128, R]) and 128x1 (qT [F, R], sT [R/128, F])."""
+    R, F2 = gu.shape
+    _check("fp8_swiglu_quant_fwd", lib().fp8_swiglu_quant_fwd(_p(gu), R, F2 // 2, fmt, _p(q), _p(s), _p(qT),
+                                                              _p(sT), _stream(stream)))
+
+
+def swiglu_bwd_quant(gu, dh, fmt, q, s, qT, sT, stream=None):
+    """dGU = SwiGLU'(gu) . dh quantized 1x128 (q [R, 2F], s [2F/128, R]) and 128x1 (qT [2F, R], sT [R/128, 2F])."""
+    R, F2 = gu.shape
+    _check("fp8_swiglu_bwd_quant", lib().fp8_swiglu_bwd_quant(_p(gu), _p(dh), R, F2 // 2, fmt, _p(q), _p(s),
+                                                              _p(qT), _p(sT), _stream(stream)))

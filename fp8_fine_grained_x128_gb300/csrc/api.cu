@@ -363,4 +363,37 @@ FP8FG_API int fp8_swiglu_bwd(const void *gu, const void *dh, int64_t rows, int64
     return launch_swiglu_bwd(gu, dh, rows, F, dgu, S(stream));
 }
 
+static int swiglu_quant_checks(const void *gu, const void *dh, bool bwd, int64_t rows, int64_t F, int fmt,
+                               const void *q, const float *s, const void *qT, const float *sT)
+{
+    if (!fmt_ok(fmt)) return FP8_ERR_INVALID_ARG;
+    if (rows < 0 || F < 0 || rows % 128 != 0 || F % 128 != 0) return FP8_ERR_SHAPE;
+    const int64_t cols = bwd ? 2 * F : F;
+    if (rows * (cols / 128) >= (int64_t)1 << 31) return FP8_ERR_SHAPE;
+    if (rows == 0 || F == 0) return FP8_OK;
+    if (!gu || (bwd && !dh) || !q || !s || !qT || !sT) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(gu) || (bwd && !aligned16(dh)) || !aligned16(q) || !aligned16(s) || !aligned16(qT) ||
+        !aligned16(sT))
+        return FP8_ERR_ALIGNMENT;
+    return FP8_OK;
+}
+
+FP8FG_API int fp8_swiglu_quant_fwd(const void *gu, int64_t rows, int64_t F, int fmt, void *q, float *s, void *qT,
+                                   float *sT, void *stream)
+{
+    const int rc = swiglu_quant_checks(gu, nullptr, false, rows, F, fmt, q, s, qT, sT);
+    if (rc != FP8_OK || rows == 0 || F == 0) return rc;
+    FP8FG_STATUS_OR_RETURN(st);
+    return launch_swiglu_quant(gu, nullptr, rows, F, fmt, q, s, qT, sT, st, S(stream));
+}
+
+FP8FG_API int fp8_swiglu_bwd_quant(const void *gu, const void *dh, int64_t rows, int64_t F, int fmt, void *q,
+                                   float *s, void *qT, float *sT, void *stream)
+{
+    const int rc = swiglu_quant_checks(gu, dh, true, rows, F, fmt, q, s, qT, sT);
+    if (rc != FP8_OK || rows == 0 || F == 0) return rc;
+    FP8FG_STATUS_OR_RETURN(st);
+    return launch_swiglu_quant(gu, dh, rows, F, fmt, q, s, qT, sT, st, S(stream));
+}
+
 }  // extern "C"

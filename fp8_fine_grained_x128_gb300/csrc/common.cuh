@@ -44,6 +44,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Two FP32 values rounded to nearest-even BF16 and packed (lo in bits 0..15).
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // |x| of both BF16 halves, as bit patterns (unsigned order = magnitude order
 // for everything but NaN, which sorts above +Inf and is caught separately).
 __device__ __forceinline__ uint32_t bf16x2_abs(uint32_t w) { return w & 0x7FFF7FFFu; }
@@ -143,6 +151,98 @@ struct Divider2 {
         }
     }
 };
+
+// SwiGLU element math (SwiGLU(g, u) = g * sigmoid(g) * u and its gradients),
+// shared by the standalone SwiGLU kernels and the quantizers that compute
+// SwiGLU while loading, so both round identically.  The 8-wide forms below
+// take 8 packed BF16 values per operand.
+// sigmoid(g) = 1 / (1 + e^-g) from the fast exponential and division: their
+// relative error (below 1e-5 for g >= -64) stays far inside half a BF16 ulp,
+// so the BF16 results are within one ulp of the correctly rounded ones.
+// Below g = -64, 1 + e^g rounds to 1, so sigmoid(g) = e^g, taken from the
+// accurate exponential: e^-g itself would overflow FP32 below g = -88.7 (and
+// the fast division's range ends before that), while e^g keeps its value down
+// into the subnormals, where g * sigmoid(g) * u can still be a nonzero BF16.
+// Groups of 8 with no gate below -64 (all but extreme inputs) run without a
+// branch; the others go out of line.
+template <bool LEFT>
+__device__ __forceinline__ float swiglu_sigmoid(float g)
+{
+    if (LEFT && g < -64.0f) return expf(g);
+    return __fdividef(1.0f, 1.0f + __expf(-g));
+}
+
+template <bool LEFT>
+__device__ __forceinline__ void swiglu_grad(float g, float u, float d, float &dg, float &du)
+{
+    const float sg = swiglu_sigmoid<LEFT>(g);
+    dg = d * u * sg * (1.0f + g * (1.0f - sg));
+    du = d * g * sg;
+}
+
+__device__ __forceinline__ float min_gate8(uint4 g4)
+{
+    const uint32_t w[4] = {g4.x, g4.y, g4.z, g4.w};
+    float m = bf16_lo(w[0]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m = fminf(m, fminf(bf16_lo(w[k]), bf16_hi(w[k])));
+    return m;
+}
+
+template <bool LEFT>
+__device__ __forceinline__ uint4 swiglu8_impl(uint4 g4, uint4 u4)
+{
+    const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float g0 = bf16_lo(gw[k]), g1 = bf16_hi(gw[k]);
+        o[k] = bf16x2_rn(g0 * swiglu_sigmoid<LEFT>(g0) * bf16_lo(uw[k]), g1 * swiglu_sigmoid<LEFT>(g1) * bf16_hi(uw[k]));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+static __device__ __noinline__ uint4 swiglu8_left(uint4 g4, uint4 u4) { return swiglu8_impl<true>(g4, u4); }
+
+// H = SwiGLU(gate, up) for 8 values, BF16 round to nearest even.
+__device__ __forceinline__ uint4 swiglu8(uint4 g4, uint4 u4)
+{
+    if (min_gate8(g4) < -64.0f) return swiglu8_left(g4, u4);
+    return swiglu8_impl<false>(g4, u4);
+}
+
+struct Uint4x2 { uint4 a, b; };
+
+template <bool LEFT>
+__device__ __forceinline__ Uint4x2 swiglu_grad8_impl(uint4 g4, uint4 u4, uint4 d4)
+{
+    const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w},
+                   dw[4] = {d4.x, d4.y, d4.z, d4.w};
+    uint32_t og[4], ou[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float dg0, du0, dg1, du1;
+        swiglu_grad<LEFT>(bf16_lo(gw[k]), bf16_lo(uw[k]), bf16_lo(dw[k]), dg0, du0);
+        swiglu_grad<LEFT>(bf16_hi(gw[k]), bf16_hi(uw[k]), bf16_hi(dw[k]), dg1, du1);
+        og[k] = bf16x2_rn(dg0, dg1);
+        ou[k] = bf16x2_rn(du0, du1);
+    }
+    return {make_uint4(og[0], og[1], og[2], og[3]), make_uint4(ou[0], ou[1], ou[2], ou[3])};
+}
+
+static __device__ __noinline__ Uint4x2 swiglu_grad8_left(uint4 g4, uint4 u4, uint4 d4)
+{
+    return swiglu_grad8_impl<true>(g4, u4, d4);
+}
+
+// dGate = dH * up * sig * (1 + gate * (1 - sig)) and dUp = dH * gate * sig
+// for 8 values, BF16 round to nearest even.
+__device__ __forceinline__ void swiglu_grad8(uint4 g4, uint4 u4, uint4 d4, uint4 &dg4, uint4 &du4)
+{
+    const Uint4x2 r = min_gate8(g4) < -64.0f ? swiglu_grad8_left(g4, u4, d4) : swiglu_grad8_impl<false>(g4, u4, d4);
+    dg4 = r.a;
+    du4 = r.b;
+}
 
 // Scales of 8 groups of 128 values spread over the 16 lanes of a half-warp
 // (each lane holds 8 values of every group; m[u] = the lane's amax bits of
@@ -277,6 +377,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+
+// 16-byte asynchronous global -> shared copy (L2 only) and the wait for all of
+// the calling thread's copies; after the wait they are visible to that thread.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {

@@ -200,13 +200,6 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parit
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
-{
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
 template <int NCOL>
 __device__ __forceinline__ void store_row(void *D, int64_t ldD, int out_f32, int64_t row, int64_t col0,
                                           const float (&v)[NCOL])
@@ -221,10 +214,10 @@ __device__ __forceinline__ void store_row(void *D, int64_t ldD, int out_f32, int
 #pragma unroll
         for (int c = 0; c < NCOL; c += 8) {
             uint4 w;
-            w.x = pack_bf16x2(v[c], v[c + 1]);
-            w.y = pack_bf16x2(v[c + 2], v[c + 3]);
-            w.z = pack_bf16x2(v[c + 4], v[c + 5]);
-            w.w = pack_bf16x2(v[c + 6], v[c + 7]);
+            w.x = bf16x2_rn(v[c], v[c + 1]);
+            w.y = bf16x2_rn(v[c + 2], v[c + 3]);
+            w.z = bf16x2_rn(v[c + 4], v[c + 5]);
+            w.w = bf16x2_rn(v[c + 6], v[c + 7]);
             *reinterpret_cast<uint4 *>(p + c) = w;
         }
     }
@@ -236,7 +229,7 @@ __device__ __forceinline__ void store_pair(void *D, int64_t ldD, int out_f32, in
     float lo, hi;
     f2_unpack(v, lo, hi);
     if (out_f32) *reinterpret_cast<float2 *>(static_cast<float *>(D) + row * ldD + col) = make_float2(lo, hi);
-    else *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(D) + row * ldD + col) = pack_bf16x2(lo, hi);
+    else *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(D) + row * ldD + col) = bf16x2_rn(lo, hi);
 }
 
 template <int BN, int STAGES, bool PROMOTE, int SBG, int GMODE, bool TSTORE>
@@ -530,8 +523,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             float f[8];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) f2_unpack(acc[4 * k + e], f[2 * e], f[2 * e + 1]);
-                            const uint4 w = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                                       pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                            const uint4 w = make_uint4(bf16x2_rn(f[0], f[1]), bf16x2_rn(f[2], f[3]),
+                                                       bf16x2_rn(f[4], f[5]), bf16x2_rn(f[6], f[7]));
                             *reinterpret_cast<uint4 *>(stg + (col >> 6) * 16384 + row * 128 +
                                                        ((((col >> 3) & 7) ^ (row & 7)) << 4)) = w;
                         }

@@ -62,5 +62,7 @@ int launch_moe_gather(const void *q, const float *s, int64_t T, int64_t K, const
                       const int32_t *offsets, int E, int64_t Mcap, void *qg, float *sg, cudaStream_t st);
 int launch_swiglu_fwd(const void *gu, int64_t rows, int64_t F, void *h, cudaStream_t st);
 int launch_swiglu_bwd(const void *gu, const void *dh, int64_t rows, int64_t F, void *dgu, cudaStream_t st);
+int launch_swiglu_quant(const void *gu, const void *dh, int64_t rows, int64_t F, int fmt, void *q, float *s,
+                        void *qT, float *sT, int *status, cudaStream_t st);
 
 }  // namespace fp8fg

@@ -277,15 +277,6 @@ __global__ void __launch_bounds__(256) k_moe_gather(const uint8_t *__restrict__ 
 
 // ---------------------------------------------------------------- SwiGLU
 
-__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + expf(-g)); }
-
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
-{
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
 __global__ void __launch_bounds__(256) k_swiglu_fwd(const uint16_t *__restrict__ gu, int64_t rows, int64_t F,
                                                     uint16_t *__restrict__ h)
 {
@@ -294,16 +285,7 @@ __global__ void __launch_bounds__(256) k_swiglu_fwd(const uint16_t *__restrict__
         const int64_t r = i / (F / 8), j = (i - r * (F / 8)) * 8;
         const uint4 g4 = *reinterpret_cast<const uint4 *>(gu + r * 2 * F + j);
         const uint4 u4 = *reinterpret_cast<const uint4 *>(gu + r * 2 * F + F + j);
-        const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float g0 = bf16_lo(gw[k]), g1 = bf16_hi(gw[k]);
-            const float h0 = g0 * sigmoidf_(g0) * bf16_lo(uw[k]);
-            const float h1 = g1 * sigmoidf_(g1) * bf16_hi(uw[k]);
-            o[k] = bf16x2_rn(h0, h1);
-        }
-        *reinterpret_cast<uint4 *>(h + r * F + j) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4 *>(h + r * F + j) = swiglu8(g4, u4);
     }
 }
 
@@ -316,26 +298,10 @@ __global__ void __launch_bounds__(256) k_swiglu_bwd(const uint16_t *__restrict__
         const uint4 g4 = *reinterpret_cast<const uint4 *>(gu + r * 2 * F + j);
         const uint4 u4 = *reinterpret_cast<const uint4 *>(gu + r * 2 * F + F + j);
         const uint4 d4 = *reinterpret_cast<const uint4 *>(dh + r * F + j);
-        const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w},
-                       dw[4] = {d4.x, d4.y, d4.z, d4.w};
-        uint32_t og[4], ou[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float dgv[2], duv[2];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const float g = hh ? bf16_hi(gw[k]) : bf16_lo(gw[k]);
-                const float u = hh ? bf16_hi(uw[k]) : bf16_lo(uw[k]);
-                const float d = hh ? bf16_hi(dw[k]) : bf16_lo(dw[k]);
-                const float sg = sigmoidf_(g);
-                dgv[hh] = d * u * sg * (1.0f + g * (1.0f - sg));
-                duv[hh] = d * g * sg;
-            }
-            og[k] = bf16x2_rn(dgv[0], dgv[1]);
-            ou[k] = bf16x2_rn(duv[0], duv[1]);
-        }
-        *reinterpret_cast<uint4 *>(dgu + r * 2 * F + j) = make_uint4(og[0], og[1], og[2], og[3]);
-        *reinterpret_cast<uint4 *>(dgu + r * 2 * F + F + j) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+        uint4 dg4, du4;
+        swiglu_grad8(g4, u4, d4, dg4, du4);
+        *reinterpret_cast<uint4 *>(dgu + r * 2 * F + j) = dg4;
+        *reinterpret_cast<uint4 *>(dgu + r * 2 * F + F + j) = du4;
     }
 }
 

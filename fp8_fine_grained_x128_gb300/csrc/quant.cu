@@ -124,36 +124,82 @@ __device__ __noinline__ uint4 quant_cols4x4_slow(uint4 lo, uint4 hi, float s0, f
 
 constexpr int kFusedSmem = 32768 + 4096 + 64 * sizeof(ColDiv2);
 
-template <int FMT>
-__global__ void __launch_bounds__(256, 3) k_quant_1x128_fused_t(const uint16_t *__restrict__ x, int64_t rows,
-                                                             int64_t cols, int64_t ldx, uint8_t *__restrict__ q,
-                                                             float *__restrict__ s, uint8_t *__restrict__ qT,
-                                                             float *__restrict__ sT, int *status)
+// What the fused quantizer reads: x itself, or SwiGLU computed while loading
+// from the gate/up projection GU [rows][2F] (forward: H [rows][F]) or from GU
+// and dH [rows][F] (backward: dGU [rows][2F], gate-gradient half then up
+// half), so the BF16 H / dGU never go to HBM.
+enum { SRC_X = 0, SRC_SWIGLU_FWD = 1, SRC_SWIGLU_BWD = 2 };
+
+// One thread's raw loads for one work unit: rows rr + 16i (i < 8), columns
+// 8g .. 8g+7 of the unit's 128-column block.  A unit is one 128x128 tile of
+// x or of H; for the backward it is a column block of the gate half together
+// with the same block of the up half (both need gate, up and dH there).  The
+// backward's dH goes to shared memory by asynchronous copies (32 more
+// registers of prefetch would not fit next to the quantizer's).
+template <int SRC> struct RawUnit;
+template <> struct RawUnit<SRC_X> { uint4 x[8]; };
+template <> struct RawUnit<SRC_SWIGLU_FWD> { uint4 g[8], u[8]; };
+template <> struct RawUnit<SRC_SWIGLU_BWD> { uint4 g[8], u[8]; };
+
+__device__ __forceinline__ void load_unit(RawUnit<SRC_X> &ru, const uint16_t *x, const uint16_t *, int64_t ldx,
+                                          int64_t, int64_t r, int64_t c, uint4 *)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ru.x[i] = ldg_stream(x + (r + 16 * i) * ldx + c);
+}
+
+__device__ __forceinline__ void load_unit(RawUnit<SRC_SWIGLU_FWD> &ru, const uint16_t *gu, const uint16_t *,
+                                          int64_t, int64_t F, int64_t r, int64_t c, uint4 *)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        ru.g[i] = ldg_stream(gu + (r + 16 * i) * 2 * F + c);
+        ru.u[i] = ldg_stream(gu + (r + 16 * i) * 2 * F + F + c);
+    }
+}
+
+// dstage: this thread's 8 staging slots (stride 256 slots: a warp's copies
+// fill 512 contiguous bytes).
+__device__ __forceinline__ void load_unit(RawUnit<SRC_SWIGLU_BWD> &ru, const uint16_t *gu, const uint16_t *dh,
+                                          int64_t, int64_t F, int64_t r, int64_t c, uint4 *dstage)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        ru.g[i] = ldg_stream(gu + (r + 16 * i) * 2 * F + c);
+        ru.u[i] = ldg_stream(gu + (r + 16 * i) * 2 * F + F + c);
+        cp_async16(dstage + 256 * i, dh + (r + 16 * i) * F + c);
+    }
+}
+
+// The plain quantizer keeps 3 CTAs per SM; the SwiGLU sources hold 64
+// registers of raw prefetch and run 2.
+template <int SRC> constexpr int fused_ctas_per_sm() { return SRC == SRC_X ? 3 : 2; }
+template <int SRC> constexpr int fused_smem() { return kFusedSmem + (SRC == SRC_SWIGLU_BWD ? 32768 : 0); }
+
+template <int FMT, int SRC>
+__global__ void __launch_bounds__(256, fused_ctas_per_sm<SRC>()) k_quant_1x128_fused_t(
+    const uint16_t *__restrict__ x, const uint16_t *__restrict__ dh, int64_t F, int64_t rows, int64_t cols,
+    int64_t ldx, uint8_t *__restrict__ q, float *__restrict__ s, uint8_t *__restrict__ qT, float *__restrict__ sT,
+    int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *tile = smem;                                              // [128][256 B], swizzled 16-B chunks
     uint32_t *colpart = reinterpret_cast<uint32_t *>(smem + 32768);    // [8 warps][128]
     ColDiv2 *cdiv = reinterpret_cast<ColDiv2 *>(smem + 32768 + 4096);  // [64 column pairs]
+    uint4 *dstage = reinterpret_cast<uint4 *>(smem + kFusedSmem) + threadIdx.x;   // backward: dH [8][256]
 
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int g = t & 15, rr = t >> 4;
-    const int64_t ncb = cols / 128, nmb = rows / 128;
-    const int64_t ntiles = ncb * nmb;
+    const int64_t nmb = rows / 128;
+    const int64_t ncb = (SRC == SRC_X ? cols : F) / 128;   // column blocks of a unit
+    const int64_t nunits = ncb * nmb;
 
-    int64_t tile_id = blockIdx.x;
-    uint4 v[8];
-    auto load_tile = [&](int64_t id) {
-        const int64_t mb = id / ncb, cb = id - mb * ncb;
-        const uint16_t *src = x + (mb * 128 + rr) * ldx + cb * 128 + g * 8;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = ldg_stream(src + 16 * i * ldx);
-    };
-    if (tile_id < ntiles) load_tile(tile_id);
-
-    for (; tile_id < ntiles; tile_id += gridDim.x) {
-        const int64_t mb = tile_id / ncb, cb = tile_id - mb * ncb;
-        const int64_t r0 = mb * 128, c0 = cb * 128;
-
+    // Quantizes the 128x128 tile at (r0, c0) whose values this thread holds in
+    // v (rows rr + 16i, columns c0 + 8g ..): codes and row scales, then the
+    // transposed codes and column scales through shared memory.  prefetch()
+    // runs once the tile is in shared memory.
+    auto quant_tile = [&](const uint4(&v)[8], int64_t r0, int64_t c0, int64_t mb, auto &&prefetch) {
+        const int64_t cb = c0 / 128;
         uint32_t cm0 = 0, cm1 = 0, cm2 = 0, cm3 = 0;
         GroupScale gs;
         {
@@ -213,8 +259,8 @@ __global__ void __launch_bounds__(256, 3) k_quant_1x128_fused_t(const uint16_t *
             *reinterpret_cast<float2 *>(sT + mb * cols + c0 + 2 * t) = make_float2(sc[0], sc[1]);
         }
         __syncthreads();
-        // the next tile's loads fly during the transposed quantization
-        if (tile_id + gridDim.x < ntiles) load_tile(tile_id + gridDim.x);
+        // the next unit's loads fly during the transposed quantization
+        prefetch();
 
         const int cw = (lane >> 3) + 4 * warp;   // columns 4cw .. 4cw+3
         const ColDiv2 d01 = cdiv[2 * cw], d23 = cdiv[2 * cw + 1];
@@ -250,6 +296,45 @@ __global__ void __launch_bounds__(256, 3) k_quant_1x128_fused_t(const uint16_t *
             *reinterpret_cast<uint32_t *>(dst + 3 * rows) = __byte_perm(t2, t3, 0x7632);
         }
         __syncthreads();   // the tile buffer is rewritten by the next iteration
+    };
+
+    int64_t unit = blockIdx.x;
+    RawUnit<SRC> ru;
+    if (unit < nunits) load_unit(ru, x, dh, ldx, F, (unit / ncb) * 128 + rr, (unit % ncb) * 128 + g * 8, dstage);
+
+    for (; unit < nunits; unit += gridDim.x) {
+        const int64_t mb = unit / ncb, cb = unit - mb * ncb;
+        const int64_t next = unit + gridDim.x;
+        auto prefetch = [&] {
+            if (next < nunits)
+                load_unit(ru, x, dh, ldx, F, (next / ncb) * 128 + rr, (next % ncb) * 128 + g * 8, dstage);
+        };
+        if constexpr (SRC == SRC_X) {
+            uint4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = ru.x[i];
+            quant_tile(v, mb * 128, cb * 128, mb, prefetch);
+        } else if constexpr (SRC == SRC_SWIGLU_FWD) {
+            uint4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = swiglu8(ru.g[i], ru.u[i]);
+            quant_tile(v, mb * 128, cb * 128, mb, prefetch);
+        } else {
+            // the up-half gradient waits in this thread's dH slots while the
+            // gate half is quantized (its registers would not fit beside it)
+            uint4 vg[8], vu[8];
+            cp_async_wait_all();   // this thread's dH copies (it reads only its own slots)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint4 du;
+                swiglu_grad8(ru.g[i], ru.u[i], dstage[256 * i], vg[i], du);
+                dstage[256 * i] = du;
+            }
+            quant_tile(vg, mb * 128, cb * 128, mb, [] {});
+#pragma unroll
+            for (int i = 0; i < 8; ++i) vu[i] = dstage[256 * i];
+            quant_tile(vu, mb * 128, F + cb * 128, mb, prefetch);
+        }
     }
 }
 
@@ -373,27 +458,45 @@ static int check_launch()
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
+template <int FMT, int SRC>
+static int launch_fused_t(const void *x, const void *dh, int64_t F, int64_t rows, int64_t cols, int64_t ldx, void *q,
+                          float *s, void *qT, float *sT, int *status, cudaStream_t st)
+{
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_done[dev & 63]) {
+        if (cudaFuncSetAttribute(k_quant_1x128_fused_t<FMT, SRC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 fused_smem<SRC>()) != cudaSuccess)
+            return FP8_ERR_CUDA;
+        attr_done[dev & 63] = true;
+    }
+    const int64_t nunits = (rows / 128) * ((SRC == SRC_X ? cols : F) / 128);
+    if (nunits == 0) return FP8_OK;
+    const int64_t grid = std::min<int64_t>(nunits, (int64_t)sm_count() * fused_ctas_per_sm<SRC>());
+    k_quant_1x128_fused_t<FMT, SRC><<<(unsigned)grid, 256, fused_smem<SRC>(), st>>>(
+        static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(dh), F, rows, cols, ldx,
+        static_cast<uint8_t *>(q), s, static_cast<uint8_t *>(qT), sT, status);
+    return check_launch();
+}
+
+int launch_swiglu_quant(const void *gu, const void *dh, int64_t rows, int64_t F, int fmt, void *q, float *s, void *qT,
+                        float *sT, int *status, cudaStream_t st)
+{
+    if (rows == 0 || F == 0) return FP8_OK;
+    if (dh == nullptr)   // forward: H [rows][F]
+        return fmt == FP8_E5M2 ? launch_fused_t<FP8_E5M2, SRC_SWIGLU_FWD>(gu, nullptr, F, rows, F, 2 * F, q, s, qT, sT, status, st)
+                               : launch_fused_t<FP8_E4M3, SRC_SWIGLU_FWD>(gu, nullptr, F, rows, F, 2 * F, q, s, qT, sT, status, st);
+    // backward: dGU [rows][2F]
+    return fmt == FP8_E5M2 ? launch_fused_t<FP8_E5M2, SRC_SWIGLU_BWD>(gu, dh, F, rows, 2 * F, 2 * F, q, s, qT, sT, status, st)
+                           : launch_fused_t<FP8_E4M3, SRC_SWIGLU_BWD>(gu, dh, F, rows, 2 * F, 2 * F, q, s, qT, sT, status, st);
+}
+
 template <int FMT>
 static int quant_1x128_fmt(const void *x, int64_t rows, int64_t cols, int64_t ldx, void *q, float *s, void *qT,
                            float *sT, int *status, cudaStream_t st)
 {
-    if (qT) {
-        static bool attr_done[64] = {};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (!attr_done[dev & 63]) {
-            if (cudaFuncSetAttribute(k_quant_1x128_fused_t<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kFusedSmem) != cudaSuccess)
-                return FP8_ERR_CUDA;
-            attr_done[dev & 63] = true;
-        }
-        const int64_t ntiles = (rows / 128) * (cols / 128);
-        const int64_t grid = std::min<int64_t>(ntiles, (int64_t)sm_count() * 3);   // 3 resident CTAs per SM
-        k_quant_1x128_fused_t<FMT><<<(unsigned)grid, 256, kFusedSmem, st>>>(
-            static_cast<const uint16_t *>(x), rows, cols, ldx, static_cast<uint8_t *>(q), s,
-            static_cast<uint8_t *>(qT), sT, status);
-        return check_launch();
-    }
+    if (qT) return launch_fused_t<FMT, SRC_X>(x, nullptr, 0, rows, cols, ldx, q, s, qT, sT, status, st);
     constexpr int U = 8;
     const int64_t items = rows * ((cols / 128 + U - 1) / U);
     // one run per half-warp: the block scheduler balances the load (a

@@ -378,6 +378,25 @@ FP8FG_API int fp8_swiglu_fwd(const void *gu, int64_t rows, int64_t F, void *h, v
 FP8FG_API int fp8_swiglu_bwd(const void *gu, const void *dh, int64_t rows, int64_t F, void *dgu,
                              void *stream);
 
+/* SwiGLU fused into the 1x128 quantizer with its 128x1 transposed copy
+ * ([Ling] "Fine-grained quantization": the activation that feeds the down
+ * projection and the gradient that feeds the up projection's dgrad/wgrad are
+ * quantized 1x128 per row, and 128x1 for the wgrad operand).  The BF16
+ * values are those fp8_swiglu_fwd / fp8_swiglu_bwd would write, bit for bit,
+ * but they are computed while loading and never stored; the outputs equal
+ * fp8_quant_1x128(those values, qT, sT set) bit for bit.
+ * Forward:  gu BF16 [rows][2F]  ->  H [rows][F] quantized:
+ *   q [rows][F], s S[F/128][rows], qT [F][rows], sT S[rows/128][F].
+ * Backward: gu, dh BF16 [rows][F]  ->  dGU [rows][2F] quantized:
+ *   q [rows][2F], s S[2F/128][rows], qT [2F][rows], sT S[rows/128][2F].
+ * rows % 128 == 0, F % 128 == 0, rows * (output cols / 128) < 2^31; all
+ * pointers 16-byte aligned and owned by the caller.  A group holding Inf/NaN
+ * records FP8_ERR_NONFINITE (its outputs unspecified). */
+FP8FG_API int fp8_swiglu_quant_fwd(const void *gu, int64_t rows, int64_t F, int fmt, void *q, float *s,
+                                   void *qT, float *sT, void *stream);
+FP8FG_API int fp8_swiglu_bwd_quant(const void *gu, const void *dh, int64_t rows, int64_t F, int fmt,
+                                   void *q, float *s, void *qT, float *sT, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

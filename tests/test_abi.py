@@ -107,6 +107,15 @@ def test_host_validation_without_launch(lib):
     assert lib.fp8_moe_route_pad(good, 16, 300, 8, 128, 1024, good, good, good, good, good, good, None, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_moe_route_pad(good, 16, 8, 9, 128, 1024, good, good, good, good, good, good, None, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_swiglu_fwd(good, 4, 12, good, S) == fg.ERR_SHAPE
+    assert lib.fp8_swiglu_quant_fwd(good, 128, 96, 0, good, good, good, good, S) == fg.ERR_SHAPE
+    assert lib.fp8_swiglu_quant_fwd(good, 100, 128, 0, good, good, good, good, S) == fg.ERR_SHAPE
+    assert lib.fp8_swiglu_quant_fwd(good, 128, 128, 7, good, good, good, good, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_swiglu_quant_fwd(good, 128, 128, 0, good, good, None, good, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_swiglu_quant_fwd(odd, 128, 128, 0, good, good, good, good, S) == fg.ERR_ALIGNMENT
+    assert lib.fp8_swiglu_quant_fwd(None, 0, 128, 0, None, None, None, None, S) == fg.OK
+    assert lib.fp8_swiglu_bwd_quant(good, None, 128, 128, 0, good, good, good, good, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_swiglu_bwd_quant(good, odd, 128, 128, 1, good, good, good, good, S) == fg.ERR_ALIGNMENT
+    assert lib.fp8_swiglu_bwd_quant(good, good, 1 << 24, 1 << 16, 1, good, good, good, good, S) == fg.ERR_SHAPE
     # delayed scaling: recipe checks
     rec = fg.DelayedRecipe(0, 0, 0, 0)
     assert lib.fp8_quant_pertensor_delayed(good, 128, 128, 128, ctypes.byref(rec), good, good, good, good,

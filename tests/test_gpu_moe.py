@@ -147,6 +147,27 @@ def test_swiglu_fwd_bwd_within_one_ulp():
         assert np.max(np.abs(gi - ri)) <= 1
 
 
+def test_swiglu_extreme_gates_within_one_ulp():
+    """Gates over [-100, 100] (the fast sigmoid's range ends near -87; below -64
+    the correctly rounded form takes over) and the zero of the gate gradient's
+    factor 1 + g(1 - sig(g)) near g = -1.28."""
+    R, F = 128, 1024
+    rng = np.random.default_rng(12)
+    g = np.concatenate([np.linspace(-100.0, 100.0, R * F // 2), rng.uniform(-1.4, -1.15, R * F // 2)])
+    gate = synth.f32_to_bf16_bits(rng.permutation(g).astype(np.float32)).reshape(R, F)
+    up = synth.bf16_normal((R, F), 13, 1.0)
+    gu = np.concatenate([gate, up], axis=1)
+    dh = synth.bf16_normal((R, F), 14, 1.0)
+    h = torch.empty((R, F), dtype=torch.bfloat16, device="cuda")
+    dgu = torch.empty((R, 2 * F), dtype=torch.bfloat16, device="cuda")
+    fg.swiglu_fwd(dev_bf16(gu), h)
+    fg.swiglu_bwd(dev_bf16(gu), dev_bf16(dh), dgu)
+    assert_status_ok()
+    si = lambda b: np.where(b & 0x8000, -(b & 0x7FFF).astype(np.int64), (b & 0x7FFF).astype(np.int64))
+    for got, ref in ((host_u16(h), oracle.swiglu_fwd(gu)), (host_u16(dgu), oracle.swiglu_bwd(gu, dh))):
+        assert np.max(np.abs(si(got) - si(ref))) <= 1
+
+
 def test_moe_fprop_full_size():
     """128 experts, hidden 2048, FFN 768, top-8 over 8192 tokens: route+pad,
     quantize once, gather, gate/up grouped GEMM, SwiGLU, 1x128 quantize,
