@@ -46,7 +46,6 @@ namespace fp8fg {
 constexpr int kGemmThreads = 384;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiWarp0 = 4;          // first epilogue warp (warpgroups 1 and 2)
-constexpr int kStageReleaseWarp = 7;  // epilogue warp that frees smem stages in promote mode
 // setmaxnreg of the control warpgroup and of the two epilogue warpgroups,
 // per scale mode (the 1x128 x 1x128 epilogue holds per-row and per-column
 // scales beside its accumulators)
@@ -361,13 +360,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         tc_mma_f8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
                                       (k > 0 || (!PROMOTE && kb > 0)) ? 1u : 0u);
                     }
+                    // the stage goes back to the producer as soon as these MMAs
+                    // have read it, whatever the epilogue is doing
+                    tc_commit(&empty[s]);
                     if (PROMOTE) {
-                        // one commit per chunk: when the accumulator is complete its
-                        // smem stage is no longer read, so the epilogue frees both
-                        tc_commit(&tfull[buf]);
+                        tc_commit(&tfull[buf]);   // one accumulator per chunk
                         ++cc;
-                    } else {
-                        tc_commit(&empty[s]);
                     }
                     ++it;
                 }
@@ -451,8 +449,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     float sr = sv[a.granA == FP8_GRAN_1x128 ? row : 128];
                     if (SBG == SB_BLOCK) sr *= sv[256 + (ew >> 2)];
                     if (!warp_wait_or_abort(&tfull[buf], (cc / L::kNbuf) & 1, abort_flag, a.status)) { ok = false; break; }
-                    // the chunk's MMAs are complete, so its smem stage is no longer read
-                    if (warp == kStageReleaseWarp && lane == 0) mbar_arrive(&empty[cc % STAGES]);
                     tc_fence_after();
                     const uint64_t s2 = f2_pack(sr, sr);
                     if (SBG == SB_BLOCK) {
