@@ -76,18 +76,34 @@ def test_fused_equals_unfused_and_oracle(bwd, fmt):
 @pytest.mark.parametrize("bwd", [False, True])
 def test_fused_equals_unfused_at_mlp_size(bwd):
     """The MLP block's shapes: 8192 tokens, FFN 14336 (GU is [8192][28672]);
-    forward H quantized E4M3, backward dGU quantized E5M2."""
+    forward H quantized E4M3, backward dGU quantized E5M2.  Everything is
+    compared with the unfused GPU path, and one 128-row block with the oracle."""
     R, F = 8192, 14336
     g = torch.Generator(device="cuda").manual_seed(7)
     gu = (torch.randn((R, 2 * F), generator=g, device="cuda") * 2).to(torch.bfloat16)
     dh = (torch.randn((R, F), generator=g, device="cuda") * 1e-3).to(torch.bfloat16) if bwd else None
     fmt = fg.E5M2 if bwd else fg.E4M3
     v, ref = unfused(gu, dh, fmt)
-    del v
     got = fused(gu, dh, fmt)
     assert_status_ok()
     for a, b in zip(got, ref):
         assert same_bits(a, b)
+    # against the oracle on one 128-row block (whole 1x128 and 128x1 groups):
+    # the GPU's SwiGLU within one BF16 ulp of the oracle's, the fused codes and
+    # scales equal to the oracle's quantization of those GPU values
+    mb = 37
+    r0, r1 = mb * 128, mb * 128 + 128
+    gu_h = host_u16(gu[r0:r1])
+    want_v = oracle.swiglu_fwd(gu_h) if dh is None else oracle.swiglu_bwd(gu_h, host_u16(dh[r0:r1]))
+    vb = host_u16(v[r0:r1])
+    si = lambda b: np.where(b & 0x8000, -(b & 0x7FFF).astype(np.int64), (b & 0x7FFF).astype(np.int64))
+    assert np.max(np.abs(si(vb) - si(want_v))) <= 1
+    q, s, _ = oracle.quant_1x128(vb, fmt)
+    qT, sT, _ = oracle.quant_128x1_transposed(vb, fmt)
+    assert np.array_equal(got[0][r0:r1].cpu().numpy(), q)
+    assert np.array_equal(got[1][:, r0:r1].cpu().numpy().view(np.uint32), s.view(np.uint32))
+    assert np.array_equal(got[2][:, r0:r1].cpu().numpy(), qT)
+    assert np.array_equal(got[3][mb:mb + 1].cpu().numpy().view(np.uint32), sT.view(np.uint32))
 
 
 def test_nonfinite_gate_is_reported():
@@ -105,3 +121,17 @@ def test_empty_is_a_no_op():
     fg.swiglu_bwd_quant(gu, torch.empty((0, 128), dtype=torch.bfloat16, device="cuda"), fg.E5M2,
                         *quant_outputs(0, 256))
     assert_status_ok()
+
+
+def test_zero_inputs_give_zero_codes_and_unit_scales():
+    """SwiGLU(0, u) = 0 and dGU(g, u, 0) = 0: every group's amax is 0, so s = 1
+    and every code is +0."""
+    R, F = 256, 256
+    gu = dev_bf16(synth.bf16_normal((R, 2 * F), 71, 1.0))
+    zero_gate = gu.clone()
+    zero_gate[:, :F] = 0
+    for dh in (None, torch.zeros((R, F), dtype=torch.bfloat16, device="cuda")):
+        out = fused(zero_gate if dh is None else gu, dh, fg.E4M3)
+        assert_status_ok()
+        assert not torch.any(out[0]) and not torch.any(out[2])
+        assert torch.all(out[1] == 1.0) and torch.all(out[3] == 1.0)
