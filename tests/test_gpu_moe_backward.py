@@ -128,3 +128,36 @@ def test_moe_wgrad_from_routing_map():
     want = oracle.grouped_wgrad_full(offs, AT, oracle.E5M2, sA, BT, oracle.E4M3, sB)
     got = run_wgrad(offs, AT, oracle.E5M2, sA, BT, oracle.E4M3, sB, torch.float32)
     gemm_tolerance_check(got.reshape(-1, K), want.reshape(-1, K), bf16_out=False)
+
+
+def test_moe_dgrad_through_batched_transpose():
+    """dH_e = dY_e . W_e for the down projection: the expert weights W_e [H][F]
+    are quantized 128x128, transposed on the GPU into W_e^T [F][H] (codes and
+    scale grid), and the grouped GEMM contracts the dispatch rows of dY (1x128
+    along H) with them; checked against the oracle's grouped GEMM over the
+    oracle's own transposes, with an empty expert and a 3-tile expert."""
+    E, H, F = 4, 256, 384
+    offs = np.array([0, 128, 128, 512, 640], np.int32)
+    cap = 768                                            # rows past the last expert stay untouched
+    w = synth.bf16_normal((E, H, F), 81, 0.02)
+    qw = np.empty((E, H, F), np.uint8)
+    sw = np.empty((E, H // 128, F // 128), np.float32)
+    for e in range(E):
+        qw[e], sw[e], _ = oracle.quant_128x128(w[e])
+    qwT = torch.empty((E, F, H), dtype=torch.uint8, device="cuda")
+    swT = torch.empty((E, F // 128, H // 128), dtype=torch.float32, device="cuda")
+    fg.transpose_128x128_batched(dev_u8(qw), dev_f32(sw), qwT, swT)
+    dy = synth.bf16_normal((cap, H), 82, 1e-3, 1e-3, 20.0)
+    qa, sa, _ = oracle.quant_1x128(dy)
+    D = torch.full((cap, F), 7.0, dtype=torch.float32, device="cuda")
+    fg.grouped_gemm(torch.from_numpy(offs).cuda(), dev_u8(qa), dev_f32(sa), qwT, swT, D)
+    assert_status_ok()
+    refT = np.stack([oracle.fp8_transpose(qw[e]) for e in range(E)])
+    assert np.array_equal(qwT.cpu().numpy(), refT)
+    srefT = np.ascontiguousarray(sw.transpose(0, 2, 1))
+    pm, pn = np.meshgrid(np.arange(offs[-1]), np.arange(F), indexing="ij")
+    pm, pn = pm.reshape(-1), pn.reshape(-1)
+    want = oracle.grouped_gemm_points(offs, qa, sa, cap, refT, srefT, pm, pn).reshape(offs[-1], F)
+    got = D.cpu().numpy().astype(np.float64)
+    gemm_tolerance_check(got[: offs[-1]], want, bf16_out=False)
+    assert np.all(got[offs[-1]:] == 7.0)
