@@ -14,6 +14,8 @@
 // then the new m and v are re-quantized with their blocks' new scales.  One
 // pass over HBM: the parameters (read + write), the BF16 gradient and both
 // code arrays.
+#include <algorithm>
+
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -53,7 +55,28 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
-// One warp per block of 128 parameters, 4 consecutive parameters per lane.
+// What a lane reads of one 128-parameter block.
+struct AdamBlockIn {
+    float4 p4;
+    uint2 g4;
+    uint32_t cm, cv;
+    float s_m, s_v;
+};
+
+__device__ __forceinline__ void load_block(AdamBlockIn &in, const float *p, const uint16_t *g, const uint8_t *qm,
+                                           const float *sm, const uint8_t *qv, const float *sv, int64_t b, int lane)
+{
+    const int64_t k = b * 128 + lane * 4;
+    in.p4 = __ldcs(reinterpret_cast<const float4 *>(p + k));
+    in.g4 = __ldcs(reinterpret_cast<const uint2 *>(g + k));
+    in.cm = *reinterpret_cast<const uint32_t *>(qm + k);
+    in.cv = *reinterpret_cast<const uint32_t *>(qv + k);
+    in.s_m = sm[b];
+    in.s_v = sv[b];
+}
+
+// One warp per block of 128 parameters, 4 consecutive parameters per lane;
+// the warp's next block is read while the current one is computed.
 __global__ void __launch_bounds__(256) k_adamw_fp8(float *__restrict__ p, const uint16_t *__restrict__ g,
                                                    uint8_t *__restrict__ qm, float *__restrict__ sm,
                                                    uint8_t *__restrict__ qv, float *__restrict__ sv, int64_t nblk,
@@ -62,13 +85,16 @@ __global__ void __launch_bounds__(256) k_adamw_fp8(float *__restrict__ p, const 
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    AdamBlockIn cur;
+    if (w0 < nblk) load_block(cur, p, g, qm, sm, qv, sv, w0, lane);
     for (int64_t b = w0; b < nblk; b += nw) {
+        AdamBlockIn nxt;
+        if (b + nw < nblk) load_block(nxt, p, g, qm, sm, qv, sv, b + nw, lane);
         const int64_t k = b * 128 + lane * 4;
-        const float4 p4 = __ldcs(reinterpret_cast<const float4 *>(p + k));
-        const uint2 g4 = __ldcs(reinterpret_cast<const uint2 *>(g + k));
-        const uint32_t cm = *reinterpret_cast<const uint32_t *>(qm + k);
-        const uint32_t cv = *reinterpret_cast<const uint32_t *>(qv + k);
-        const float s_m = sm[b], s_v = sv[b];
+        const float4 p4 = cur.p4;
+        const uint2 g4 = cur.g4;
+        const uint32_t cm = cur.cm, cv = cur.cv;
+        const float s_m = cur.s_m, s_v = cur.s_v;
         float pp[4] = {p4.x, p4.y, p4.z, p4.w};
         const float gg[4] = {bf16_lo(g4.x), bf16_hi(g4.x), bf16_lo(g4.y), bf16_hi(g4.y)};
         float m[4], v[4];
@@ -100,6 +126,7 @@ __global__ void __launch_bounds__(256) k_adamw_fp8(float *__restrict__ p, const 
             sm[b] = nsm;
             sv[b] = nsv;
         }
+        cur = nxt;
     }
 }
 
@@ -108,8 +135,15 @@ int launch_adamw_fp8(float *p, const void *g, uint8_t *qm, float *sm, uint8_t *q
 {
     const int64_t nblk = n / 128;
     if (nblk == 0) return FP8_OK;
+    // one wave of resident blocks, each warp striding over the 128-blocks
+    static int per_sm[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (per_sm[dev & 63] == 0 &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[dev & 63], k_adamw_fp8, 256, 0) != cudaSuccess)
+        return FP8_ERR_CUDA;
     int64_t blocks = (nblk + 7) / 8;
-    const int64_t cap = (int64_t)sm_count() * 8;
+    const int64_t cap = (int64_t)sm_count() * std::max(1, per_sm[dev & 63]);
     if (blocks > cap) blocks = cap;
     k_adamw_fp8<<<(unsigned)blocks, 256, 0, st>>>(p, static_cast<const uint16_t *>(g), qm, sm, qv, sv, nblk, h);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
