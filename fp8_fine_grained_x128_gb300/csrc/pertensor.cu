@@ -413,8 +413,11 @@ __device__ __forceinline__ void mon_group(uint2 xv, uint32_t qv, float sc, Group
         uf += nzero && ((code & 0x7Fu) == 0);
         sat += st(xs[e], fm);
         kx[e] = key_bf16(xs[e]);
-        const uint32_t bit = 1u << (kx[e] & 31);
-        din += (atomicOr(&g.bx[kx[e] >> 5], bit) & bit) == 0;
+        // word from the key's low 11 bits, bit from its top 5 (sign and high
+        // exponent bits): a group's values share a few binades, and this
+        // spreads them over words and banks instead of stacking them on a few
+        const uint32_t bit = 1u << (kx[e] >> 11);
+        din += (atomicOr(&g.bx[kx[e] & 2047u], bit) & bit) == 0;
         fqb[key_fp8(code)] = 1;
     }
     __syncwarp();
@@ -423,7 +426,7 @@ __device__ __forceinline__ void mon_group(uint2 xv, uint32_t qv, float sc, Group
     g.fq[lane] = 0;
     g.fq[lane + 32] = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) g.bx[kx[e] >> 5] = 0;
+    for (int e = 0; e < 4; ++e) g.bx[kx[e] & 2047u] = 0;
     __syncwarp();
 }
 
@@ -473,18 +476,26 @@ __global__ void __launch_bounds__(kG128Warps * 32) k_stats_1x128(const uint16_t 
     const int64_t ncb = cols / 128, ngroups = rows * ncb;
     constexpr int U = 4;
     uint32_t nz = 0, uf = 0, sat = 0, din = 0, dout = 0;
+    // group gi = r * ncb + cb; stepping gi by nwarps moves (r, cb) by (dq, dr)
+    // with one carry, so no division runs per group
+    const int64_t dq = nwarps / ncb, dr = nwarps - dq * ncb;
+    int64_t r = warp0 / ncb, cb = warp0 - r * ncb;
     for (int64_t base = warp0; base < ngroups; base += U * nwarps) {
         uint2 xv[U];
         uint32_t qv[U];
         float sc[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t gi = base + u * nwarps;
-            if (gi < ngroups) {
-                const int64_t r = gi / ncb, cb = gi - r * ncb;
+            if (base + u * nwarps < ngroups) {
                 xv[u] = __ldcs(reinterpret_cast<const uint2 *>(x + r * ldx + cb * 128) + lane);
                 qv[u] = __ldcs(reinterpret_cast<const uint32_t *>(q + r * cols + cb * 128) + lane);
                 sc[u] = s[cb * rows + r];
+            }
+            r += dq;
+            cb += dr;
+            if (cb >= ncb) {
+                cb -= ncb;
+                ++r;
             }
         }
 #pragma unroll
