@@ -45,7 +45,7 @@ M_TOK, HID, FFN = 8192, 4096, 14336
 # six, from a one-pass ncu capture of the current kernel; the summary with
 # its command is profiles/k_gemm_step_dram_traffic.md).  Set to None when the
 # kernel changes until it is captured again.
-GEMM_TRAFFIC_BYTES = 734519082
+GEMM_TRAFFIC_BYTES = 736739882
 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0

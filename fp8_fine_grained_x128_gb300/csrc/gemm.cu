@@ -452,24 +452,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after();
                     const uint64_t s2 = f2_pack(sr, sr);
                     if (SBG == SB_BLOCK) {
-                        // 64 columns per wait: two x32 loads in flight
+                        // 16 columns per wait: the 128 accumulator registers and the
+                        // staging registers fit the epilogue's budget with room to spare
+                        // (two x32 loads per wait measured 8% slower, x8 loads 13%)
 #pragma unroll
-                        for (int j = 0; j < HALF / 64; ++j) {
-                            uint32_t r0[32], r1[32];
-                            tc_ld_32x32b_x32(tm_lane + buf * BN + colbase + j * 64, r0);
-                            tc_ld_32x32b_x32(tm_lane + buf * BN + colbase + j * 64 + 32, r1);
+                        for (int j = 0; j < HALF / 16; ++j) {
+                            uint32_t r0[16];
+                            tc_ld_32x32b_x16(tm_lane + buf * BN + colbase + j * 16, r0);
                             tc_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                acc[j * 32 + i] = f2_fma_bits(r0[2 * i], r0[2 * i + 1], s2, acc[j * 32 + i]);
-                                acc[j * 32 + 16 + i] = f2_fma_bits(r1[2 * i], r1[2 * i + 1], s2, acc[j * 32 + 16 + i]);
-                            }
+                            for (int i = 0; i < 8; ++i)
+                                acc[j * 8 + i] = f2_fma_bits(r0[2 * i], r0[2 * i + 1], s2, acc[j * 8 + i]);
                         }
                     } else {
                         // per-column scales sB(n, kb).  16x256b fragments: each
                         // thread holds rows {16h + q, 16h + q + 8} (q = lane / 4,
                         // h = 0, 1) of its lane quarter and columns 8i + 2(lane % 4)
-                        // + {0, 1}, so it reads 1/4 of the column scales.
+                        // + {0, 1}, so it reads 1/4 of the column scales.  32
+                        // columns of one 16-lane half per wait (two 64-column x8
+                        // loads per wait were 13% slower on the grouped wgrad).
                         uint64_t sa2[4];
 #pragma unroll
                         for (int rr = 0; rr < 4; ++rr) {
@@ -477,21 +478,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             sa2[rr] = f2_pack(v, v);
                         }
 #pragma unroll
-                        for (int c = 0; c < HALF / 64; ++c) {
-                            // both 16-lane halves of the quarter in flight per wait
-                            uint32_t p0[32], p1[32];
-                            const uint32_t ta = tmem_base + ((uint32_t)(lg * 32) << 16) + buf * BN + colbase + 64 * c;
-                            tc_ld_16x256b_x8(ta, p0);
-                            tc_ld_16x256b_x8(ta + (16u << 16), p1);
-                            tc_wait_ld();
+                        for (int c2 = 0; c2 < HALF / 32; ++c2) {
+                            uint64_t sbv[4];   // column-scale pairs of this thread's 4 eight-column groups
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const uint64_t sb = *reinterpret_cast<const uint64_t *>(sv + 256 + colbase + 64 * c + 8 * i + 2 * (lane & 3));
-                                uint64_t *ac = acc + 8 * c + i;
-                                ac[0 * (HALF / 8)] = f2_fma(f2_mul_bits(p0[4 * i], p0[4 * i + 1], sb), sa2[0], ac[0 * (HALF / 8)]);
-                                ac[1 * (HALF / 8)] = f2_fma(f2_mul_bits(p0[4 * i + 2], p0[4 * i + 3], sb), sa2[1], ac[1 * (HALF / 8)]);
-                                ac[2 * (HALF / 8)] = f2_fma(f2_mul_bits(p1[4 * i], p1[4 * i + 1], sb), sa2[2], ac[2 * (HALF / 8)]);
-                                ac[3 * (HALF / 8)] = f2_fma(f2_mul_bits(p1[4 * i + 2], p1[4 * i + 3], sb), sa2[3], ac[3 * (HALF / 8)]);
+                            for (int i = 0; i < 4; ++i)
+                                sbv[i] = *reinterpret_cast<const uint64_t *>(sv + 256 + colbase + 32 * c2 + 8 * i +
+                                                                             2 * (lane & 3));
+                            // one 16-lane half of the quarter (32 columns) per wait
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                uint32_t p0[16];
+                                tc_ld_16x256b_x4(tmem_base + ((uint32_t)(lg * 32 + 16 * hh) << 16) + buf * BN + colbase +
+                                                     32 * c2,
+                                                 p0);
+                                tc_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    uint64_t *ac = acc + 4 * c2 + i;
+                                    ac[(2 * hh) * (HALF / 8)] = f2_fma(f2_mul_bits(p0[4 * i], p0[4 * i + 1], sbv[i]),
+                                                                       sa2[2 * hh], ac[(2 * hh) * (HALF / 8)]);
+                                    ac[(2 * hh + 1) * (HALF / 8)] =
+                                        f2_fma(f2_mul_bits(p0[4 * i + 2], p0[4 * i + 3], sbv[i]), sa2[2 * hh + 1],
+                                               ac[(2 * hh + 1) * (HALF / 8)]);
+                                }
                             }
                         }
                     }
