@@ -161,3 +161,46 @@ def test_moe_dgrad_through_batched_transpose():
     got = D.cpu().numpy().astype(np.float64)
     gemm_tolerance_check(got[: offs[-1]], want, bf16_out=False)
     assert np.all(got[offs[-1]:] == 7.0)
+
+
+def test_moe_down_wgrad_full_size():
+    """The MoE block's shapes (8192 tokens, 128 experts, top-8, hidden 2048,
+    FFN 768): dW_down_e = dY_e^T . H_e over each expert's dispatch rows, from a
+    real routing map.  The fused quantizer's transposed copies of the dispatch
+    buffers must equal the oracle's 128x1 quantization bit for bit; the grouped
+    wgrad is checked on sampled outputs of every expert."""
+    T, E, topk, Hd, F = 8192, 128, 8, 2048, 768
+    _, logits, _, _ = synth.moe_inputs()
+    ref = oracle.moe_route(logits, topk=topk, align=128)
+    offs, rows, tot = ref["offsets"], ref["row_token"], ref["total"]
+    cap = (ref["cap"] + 127) // 128 * 128
+    dy_tok = synth.bf16_normal((T, Hd), 91, 1e-3, 1e-3, 20.0)
+    h_tok = synth.bf16_normal((T, F), 92, 1.0, 1e-3, 20.0)
+    dy_d = np.zeros((cap, Hd), np.uint16)
+    h_d = np.zeros((cap, F), np.uint16)
+    dy_d[:tot] = dy_tok[rows[:tot]]
+    h_d[:tot] = h_tok[rows[:tot]]
+    dy_d[:tot][ref["row_is_pad"][:tot] == 1] = 0          # padding rows carry no gradient
+    ops = []
+    for bits, fmt in ((dy_d, oracle.E5M2), (h_d, oracle.E4M3)):
+        R, C = bits.shape
+        q, s = torch.empty((R, C), dtype=torch.uint8, device="cuda"), torch.empty((C // 128, R), device="cuda")
+        qT, sT = torch.empty((C, R), dtype=torch.uint8, device="cuda"), torch.empty((R // 128, C), device="cuda")
+        fg.quant_1x128(dev_bf16(bits), fmt, q, s, qT, sT)
+        assert_status_ok()
+        rqT, rsT, _ = oracle.quant_128x1_transposed(bits, fmt)
+        assert np.array_equal(qT.cpu().numpy(), rqT)
+        assert np.array_equal(sT.cpu().numpy().view(np.uint32), rsT.view(np.uint32))
+        ops.append((qT, sT, rqT, rsT))
+        del q, s
+    (AT, sA, rAT, rsA), (BT, sB, rBT, rsB) = ops
+    D = torch.empty((E * Hd, F), dtype=torch.float32, device="cuda")
+    fg.grouped_gemm_wgrad(torch.from_numpy(offs.astype(np.int32)).cuda(), AT, fg.E5M2, sA, BT, fg.E4M3, sB, D)
+    assert_status_ok()
+    rng = np.random.default_rng(93)
+    pg = np.repeat(np.arange(E), 256)                     # 256 samples from every expert
+    pn = rng.integers(0, Hd, pg.size)
+    pk = rng.integers(0, F, pg.size)
+    want = oracle.grouped_wgrad_points(offs, rAT, oracle.E5M2, rsA, rBT, oracle.E4M3, rsB, pg, pn, pk)
+    got = D.view(E, Hd, F)[torch.from_numpy(pg).cuda(), torch.from_numpy(pn).cuda(), torch.from_numpy(pk).cuda()]
+    gemm_tolerance_check(got.cpu().numpy().astype(np.float64), want, bf16_out=False)
