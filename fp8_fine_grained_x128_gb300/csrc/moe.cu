@@ -36,8 +36,14 @@ __device__ __forceinline__ float key_logit(uint32_t k)
 
 template <int EPL>
 __global__ void __launch_bounds__(256) k_moe_topk(const float *__restrict__ logits, int64_t T, int E, int topk,
-                                                  int32_t *__restrict__ topk_idx, float *__restrict__ topk_prob)
+                                                  int32_t *__restrict__ topk_idx, float *__restrict__ topk_prob,
+                                                  int32_t *__restrict__ counts)
 {
+    // per-expert counts of this block's choices (E <= 256), merged into
+    // counts[] (zeroed by the launcher) at the end
+    __shared__ int hist[256];
+    for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -83,24 +89,8 @@ __global__ void __launch_bounds__(256) k_moe_topk(const float *__restrict__ logi
         if (lane < topk) {
             topk_idx[t * topk + lane] = (int32_t)my_idx;
             topk_prob[t * topk + lane] = expf(key_logit(my_key) - m) / sum;
+            if (my_idx < (uint32_t)E) atomicAdd(&hist[my_idx], 1);
         }
-    }
-}
-
-// ------------------------------------------------------------ per-expert count
-
-// Histogram of the top-k choices (each token's choices are distinct experts):
-// one pass over topk_idx, shared-memory counts merged into counts[], which
-// the launcher has zeroed.
-__global__ void __launch_bounds__(256) k_moe_count(const int32_t *__restrict__ topk_idx, int64_t n, int E,
-                                                   int32_t *__restrict__ counts)
-{
-    __shared__ int hist[256];
-    for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const int e = topk_idx[i];
-        if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < E; i += blockDim.x)
@@ -319,16 +309,12 @@ int launch_moe_route_pad(const float *logits, int64_t T, int E, int topk, int al
     if (blocks < 1) blocks = 1;
     const unsigned b = (unsigned)blocks;
     const int epl = (E + 31) / 32;
-    if (epl <= 1) k_moe_topk<1><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob);
-    else if (epl <= 2) k_moe_topk<2><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob);
-    else if (epl <= 4) k_moe_topk<4><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob);
-    else k_moe_topk<8><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob);
+    // the top-k kernel also counts each expert's tokens
     if (cudaMemsetAsync(counts, 0, (size_t)E * sizeof(int32_t), st) != cudaSuccess) return FP8_ERR_CUDA;
-    const int64_t n = T * topk;
-    if (n > 0) {
-        const int64_t cb = std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 2);
-        k_moe_count<<<(unsigned)cb, 256, 0, st>>>(topk_idx, n, E, counts);
-    }
+    if (epl <= 1) k_moe_topk<1><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob, counts);
+    else if (epl <= 2) k_moe_topk<2><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob, counts);
+    else if (epl <= 4) k_moe_topk<4><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob, counts);
+    else k_moe_topk<8><<<b, 256, 0, st>>>(logits, T, E, topk, topk_idx, topk_prob, counts);
     k_moe_fill<<<E, kFillThreads, 0, st>>>(topk_idx, topk_prob, counts, T, E, topk, align, Mcap, offsets, row_token, row_prob,
                                   row_is_pad, status);
     return check_launch();
