@@ -128,3 +128,23 @@ def test_host_validation_without_launch(lib):
                                            None, None, good, S) == fg.ERR_SHAPE
     assert lib.fp8_selftest_wait_timeout(0, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_device_status(S, None) == fg.ERR_INVALID_ARG
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/fp8fg.h is a C header: it compiles as pedantic C99 with every
+    warning an error, and a C caller links nothing but the declarations."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "fp8fg.h"\n'
+                   "int main(void)\n{\n"
+                   "    fp8_adamw_hparams_t h = {0};\n    fp8_wgrad_err_t e = {0};\n    fp8_stats_t s = {0};\n"
+                   "    (void)h; (void)e; (void)s;\n"
+                   "    return fp8_abi_version() > 0 ? 0 : 1;\n}\n")
+    p = subprocess.run([cc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), "-c", str(src), "-o", str(tmp_path / "use_header.o")],
+                       capture_output=True, text=True)
+    assert p.returncode == 0, p.stderr
