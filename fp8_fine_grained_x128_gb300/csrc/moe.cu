@@ -8,7 +8,9 @@
 // mathematically unchanged.  Here the multiple is 128 (the GEMM's M tile and
 // the 1x128 scale group), the added entries are the lowest-index tokens not
 // already routed to that expert, and the rows of an expert are its tokens in
-// ascending order -- all decided on the device, no host round trip.
+// ascending order -- all decided on the device, no host round trip.  The
+// SwiGLU element math lives in common.cuh, shared with the quantizer that
+// computes SwiGLU while loading, so both give the same BF16 values.
 #include <math.h>
 
 #include <algorithm>

@@ -5,7 +5,9 @@
 //     are quantized dynamically, FP8-RL article "dynamic weight sync").
 //   * the same plus the transposed copy quantized along the token dimension
 //     for the wgrad operand ("grad (transpose)" in the blog's monitor table),
-//     from ONE read of the input.
+//     from ONE read of the input -- also with SwiGLU computed while loading,
+//     so that the MLP's H (forward) and dGU (backward) are quantized without
+//     ever being written in BF16.
 //   * 128x128 weight blocks (FP8-RL article, "dynamic weight sync"), with an
 //     optional transposed copy written in the same pass.
 //   * the on-demand FP8 weight transpose (blog, "FP8 on-demand transpose
@@ -13,8 +15,9 @@
 // Quantization rule ("FP8-LM: Training FP8 Large Language Models", "Tensor
 // scaling"): s = fp32(amax / fmax), q = RNE_satfinite(fp32(x) / s).
 //
-// All of these are HBM-bound streaming kernels: 16-byte vector loads, amax by
-// warp shuffles, coalesced FP8 stores, no tensor-core work.
+// All of these are streaming kernels (HBM-bound, or bound by instruction issue
+// where SwiGLU and the transposed copy add work): 16-byte vector loads, amax
+// by warp shuffles, coalesced FP8 stores, no tensor-core work.
 #include <algorithm>
 
 #include "common.cuh"
