@@ -18,20 +18,25 @@
 //               issues tcgen05.mma kind::f8f6f4 (M=128, N=BN, K=32, 4 per
 //               chunk) from one thread; tcgen05.commit frees the stage and
 //               publishes the accumulator.
-//   warp 2      scale producer: runs up to SD chunks ahead and writes each
-//               chunk's scales into a shared-memory ring -- per row
-//               sA(m,kb)*sB(n-block,kb) for 128x128 B scales, or sA(m,kb) and
-//               the per-column sB(n,kb) -- so the epilogue never waits on a
-//               global load.  (Warp 3 idles.)  This warpgroup gives registers
-//               away (setmaxnreg.dec).
-//   warps 4..11 epilogue, two warpgroups raised to 216 registers: each thread
-//               owns one accumulator row and half of the tile's columns as an
-//               FP32 running sum in registers; per chunk it pulls 64 columns
-//               per wait from tensor memory (two tcgen05.ld 32x32b.x32) and
-//               promotes them with packed fma.rn.f32x2, then stores BF16/FP32
-//               rows at the end of the tile.  The two accumulators alternate
-//               per chunk, so the tensor cores fill one while the epilogue
-//               drains the other.
+//   warp 2      scale producer: runs up to 4 chunks ahead and copies each
+//               chunk's scales into a shared-memory ring -- the tile's row
+//               scales sA(m,kb), and either the two column-half scalars
+//               sB(n-block,kb) (128x128 B) or the per-column sB(n,kb) (1x128
+//               B) -- so the epilogue never waits on a global load.  (Warp 3
+//               idles.)  This warpgroup gives registers away (setmaxnreg.dec).
+//   warps 4..11 epilogue, two warpgroups raised to 176 registers (216 for the
+//               per-column mode): the tile's FP32 running sum lives in their
+//               registers.  With 128x128 B scales each thread owns one row and
+//               half of the columns and drains 16 columns per tcgen05.ld /
+//               wait (32x32b.x16), promoting them with packed fma.rn.f32x2;
+//               with per-column scales each thread owns 4 rows x 32 columns of
+//               16x256b fragments and drains 32 columns of one 16-lane half per
+//               wait (the small rounds keep the staging registers beside the
+//               accumulators).  At the end of a tile BF16 output leaves through
+//               swizzled shared memory and TMA stores (K <= 8192), otherwise
+//               straight from registers.  The two accumulators alternate per
+//               chunk, so the tensor cores fill one while the epilogue drains
+//               the other.
 // Every mbarrier wait is bounded (about 1 s): on a timeout the CTA records
 // FP8_ERR_TIMEOUT, tells the other roles through a shared flag, waits for
 // its own copies and MMAs in flight (bounded again), frees the tensor memory
