@@ -13,6 +13,11 @@
 // from?" and the underflow / distortion monitor table): nonzero, underflow
 // (nonzero -> +-0), saturated (|x/s| > fmax), distinct values in and out per
 // scaling group (+-0 counted once).
+//
+// Per-tensor current scaling (FP8-RL article, "KV cache compression": one
+// scale per cache tensor from its own amax): an amax pass whose last CTA
+// writes s = amax / fmax to device memory, then a quantize pass that reads it
+// -- two launches, no host round trip.
 #include "common.cuh"
 #include "kernels.h"
 
