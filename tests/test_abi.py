@@ -148,3 +148,16 @@ def test_header_is_plain_c(tmp_path):
                         "-I", os.path.join(ROOT, "include"), "-c", str(src), "-o", str(tmp_path / "use_header.o")],
                        capture_output=True, text=True)
     assert p.returncode == 0, p.stderr
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the CUDA library every entry point raises: there is no CPU
+    fallback behind the binding."""
+    monkeypatch.setattr(fg, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(fg, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        fg.lib()
+    import torch
+    x = torch.zeros((128, 128), dtype=torch.bfloat16)
+    with pytest.raises(RuntimeError):
+        fg.quant_1x128(x, fg.E4M3, torch.empty((128, 128), dtype=torch.uint8), torch.empty((1, 128)))
