@@ -635,12 +635,16 @@ __global__ void __launch_bounds__(256) k_stats_blocks(const uint16_t *__restrict
 // scaling factor of the FP8 KV cache is recomputed from the current tensor
 // after every model update).  Pass 1 reduces the tensor's amax and its last
 // CTA writes s = amax / fmax to the device (no host round trip); pass 2
-// quantizes with that s.
+// quantizes with that s.  Pass 2 is a programmatic dependent launch: pass 1
+// lets it be scheduled as soon as every pass-1 CTA is running, and each pass-2
+// thread waits (griddepcontrol.wait: pass 1 complete, its writes visible)
+// before it reads s or x or writes q, so only the launch latency overlaps.
 // ---------------------------------------------------------------------------
 template <int FMT>
 __global__ void __launch_bounds__(256) k_amax_scale(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
                                                     int64_t ldx, float *scale, PtWorkspace *ws, int *status)
 {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ uint32_t red[32];
     __shared__ int is_last;
     const int64_t vpr = cols / 8, nvec = rows * vpr;
@@ -683,6 +687,7 @@ template <int FMT>
 __global__ void __launch_bounds__(256) k_quant_scale(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
                                                      int64_t ldx, const float *scale, uint8_t *__restrict__ q)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const Divider2 d(*scale);
     const int64_t vpr = cols / 8, nvec = rows * vpr;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -820,13 +825,25 @@ int launch_pertensor_current(const void *x, int64_t rows, int64_t cols, int64_t 
     auto X = static_cast<const uint16_t *>(x);
     auto W = static_cast<PtWorkspace *>(ws);
     auto Q = static_cast<uint8_t *>(q);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(bq);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    const float *S = scale;
+    cudaError_t e = cudaSuccess;
     if (fmt == FP8_E5M2) {
         k_amax_scale<FP8_E5M2><<<ba, 256, 0, st>>>(X, rows, cols, ldx, scale, W, status);
-        if (nvec > 0) k_quant_scale<FP8_E5M2><<<bq, 256, 0, st>>>(X, rows, cols, ldx, scale, Q);
+        if (nvec > 0) e = cudaLaunchKernelEx(&cfg, k_quant_scale<FP8_E5M2>, X, rows, cols, ldx, S, Q);
     } else {
         k_amax_scale<FP8_E4M3><<<ba, 256, 0, st>>>(X, rows, cols, ldx, scale, W, status);
-        if (nvec > 0) k_quant_scale<FP8_E4M3><<<bq, 256, 0, st>>>(X, rows, cols, ldx, scale, Q);
+        if (nvec > 0) e = cudaLaunchKernelEx(&cfg, k_quant_scale<FP8_E4M3>, X, rows, cols, ldx, S, Q);
     }
+    if (e != cudaSuccess) return FP8_ERR_CUDA;
     return check_launch();
 }
 
