@@ -7,8 +7,16 @@ PyTorch provides device memory and streams.  There is no fallback: if the
 library is missing or fails to load, every call raises.
 
 BF16 tensors are ``torch.bfloat16`` (or int16/uint16 bit patterns), FP8
-tensors are ``torch.uint8`` code arrays, scales are ``torch.float32``.
+tensors are ``torch.uint8`` code arrays (int8 and torch's float8 types are
+accepted too), scales are ``torch.float32``, index arrays ``torch.int32``.
 Layouts follow the header (1x128 scales are chunk-major ``S[C/128][R]``).
+
+Before a call the binding checks what the C ABI cannot see behind a pointer:
+every tensor is on the current CUDA device and of the element type above;
+a 2-D input passed with a leading dimension has unit column stride; every
+other array is contiguous and at least as large as the header's layout for
+the call's sizes.  A failed check raises ValueError / TypeError before anything
+is launched.  A plain ``int`` is taken as a raw device pointer, unchecked.
 """
 from __future__ import annotations
 
@@ -119,12 +127,69 @@ def status_string(code: int) -> str:
     return lib().fp8_status_string(int(code)).decode()
 
 
-def _p(t):
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16)
+_CODES = (torch.uint8, torch.int8, torch.float8_e4m3fn, torch.float8_e5m2)
+_F32 = (torch.float32,)
+_I32 = (torch.int32,)
+_OUT = (torch.bfloat16, torch.float32)
+
+
+def _on_device(t, name, dtypes):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: expected a CUDA tensor, got one on {t.device}")
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise ValueError(f"{name}: on {t.device}, but the current device is cuda:{cur}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected one of {tuple(str(d) for d in dtypes)}")
+
+
+def _buf(t, name, dtypes, numel, optional=False):
+    """Device pointer of an array the library reads or writes as `numel`
+    contiguous elements."""
     if t is None:
-        return None
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
     if isinstance(t, int):
         return t
+    _on_device(t, name, dtypes)
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: holds {t.numel()} elements, the call needs {numel}")
     return t.data_ptr()
+
+
+def _mat(t, name, dtypes):
+    """(pointer, rows, cols, leading dimension) of a row-major 2-D view."""
+    _on_device(t, name, dtypes)
+    if t.dim() != 2:
+        raise ValueError(f"{name}: expected a 2-D tensor, got shape {tuple(t.shape)}")
+    R, C = t.shape
+    if C > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name}: columns must be contiguous (stride {t.stride(1)})")
+    ld = t.stride(0) if R > 1 else C
+    return t.data_ptr(), R, C, ld
+
+
+def _shape(t, name, dims):
+    if isinstance(t, torch.Tensor) and t.dim() != dims:
+        raise ValueError(f"{name}: expected a {dims}-D tensor, got shape {tuple(t.shape)}")
+    return tuple(t.shape)
+
+
+def _gran_scales(gran, rows, cols):
+    """Element count of the scale array of a [rows][cols] operand (header layouts)."""
+    if gran == GRAN_1x128:
+        return (cols // 128) * rows
+    if gran == GRAN_128x128:
+        return (rows // 128) * (cols // 128)
+    if gran == GRAN_128x1:
+        return (rows // 128) * cols
+    return 1
 
 
 def _stream(stream=None):
@@ -136,11 +201,6 @@ def _stream(stream=None):
 def _check(name: str, rc: int) -> None:
     if rc != OK:
         raise Fp8Error(name, rc)
-
-
-def _rows_cols(t):
-    assert t.dim() == 2, "expected a 2-D tensor"
-    return t.shape[0], t.shape[1], t.stride(0)
 
 
 # ------------------------------------------------------------------ utility
@@ -174,37 +234,55 @@ def new_stats(device="cuda") -> torch.Tensor:
 # ------------------------------------------------------------------ quantizers
 
 def quant_1x128(x, fmt, q, s, qT=None, sT=None, stream=None):
-    R, C, ld = _rows_cols(x)
-    _check("fp8_quant_1x128", lib().fp8_quant_1x128(_p(x), R, C, ld, fmt, _p(q), _p(s), _p(qT), _p(sT),
-                                                    _stream(stream)))
+    L = lib()
+    px, R, C, ld = _mat(x, "x", _BF16)
+    args = (_buf(q, "q", _CODES, R * C), _buf(s, "s", _F32, (C // 128) * R),
+            _buf(qT, "qT", _CODES, C * R, True), _buf(sT, "sT", _F32, (R // 128) * C, True))
+    _check("fp8_quant_1x128", L.fp8_quant_1x128(px, R, C, ld, fmt, *args, _stream(stream)))
 
 
 def quant_128x128(w, fmt, q, s, qT=None, sT=None, stream=None):
-    R, C, ld = _rows_cols(w)
-    _check("fp8_quant_128x128", lib().fp8_quant_128x128(_p(w), R, C, ld, fmt, _p(q), _p(s), _p(qT),
-                                                        _p(sT), _stream(stream)))
+    L = lib()
+    pw, R, C, ld = _mat(w, "w", _BF16)
+    nb = (R // 128) * (C // 128)
+    args = (_buf(q, "q", _CODES, R * C), _buf(s, "s", _F32, nb),
+            _buf(qT, "qT", _CODES, C * R, True), _buf(sT, "sT", _F32, nb, True))
+    _check("fp8_quant_128x128", L.fp8_quant_128x128(pw, R, C, ld, fmt, *args, _stream(stream)))
 
 
 def transpose_128x128(q, s, qT, sT, stream=None):
-    R, C = q.shape
-    _check("fp8_transpose_128x128", lib().fp8_transpose_128x128(_p(q), _p(s), R, C, _p(qT), _p(sT),
-                                                                _stream(stream)))
+    L = lib()
+    R, C = _shape(q, "q", 2)
+    nb = (R // 128) * (C // 128)
+    args = (_buf(q, "q", _CODES, R * C), _buf(s, "s", _F32, nb), R, C,
+            _buf(qT, "qT", _CODES, C * R), _buf(sT, "sT", _F32, nb))
+    _check("fp8_transpose_128x128", L.fp8_transpose_128x128(*args, _stream(stream)))
 
 
 def transpose_128x128_batched(q, s, qT, sT, stream=None):
     """q [B, R, C] codes with scales [B, R/128, C/128] -> qT [B, C, R], sT [B, C/128, R/128]."""
-    B, R, C = q.shape
-    _check("fp8_transpose_128x128_batched",
-           lib().fp8_transpose_128x128_batched(_p(q), _p(s), B, R, C, _p(qT), _p(sT), _stream(stream)))
+    L = lib()
+    B, R, C = _shape(q, "q", 3)
+    nb = B * (R // 128) * (C // 128)
+    args = (_buf(q, "q", _CODES, B * R * C), _buf(s, "s", _F32, nb), B, R, C,
+            _buf(qT, "qT", _CODES, B * C * R), _buf(sT, "sT", _F32, nb))
+    _check("fp8_transpose_128x128_batched", L.fp8_transpose_128x128_batched(*args, _stream(stream)))
+
+
+def _delayed_state(recipe, hist, step, scale, R, C, q, qT, stats):
+    return (_buf(hist, "amax_history", _F32, max(int(recipe.history_len), 1)), _buf(step, "step", _I32, 1),
+            _buf(scale, "scale", _F32, 1), _buf(q, "q", _CODES, R * C), _buf(qT, "qT", _CODES, C * R, True),
+            _buf(stats, "stats", (torch.int64,), 5, True))
 
 
 def quant_pertensor_delayed(x, recipe: DelayedRecipe, hist, step, scale, q, workspace, qT=None,
                             stats=None, stream=None):
-    R, C, ld = _rows_cols(x)
+    L = lib()
+    px, R, C, ld = _mat(x, "x", _BF16)
+    st = _delayed_state(recipe, hist, step, scale, R, C, q, qT, stats)
+    ws = _buf(workspace, "workspace", (torch.uint8,), workspace_bytes())
     _check("fp8_quant_pertensor_delayed",
-           lib().fp8_quant_pertensor_delayed(_p(x), R, C, ld, ctypes.byref(recipe), _p(hist), _p(step),
-                                             _p(scale), _p(q), _p(qT), _p(stats), _p(workspace),
-                                             _stream(stream)))
+           L.fp8_quant_pertensor_delayed(px, R, C, ld, ctypes.byref(recipe), *st, ws, _stream(stream)))
 
 
 def quant_pertensor_delayed_noalloc(x, recipe: DelayedRecipe, hist, step, scale, q, qT=None, stats=None,
@@ -212,55 +290,83 @@ def quant_pertensor_delayed_noalloc(x, recipe: DelayedRecipe, hist, step, scale,
     """The delayed-scaling step without a caller workspace, for callers that
     cannot allocate device memory (the library's own scratch block is used;
     calls that overlap on the GPU race on it)."""
-    R, C, ld = _rows_cols(x)
+    L = lib()
+    px, R, C, ld = _mat(x, "x", _BF16)
+    st = _delayed_state(recipe, hist, step, scale, R, C, q, qT, stats)
     _check("fp8_quant_pertensor_delayed_noalloc",
-           lib().fp8_quant_pertensor_delayed_noalloc(_p(x), R, C, ld, ctypes.byref(recipe), _p(hist), _p(step),
-                                                     _p(scale), _p(q), _p(qT), _p(stats), _stream(stream)))
+           L.fp8_quant_pertensor_delayed_noalloc(px, R, C, ld, ctypes.byref(recipe), *st, _stream(stream)))
 
 
 def quant_pertensor_current(x, fmt, scale, q, workspace, stream=None):
     """Per-tensor current scaling: scale (device float[1]) = amax / fmax of x, q = codes."""
-    R, C, ld = _rows_cols(x)
-    _check("fp8_quant_pertensor_current",
-           lib().fp8_quant_pertensor_current(_p(x), R, C, ld, fmt, _p(scale), _p(q), _p(workspace),
-                                             _stream(stream)))
+    L = lib()
+    px, R, C, ld = _mat(x, "x", _BF16)
+    args = (_buf(scale, "scale", _F32, 1), _buf(q, "q", _CODES, R * C),
+            _buf(workspace, "workspace", (torch.uint8,), workspace_bytes()))
+    _check("fp8_quant_pertensor_current", L.fp8_quant_pertensor_current(px, R, C, ld, fmt, *args, _stream(stream)))
 
 
 def quant_stats(x, q, s, gran, fmt, stats, workspace=None, stream=None):
-    R, C, ld = _rows_cols(x)
-    _check("fp8_quant_stats", lib().fp8_quant_stats(_p(x), R, C, ld, _p(q), _p(s), gran, fmt, _p(stats),
-                                                    _p(workspace), _stream(stream)))
+    L = lib()
+    px, R, C, ld = _mat(x, "x", _BF16)
+    args = (_buf(q, "q", _CODES, R * C), _buf(s, "s", _F32, _gran_scales(gran, R, C)), gran, fmt,
+            _buf(stats, "stats", (torch.int64,), 5),
+            _buf(workspace, "workspace", (torch.uint8,), workspace_bytes(), True))
+    _check("fp8_quant_stats", L.fp8_quant_stats(px, R, C, ld, *args, _stream(stream)))
 
 
 # ------------------------------------------------------------------ GEMMs
 
+def _out_mat(D, rows, cols):
+    pd, R, C, ld = _mat(D, "D", _OUT)
+    if R < rows or C < cols:
+        raise ValueError(f"D: shape {(R, C)}, the call writes [{rows}][{cols}]")
+    return pd, (OUT_F32 if D.dtype == torch.float32 else OUT_BF16), ld
+
+
 def blockscaled_gemm(A, fmtA, sA, granA, B, fmtB, sB, granB, D, stream=None):
-    M, K = A.shape
-    N = B.shape[0]
-    out = OUT_F32 if D.dtype == torch.float32 else OUT_BF16
+    L = lib()
+    M, K = _shape(A, "A", 2)
+    N, KB = _shape(B, "B", 2)
+    if KB != K:
+        raise ValueError(f"B: shape {(N, KB)}, expected [N][{K}]")
+    pA, pB = _buf(A, "A", _CODES, M * K), _buf(B, "B", _CODES, N * K)
+    psA = _buf(sA, "sA", _F32, _gran_scales(granA, M, K))
+    psB = _buf(sB, "sB", _F32, _gran_scales(granB, N, K))
+    pD, out, ldD = _out_mat(D, M, N)
     _check("fp8_blockscaled_gemm",
-           lib().fp8_blockscaled_gemm(M, N, K, _p(A), fmtA, _p(sA), granA, _p(B), fmtB, _p(sB), granB,
-                                      _p(D), out, D.stride(0), _stream(stream)))
+           L.fp8_blockscaled_gemm(M, N, K, pA, fmtA, psA, granA, pB, fmtB, psB, granB, pD, out, ldD,
+                                  _stream(stream)))
 
 
 def grouped_gemm(offsets, A, sA, B, sB, D, stream=None):
-    G, N, K = B.shape
-    Mcap = A.shape[0]
-    out = OUT_F32 if D.dtype == torch.float32 else OUT_BF16
-    _check("fp8_grouped_gemm",
-           lib().fp8_grouped_gemm(G, _p(offsets), Mcap, N, K, _p(A), _p(sA), _p(B), _p(sB), _p(D), out,
-                                  D.stride(0), _stream(stream)))
+    L = lib()
+    G, N, K = _shape(B, "B", 3)
+    Mcap, KA = _shape(A, "A", 2)
+    if KA != K:
+        raise ValueError(f"A: shape {(Mcap, KA)}, expected [M_capacity][{K}]")
+    args = (_buf(offsets, "offsets", _I32, G + 1), Mcap, N, K, _buf(A, "A", _CODES, Mcap * K),
+            _buf(sA, "sA", _F32, (K // 128) * Mcap), _buf(B, "B", _CODES, G * N * K),
+            _buf(sB, "sB", _F32, G * (N // 128) * (K // 128)))
+    pD, out, ldD = _out_mat(D, Mcap, N)
+    _check("fp8_grouped_gemm", L.fp8_grouped_gemm(G, *args, pD, out, ldD, _stream(stream)))
 
 
 def grouped_gemm_wgrad(offsets, AT, fmtA, sAT, BT, fmtB, sBT, D, stream=None):
     """D [G*N, ldD]: expert g's AT[:, rows_g] . BT[:, rows_g]^T (transposed copies, 1x128 scales)."""
+    L = lib()
+    if not isinstance(offsets, torch.Tensor):
+        raise TypeError("offsets: expected a torch.Tensor (its length gives the number of experts)")
     G = offsets.numel() - 1
-    N, Mcap = AT.shape
-    K = BT.shape[0]
-    out = OUT_F32 if D.dtype == torch.float32 else OUT_BF16
-    _check("fp8_grouped_gemm_wgrad",
-           lib().fp8_grouped_gemm_wgrad(G, _p(offsets), Mcap, N, K, _p(AT), fmtA, _p(sAT), _p(BT), fmtB, _p(sBT),
-                                        _p(D), out, D.stride(0), _stream(stream)))
+    N, Mcap = _shape(AT, "AT", 2)
+    K, MB = _shape(BT, "BT", 2)
+    if MB != Mcap:
+        raise ValueError(f"BT: shape {(K, MB)}, expected [K][{Mcap}]")
+    args = (_buf(offsets, "offsets", _I32, G + 1), Mcap, N, K, _buf(AT, "AT", _CODES, N * Mcap), fmtA,
+            _buf(sAT, "sAT", _F32, (Mcap // 128) * N), _buf(BT, "BT", _CODES, K * Mcap), fmtB,
+            _buf(sBT, "sBT", _F32, (Mcap // 128) * K))
+    pD, out, ldD = _out_mat(D, max(G, 0) * N, K)
+    _check("fp8_grouped_gemm_wgrad", L.fp8_grouped_gemm_wgrad(G, *args, pD, out, ldD, _stream(stream)))
 
 
 # ------------------------------------------------------------------ high-precision dw monitor
@@ -268,11 +374,18 @@ def grouped_gemm_wgrad(offsets, AT, fmtA, sAT, BT, fmtB, sBT, D, stream=None):
 def wgrad_recompute_error(dY, X, D, ref_workspace, err, stream=None):
     """err (device float64[3] view of fp8_wgrad_err_t: see new_wgrad_err) <- statistics of the FP8
     wgrad D [N, K] against R = dY^T . X recomputed from the BF16 operands into ref_workspace."""
-    M, N = dY.shape
-    K = X.shape[1]
-    _check("fp8_wgrad_recompute_error",
-           lib().fp8_wgrad_recompute_error(M, N, K, _p(dY), _p(X), _p(D), D.stride(0), _p(ref_workspace), _p(err),
-                                           _stream(stream)))
+    L = lib()
+    M, N = _shape(dY, "dY", 2)
+    MX, K = _shape(X, "X", 2)
+    if MX != M:
+        raise ValueError(f"X: shape {(MX, K)}, expected [{M}][K]")
+    pdY, pX = _buf(dY, "dY", _BF16, M * N), _buf(X, "X", _BF16, M * K)
+    pD, R, C, ldD = _mat(D, "D", _F32)
+    if R < N or C < K:
+        raise ValueError(f"D: shape {(R, C)}, expected at least [{N}][{K}]")
+    args = (pdY, pX, pD, ldD, _buf(ref_workspace, "ref_workspace", _F32, N * K),
+            _buf(err, "err", (torch.float64,), 3))
+    _check("fp8_wgrad_recompute_error", L.fp8_wgrad_recompute_error(M, N, K, *args, _stream(stream)))
 
 
 def new_wgrad_err(device="cuda") -> torch.Tensor:
@@ -298,47 +411,75 @@ def adamw_hparams(lr, beta1, beta2, eps, weight_decay, step) -> AdamWHparams:
 def adamw_step_fp8_states(param, grad, m, m_scales, v, v_scales, hparams: AdamWHparams, stream=None):
     """In place: FP32 ``param`` [n], BF16 ``grad`` [n], E4M3 ``m`` / E5M2 ``v`` codes [n] with
     scales [n/128]."""
-    _check("fp8_adamw_step_fp8_states",
-           lib().fp8_adamw_step_fp8_states(_p(param), _p(grad), _p(m), _p(m_scales), _p(v), _p(v_scales),
-                                           param.numel(), ctypes.byref(hparams), _stream(stream)))
+    L = lib()
+    if not isinstance(param, torch.Tensor):
+        raise TypeError("param: expected a torch.Tensor (its size gives n)")
+    n = param.numel()
+    args = (_buf(param, "param", _F32, n), _buf(grad, "grad", _BF16, n), _buf(m, "m", _CODES, n),
+            _buf(m_scales, "m_scales", _F32, n // 128), _buf(v, "v", _CODES, n),
+            _buf(v_scales, "v_scales", _F32, n // 128))
+    _check("fp8_adamw_step_fp8_states", L.fp8_adamw_step_fp8_states(*args, n, ctypes.byref(hparams),
+                                                                    _stream(stream)))
 
 
 # ------------------------------------------------------------------ MoE glue
 
 def moe_route_pad(logits, topk, align, Mcap, topk_idx, topk_prob, counts, offsets, row_token,
                   row_prob, row_is_pad=None, stream=None):
-    T, E = logits.shape
-    _check("fp8_moe_route_pad",
-           lib().fp8_moe_route_pad(_p(logits), T, E, topk, align, Mcap, _p(topk_idx), _p(topk_prob),
-                                   _p(counts), _p(offsets), _p(row_token), _p(row_prob),
-                                   _p(row_is_pad), _stream(stream)))
+    L = lib()
+    T, E = _shape(logits, "logits", 2)
+    args = (_buf(logits, "logits", _F32, T * E), T, E, topk, align, Mcap,
+            _buf(topk_idx, "topk_idx", _I32, T * topk), _buf(topk_prob, "topk_prob", _F32, T * topk),
+            _buf(counts, "counts", _I32, E), _buf(offsets, "offsets", _I32, E + 1),
+            _buf(row_token, "row_token", _I32, Mcap), _buf(row_prob, "row_prob", _F32, Mcap),
+            _buf(row_is_pad, "row_is_pad", (torch.uint8, torch.bool), Mcap, True))
+    _check("fp8_moe_route_pad", L.fp8_moe_route_pad(*args, _stream(stream)))
 
 
 def moe_gather(q, s, row_token, offsets, E, Mcap, qg, sg, stream=None):
-    T, K = q.shape
-    _check("fp8_moe_gather", lib().fp8_moe_gather(_p(q), _p(s), T, K, _p(row_token), _p(offsets), E,
-                                                  Mcap, _p(qg), _p(sg), _stream(stream)))
+    L = lib()
+    T, K = _shape(q, "q", 2)
+    args = (_buf(q, "q", _CODES, T * K), _buf(s, "s", _F32, (K // 128) * T), T, K,
+            _buf(row_token, "row_token", _I32, Mcap), _buf(offsets, "offsets", _I32, E + 1), E, Mcap,
+            _buf(qg, "qg", _CODES, Mcap * K), _buf(sg, "sg", _F32, (K // 128) * Mcap))
+    _check("fp8_moe_gather", L.fp8_moe_gather(*args, _stream(stream)))
+
+
+def _gu(gu):
+    R, F2 = _shape(gu, "gu", 2)
+    return _buf(gu, "gu", _BF16, R * F2), R, F2 // 2
 
 
 def swiglu_fwd(gu, h, stream=None):
-    R, F2 = gu.shape
-    _check("fp8_swiglu_fwd", lib().fp8_swiglu_fwd(_p(gu), R, F2 // 2, _p(h), _stream(stream)))
+    L = lib()
+    pg, R, F = _gu(gu)
+    _check("fp8_swiglu_fwd", L.fp8_swiglu_fwd(pg, R, F, _buf(h, "h", _BF16, R * F), _stream(stream)))
 
 
 def swiglu_bwd(gu, dh, dgu, stream=None):
-    R, F2 = gu.shape
-    _check("fp8_swiglu_bwd", lib().fp8_swiglu_bwd(_p(gu), _p(dh), R, F2 // 2, _p(dgu), _stream(stream)))
+    L = lib()
+    pg, R, F = _gu(gu)
+    args = (_buf(dh, "dh", _BF16, R * F), R, F, _buf(dgu, "dgu", _BF16, R * 2 * F))
+    _check("fp8_swiglu_bwd", L.fp8_swiglu_bwd(pg, *args, _stream(stream)))
+
+
+def _quant_outs(q, s, qT, sT, R, C):
+    return (_buf(q, "q", _CODES, R * C), _buf(s, "s", _F32, (C // 128) * R), _buf(qT, "qT", _CODES, C * R),
+            _buf(sT, "sT", _F32, (R // 128) * C))
 
 
 def swiglu_quant_fwd(gu, fmt, q, s, qT, sT, stream=None):
     """H = SwiGLU(gu) quantized 1x128 (q [R, F], s [F/128, R]) and 128x1 (qT [F, R], sT [R/128, F])."""
-    R, F2 = gu.shape
-    _check("fp8_swiglu_quant_fwd", lib().fp8_swiglu_quant_fwd(_p(gu), R, F2 // 2, fmt, _p(q), _p(s), _p(qT),
-                                                              _p(sT), _stream(stream)))
+    L = lib()
+    pg, R, F = _gu(gu)
+    _check("fp8_swiglu_quant_fwd", L.fp8_swiglu_quant_fwd(pg, R, F, fmt, *_quant_outs(q, s, qT, sT, R, F),
+                                                          _stream(stream)))
 
 
 def swiglu_bwd_quant(gu, dh, fmt, q, s, qT, sT, stream=None):
     """dGU = SwiGLU'(gu) . dh quantized 1x128 (q [R, 2F], s [2F/128, R]) and 128x1 (qT [2F, R], sT [R/128, 2F])."""
-    R, F2 = gu.shape
-    _check("fp8_swiglu_bwd_quant", lib().fp8_swiglu_bwd_quant(_p(gu), _p(dh), R, F2 // 2, fmt, _p(q), _p(s),
-                                                              _p(qT), _p(sT), _stream(stream)))
+    L = lib()
+    pg, R, F = _gu(gu)
+    pdh = _buf(dh, "dh", _BF16, R * F)
+    _check("fp8_swiglu_bwd_quant", L.fp8_swiglu_bwd_quant(pg, pdh, R, F, fmt, *_quant_outs(q, s, qT, sT, R, 2 * F),
+                                                          _stream(stream)))

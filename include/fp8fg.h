@@ -247,7 +247,9 @@ FP8FG_API int fp8_quant_stats(const void *x, int64_t rows, int64_t cols, int64_t
  *   TENSOR must be used on both sides or neither.
  *   fmtA/fmtB: E4M3 or E5M2, mixed allowed (HYBRID dgrad/wgrad).
  *   D [M][ldD], BF16 (round to nearest even) or FP32.
- * M % 128 == 0, N % 128 == 0, K % 128 == 0; M, N, K >= 0 (0 = no-op). */
+ * M % 128 == 0, N % 128 == 0, K % 128 == 0; M, N, K >= 0.  M == 0 or N == 0
+ * is a no-op; K == 0 writes D[M][N] = 0 (the empty sum; A, B and the scales
+ * may then be NULL). */
 FP8FG_API int fp8_blockscaled_gemm(int64_t M, int64_t N, int64_t K,
                                    const void *A, int fmtA, const float *sA, int granA,
                                    const void *B, int fmtB, const float *sB, int granB,
@@ -262,7 +264,8 @@ FP8FG_API int fp8_blockscaled_gemm(int64_t M, int64_t N, int64_t K,
  * A [M_capacity][K] E4M3 with 1x128 scales S[K/128][M_capacity];
  * B [G][N][K] E4M3 with scales [G][N/128][K/128]; D [M_capacity][ldD]
  * (rows >= off[G] are not written).  N % 128 == 0, K % 128 == 0,
- * M_capacity % 128 == 0, 1 <= G <= 1024. */
+ * M_capacity % 128 == 0, 1 <= G <= 1024.  M_capacity, N or K == 0 is a
+ * no-op: D is not written. */
 FP8FG_API int fp8_grouped_gemm(int G, const int32_t *group_offsets, int64_t M_capacity,
                                int64_t N, int64_t K, const void *A, const float *sA,
                                const void *B, const float *sB, void *D, int out_dtype,

@@ -161,3 +161,25 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     x = torch.zeros((128, 128), dtype=torch.bfloat16)
     with pytest.raises(RuntimeError):
         fg.quant_1x128(x, fg.E4M3, torch.empty((128, 128), dtype=torch.uint8), torch.empty((1, 128)))
+
+
+def test_binding_refuses_host_memory():
+    """The binding checks what the C ABI cannot: a host tensor's address
+    would reach a kernel as a device pointer, so it is refused (ValueError)
+    before anything is launched; so is a non-tensor where a tensor's shape is
+    needed (TypeError)."""
+    import torch
+    fg.lib()
+    x = torch.zeros((128, 128), dtype=torch.bfloat16)
+    q, s = torch.empty((128, 128), dtype=torch.uint8), torch.empty((1, 128))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fg.quant_1x128(x, fg.E4M3, q, s)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fg.swiglu_fwd(torch.zeros((128, 256), dtype=torch.bfloat16), x)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fg.blockscaled_gemm(q, fg.E4M3, s, fg.GRAN_1x128, q, fg.E4M3, s, fg.GRAN_1x128,
+                            torch.empty((128, 128), dtype=torch.bfloat16))
+    with pytest.raises(TypeError, match="torch.Tensor"):
+        fg.grouped_gemm_wgrad([0, 128], q, fg.E4M3, s, q, fg.E4M3, s, x)
+    with pytest.raises(TypeError, match="torch.Tensor"):
+        fg.adamw_step_fp8_states(None, None, None, None, None, None, fg.adamw_hparams(1e-3, 0.9, 0.95, 1e-8, 0, 1))
