@@ -639,7 +639,64 @@ __global__ void __launch_bounds__(256) k_stats_blocks(const uint16_t *__restrict
 // lets it be scheduled as soon as every pass-1 CTA is running, and each pass-2
 // thread waits (griddepcontrol.wait: pass 1 complete, its writes visible)
 // before it reads s or x or writes q, so only the launch latency overlaps.
+//
+// Pass 2 re-reads x, which pass 1 has just brought through L2 (129 MB).  With
+// plain streaming loads much of a 64 MB tensor is evicted before pass 2 gets
+// to it; pass 1 therefore loads with an L2 evict_last policy, and pass 2, as it
+// consumes each 128-byte line, puts the line back to normal priority
+// (applypriority), so nothing stays pinned for the kernels that follow.  This
+// is done only when x is contiguous and 128-byte aligned: then every line
+// pass 1 marks starts at one of pass 2's vectors and is reset.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ bool keep_in_l2(const uint16_t *x, int64_t cols, int64_t ldx)
+{
+    return ldx == cols && (reinterpret_cast<uintptr_t>(x) & 127u) == 0;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint4 ldg_stream_policy(const void *ptr, uint64_t policy)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr), "l"(policy));
+    return v;
+}
+
+// Back to normal eviction priority for the line that starts at p (no-op for a
+// p inside a line).
+__device__ __forceinline__ void l2_priority_normal(const void *p)
+{
+    if ((reinterpret_cast<uintptr_t>(p) & 127u) == 0)
+        asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(p) : "memory");
+}
+
+// Amax of the contiguous vectors [0, nvec) of x, grid-strided, U loads in flight.
+template <bool KEEP>
+__device__ __forceinline__ uint32_t amax_flat(const uint16_t *__restrict__ x, int64_t nvec, int64_t stride)
+{
+    constexpr int U = 8;
+    const uint64_t pol = KEEP ? l2_policy_evict_last() : 0;
+    auto load = [&](int64_t i) { return KEEP ? ldg_stream_policy(x + i * 8, pol) : ldg_stream(x + i * 8); };
+    uint32_t m = 0;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + (U - 1) * stride < nvec; i += U * stride) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = load(i + u * stride);
+#pragma unroll
+        for (int u = 0; u < U; ++u) m = max(m, absmax8(v[u]));
+    }
+    for (; i < nvec; i += stride) m = max(m, absmax8(load(i)));
+    return m;
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(256) k_amax_scale(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
                                                     int64_t ldx, float *scale, PtWorkspace *ws, int *status)
@@ -650,17 +707,10 @@ __global__ void __launch_bounds__(256) k_amax_scale(const uint16_t *__restrict__
     const int64_t vpr = cols / 8, nvec = rows * vpr;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     uint32_t m = 0;
-    if (ldx == cols) {   // contiguous: flat 16-byte vectors, eight loads in flight
-        constexpr int U = 8;
-        int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-        for (; i + (U - 1) * stride < nvec; i += U * stride) {
-            uint4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) v[u] = ldg_stream(x + (i + u * stride) * 8);
-#pragma unroll
-            for (int u = 0; u < U; ++u) m = max(m, absmax8(v[u]));
-        }
-        for (; i < nvec; i += stride) m = max(m, absmax8(ldg_stream(x + i * 8)));
+    if (keep_in_l2(x, cols, ldx)) {
+        m = amax_flat<true>(x, nvec, stride);
+    } else if (ldx == cols) {
+        m = amax_flat<false>(x, nvec, stride);
     } else {
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
             const int64_t r = i / vpr, c = (i - r * vpr) * 8;
@@ -692,17 +742,24 @@ __global__ void __launch_bounds__(256) k_quant_scale(const uint16_t *__restrict_
     const int64_t vpr = cols / 8, nvec = rows * vpr;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     if (ldx == cols) {   // contiguous: flat 16-byte vectors, four loads in flight
+        const bool keep = keep_in_l2(x, cols, ldx);
         constexpr int U = 4;
         int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
         for (; i + (U - 1) * stride < nvec; i += U * stride) {
             uint4 v[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) v[u] = ldg_stream(x + (i + u * stride) * 8);
+            if (keep) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) l2_priority_normal(x + (i + u * stride) * 8);
+            }
 #pragma unroll
             for (int u = 0; u < U; ++u) *reinterpret_cast<uint2 *>(q + (i + u * stride) * 8) = quant8p<FMT>(v[u], d);
         }
-        for (; i < nvec; i += stride)
+        for (; i < nvec; i += stride) {
             *reinterpret_cast<uint2 *>(q + i * 8) = quant8p<FMT>(ldg_stream(x + i * 8), d);
+            if (keep) l2_priority_normal(x + i * 8);
+        }
     } else {
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
             const int64_t r = i / vpr, c = (i - r * vpr) * 8;

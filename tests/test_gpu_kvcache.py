@@ -65,3 +65,24 @@ def test_kv_cache_layer_full_size():
     assert_status_ok()
     rq, rs, _ = oracle.quant_pertensor_current(xb)
     assert np.array_equal(q.cpu().numpy(), rq) and np.float32(scale.item()) == np.float32(rs)
+
+
+@pytest.mark.parametrize("offset", [0, 8, 24])
+def test_alignment_paths_agree(offset):
+    """A contiguous tensor that starts on a 128-byte line is read with an L2
+    evict_last policy in pass 1 and reset line by line in pass 2; one that is
+    only 16-byte aligned (offset 8 or 24 BF16 elements) is read plainly.  Both
+    give the oracle's codes and scale."""
+    R, C = 1536, 640
+    ws = fg.new_workspace()
+    xb = synth.bf16_normal((R, C), 65 + offset, 2.0, 1e-3, 30.0)
+    flat = torch.zeros(R * C + 128, dtype=torch.int16, device="cuda")
+    flat[offset:offset + R * C] = torch.from_numpy(xb.reshape(-1).view(np.int16)).cuda()
+    x = flat[offset:offset + R * C].view(torch.bfloat16).view(R, C)
+    assert (x.data_ptr() % 128 == 0) == (offset == 0)
+    scale = torch.full((1,), float("nan"), device="cuda")
+    q = torch.empty((R, C), dtype=torch.uint8, device="cuda")
+    fg.quant_pertensor_current(x, fg.E4M3, scale, q, ws)
+    assert_status_ok()
+    rq, rs, _ = oracle.quant_pertensor_current(xb)
+    assert np.array_equal(q.cpu().numpy(), rq) and np.float32(scale.item()) == np.float32(rs)
