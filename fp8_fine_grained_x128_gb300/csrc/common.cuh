@@ -315,19 +315,9 @@ __device__ __forceinline__ uint32_t cvt2(float lo, float hi)
     return (uint32_t)r;
 }
 
-// Quantize 8 BF16 values (a uint4) with one divider; returns 8 codes in a uint2.
-template <int FMT>
-__device__ __forceinline__ uint2 quant8(uint4 v, const Divider &d)
-{
-    uint2 out;
-    out.x = cvt2<FMT>(d(bf16_lo(v.x)), d(bf16_hi(v.x))) | (cvt2<FMT>(d(bf16_lo(v.y)), d(bf16_hi(v.y))) << 16);
-    out.y = cvt2<FMT>(d(bf16_lo(v.z)), d(bf16_hi(v.z))) | (cvt2<FMT>(d(bf16_lo(v.w)), d(bf16_hi(v.w))) << 16);
-    return out;
-}
-
-// Same with the packed divider.  The fast path is inlined; a scale outside
-// its range (rare: an all-tiny or non-finite group) takes one out-of-line
-// call for the whole group, which keeps the unrolled loops small.
+// Quantize BF16 values with the packed divider.  The fast path is inlined; a
+// scale outside its range (rare: an all-tiny or non-finite group) takes one
+// out-of-line call for the whole group, which keeps the unrolled loops small.
 template <int FMT>
 __device__ __forceinline__ uint32_t quant4p_fast(uint32_t w0, uint32_t w1, const Divider2 &d)
 {
@@ -395,11 +385,6 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 __device__ __forceinline__ void fence_barrier_init()
 {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_shared()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
