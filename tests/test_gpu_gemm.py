@@ -89,6 +89,21 @@ def test_gemm_qkv_fprop_full_size_sampled():
     gemm_tolerance_check(got, ref, bf16_out=True)
 
 
+@pytest.mark.parametrize("fa", [oracle.E4M3, oracle.E5M2], ids=["e4m3", "hybrid_e5m2"])
+def test_gemm_pertensor_full_size_sampled(fa):
+    """Per-tensor scaling at its benchmarked size: X [16384,4096] (E4M3, or
+    E5M2 for the HYBRID gradient side) x W [4096,4096] E4M3, whole-K
+    accumulation on the tensor cores and one scale product, BF16 out."""
+    M, N, K = 16384, 4096, 4096
+    qa, sa = quantized_operand(M, K, 31, oracle.GRAN_TENSOR, fa)
+    qb, sb = quantized_operand(N, K, 32, oracle.GRAN_TENSOR, oracle.E4M3, std=0.02)
+    D = run_gemm(qa, fa, sa, oracle.GRAN_TENSOR, qb, oracle.E4M3, sb, oracle.GRAN_TENSOR, torch.bfloat16)
+    pm, pn = sample_points(M, N, 1 << 15, seed=3)
+    ref = oracle.gemm_points(qa, fa, sa, oracle.GRAN_TENSOR, qb, oracle.E4M3, sb, oracle.GRAN_TENSOR, pm, pn)
+    got = bf16_to_f64(host_u16(D))[pm, pn]
+    gemm_tolerance_check(got, ref, bf16_out=True)
+
+
 def test_gemm_k_zero_gives_zeros_and_empty_is_no_op():
     D = torch.full((256, 256), 7.0, dtype=torch.float32, device="cuda")
     z = torch.empty(0, dtype=torch.uint8, device="cuda")
