@@ -65,3 +65,34 @@ def test_no_rows_gives_zero_reference():
     D = torch.ones((N, K), dtype=torch.float32, device="cuda")
     (sdd, srr, mdd, mrr), R = monitor(np.zeros((0, N), np.uint16), np.zeros((0, K), np.uint16), D)
     assert srr == 0.0 and mrr == 0.0 and sdd == float(N * K) and mdd == 1.0
+
+
+def test_full_size_exact_properties():
+    """The benchmarked size: dW_down [4096, 14336] recomputed over 8192 tokens.
+    Small-integer operands make every product and partial sum exact in FP32
+    (|R| <= 8192 * 64 < 2^24), so R is the integer matmul whatever the GEMM's
+    reduction order: sampled entries equal int64 dot products, D = 0 gives
+    sum (D-R)^2 = sum R^2 and max|D-R| = max|R|, and D = R gives zero error."""
+    M, N, K = 8192, 4096, 14336
+    g = torch.Generator(device="cuda").manual_seed(11)
+    dy = torch.randint(-8, 9, (M, N), generator=g, device="cuda").to(torch.bfloat16)
+    x = torch.randint(-8, 9, (M, K), generator=g, device="cuda").to(torch.bfloat16)
+    R = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    D = torch.zeros((N, K), dtype=torch.float32, device="cuda")
+    err = fg.new_wgrad_err()
+    fg.wgrad_recompute_error(dy, x, D, R, err)
+    assert_status_ok()
+    sdd, srr, mdd, mrr = fg.wgrad_err_values(err)
+    assert srr > 0 and abs(sdd - srr) <= 1e-12 * srr and mdd == mrr
+    rng = np.random.default_rng(12)
+    pn, pk = rng.integers(0, N, 4096), rng.integers(0, K, 4096)
+    dyc = dy[:, torch.from_numpy(pn).cuda()].float().cpu().numpy().astype(np.int64)
+    xc = x[:, torch.from_numpy(pk).cuda()].float().cpu().numpy().astype(np.int64)
+    want = (dyc * xc).sum(axis=0)
+    got = R[torch.from_numpy(pn).cuda(), torch.from_numpy(pk).cuda()].cpu().numpy()
+    assert np.array_equal(got.astype(np.int64), want) and np.all(got == want)
+    assert mrr == float(R.abs().max().item())
+    fg.wgrad_recompute_error(dy, x, R.clone(), R, err)
+    assert_status_ok()
+    sdd2, srr2, mdd2, mrr2 = fg.wgrad_err_values(err)
+    assert sdd2 == 0.0 and mdd2 == 0.0 and srr2 == srr and mrr2 == mrr

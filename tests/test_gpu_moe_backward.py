@@ -204,3 +204,19 @@ def test_moe_down_wgrad_full_size():
     want = oracle.grouped_wgrad_points(offs, rAT, oracle.E5M2, rsA, rBT, oracle.E4M3, rsB, pg, pn, pk)
     got = D.view(E, Hd, F)[torch.from_numpy(pg).cuda(), torch.from_numpy(pn).cuda(), torch.from_numpy(pk).cuda()]
     gemm_tolerance_check(got.cpu().numpy().astype(np.float64), want, bf16_out=False)
+
+
+def test_batched_transpose_full_size():
+    """The benchmarked size: the 128 experts' gate/up weights [1536][2048] as
+    FP8 codes with 128x128 scale grids; the GPU transposes equal the byte and
+    scale-grid transposes bit for bit."""
+    E, R, C = 128, 1536, 2048
+    g = torch.Generator(device="cuda").manual_seed(13)
+    q = torch.randint(0, 256, (E, R, C), generator=g, device="cuda", dtype=torch.uint8)
+    s = torch.rand((E, R // 128, C // 128), generator=g, device="cuda") + 0.5
+    qT = torch.empty((E, C, R), dtype=torch.uint8, device="cuda")
+    sT = torch.empty((E, C // 128, R // 128), device="cuda")
+    fg.transpose_128x128_batched(q, s, qT, sT)
+    assert_status_ok()
+    assert torch.equal(qT, q.transpose(1, 2))
+    assert torch.equal(sT.view(torch.int32), s.transpose(1, 2).contiguous().view(torch.int32))
