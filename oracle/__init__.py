@@ -4,7 +4,8 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 leg may import this package.  The product path (the CUDA library and its
 binding) never loads it, and it shares no code with that path: the arithmetic
 lives in ``fp8fg_oracle.c`` (plain C, FP64 where the definition is real
-valued), compiled with gcc, no fast-math, no FP contraction.
+valued), compiled with gcc, no fast-math, no FP contraction, and for MXFP8 in
+``mx.py`` (plain numpy around the C encoder and decoders).
 
 Each wrapper below takes and returns numpy arrays (BF16 as uint16 bit
 patterns, FP8 as uint8 codes).  Citations and the readings taken where the
