@@ -89,6 +89,7 @@ _SIGS = {
                                                    _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "fp8_quant_pertensor_current": (_INT, [_VP, _I64, _I64, _I64, _INT, _VP, _VP, _VP, _VP]),
     "fp8_quant_stats": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _INT, _INT, _VP, _VP, _VP]),
+    "fp8_quant_mx": (_INT, [_VP, _I64, _I64, _I64, _INT, _VP, _VP, _VP]),
     "fp8_blockscaled_gemm": (_INT, [_I64, _I64, _I64, _VP, _INT, _VP, _INT, _VP, _INT, _VP, _INT,
                                     _VP, _INT, _I64, _VP]),
     "fp8_grouped_gemm": (_INT, [_INT, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _INT, _I64,
@@ -313,6 +314,14 @@ def quant_stats(x, q, s, gran, fmt, stats, workspace=None, stream=None):
             _buf(stats, "stats", (torch.int64,), 5),
             _buf(workspace, "workspace", (torch.uint8,), workspace_bytes(), True))
     _check("fp8_quant_stats", L.fp8_quant_stats(px, R, C, ld, *args, _stream(stream)))
+
+
+def quant_mx(x, fmt, q, e8, stream=None):
+    """MXFP8: q [R, C] codes and e8 [R, C/32] uint8 scale codes, X = 2^(e8 - 127)."""
+    L = lib()
+    px, R, C, ld = _mat(x, "x", _BF16)
+    args = (_buf(q, "q", _CODES, R * C), _buf(e8, "e8", (torch.uint8,), R * (C // 32)))
+    _check("fp8_quant_mx", L.fp8_quant_mx(px, R, C, ld, fmt, *args, _stream(stream)))
 
 
 # ------------------------------------------------------------------ GEMMs

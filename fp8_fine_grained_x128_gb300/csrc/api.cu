@@ -203,6 +203,19 @@ FP8FG_API int fp8_quant_pertensor_current(const void *x, int64_t rows, int64_t c
     return launch_pertensor_current(x, rows, cols, ldx, fmt, scale, q, workspace, st, S(stream));
 }
 
+FP8FG_API int fp8_quant_mx(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, void *q, uint8_t *e8,
+                           void *stream)
+{
+    if (!fmt_ok(fmt)) return FP8_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || cols % 32 != 0) return FP8_ERR_SHAPE;
+    if (rows == 0 || cols == 0) return FP8_OK;
+    if (!x || !q || !e8) return FP8_ERR_INVALID_ARG;
+    if (ldx < cols) return FP8_ERR_SHAPE;
+    if (!aligned16(x) || ldx % 8 != 0 || (reinterpret_cast<uintptr_t>(q) & 7u)) return FP8_ERR_ALIGNMENT;
+    FP8FG_STATUS_OR_RETURN(st);
+    return launch_quant_mx(x, rows, cols, ldx, fmt, q, e8, st, S(stream));
+}
+
 FP8FG_API int fp8_quant_stats(const void *x, int64_t rows, int64_t cols, int64_t ldx, const void *q, const float *s,
                               int gran, int fmt, fp8_stats_t *stats, void *workspace, void *stream)
 {

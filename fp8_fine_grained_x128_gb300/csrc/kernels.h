@@ -18,6 +18,8 @@ int *status_word_ptr();
 // quant.cu
 int launch_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, void *q, float *s,
                        void *qT, float *sT, int *status, cudaStream_t st);
+int launch_quant_mx(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, void *q, uint8_t *e8,
+                    int *status, cudaStream_t st);
 int launch_quant_128x128(const void *w, int64_t rows, int64_t cols, int64_t ldw, int fmt, void *q, float *s,
                          void *qT, float *sT, int *status, cudaStream_t st);
 // batch matrices of [rows][cols] stored back to back (scales likewise)

@@ -203,6 +203,22 @@ FP8FG_API int fp8_quant_pertensor_current(const void *x, int64_t rows, int64_t c
                                           int fmt, float *scale, void *q, void *workspace,
                                           void *stream);
 
+/* MXFP8 quantization ([Infra] "Hardware requirements for FP8 training":
+ * Blackwell adds MXFP8, micro-scaled FP8; "Scaling strategies and
+ * stability": each block inside a tensor gets its own scale factor).  The
+ * pages give neither the block size nor the scale encoding; here a block is
+ * 32 consecutive elements of a row, and its scale is a power of two
+ * X = 2^(e8 - 127) stored as an 8-bit exponent code: the smallest power of
+ * two with amax / X <= fmax, so no element saturates (X = 1 for an all-zero
+ * block).  q = RNE_satfinite(x / X), exact since X is a power of two.
+ *   x: BF16 [rows][ldx], cols % 32 == 0, x 16-byte aligned, ldx % 8 == 0.
+ *   q: [rows][cols] codes (fmt), 8-byte aligned.
+ *   e8: [rows][cols/32] scale codes, any alignment.
+ * A block holding Inf/NaN records FP8_ERR_NONFINITE (its outputs are
+ * unspecified).  rows or cols == 0 is a no-op. */
+FP8FG_API int fp8_quant_mx(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                           void *q, uint8_t *e8, void *stream);
+
 /* The same delayed-scaling step for callers that cannot allocate device
  * memory -- for example code that runs inside another framework's fixed
  * memory plan or arena, or a plugin that is handed buffers but no allocator.

@@ -126,6 +126,15 @@ def test_host_validation_without_launch(lib):
     rec = fg.DelayedRecipe(1, 16, 0, 1)
     assert lib.fp8_quant_pertensor_delayed(good, 128, 100, 128, ctypes.byref(rec), good, good, good, good,
                                            None, None, good, S) == fg.ERR_SHAPE
+    # MXFP8 quantizer
+    assert lib.fp8_quant_mx(good, 4, 48, 48, 0, good, good, S) == fg.ERR_SHAPE
+    assert lib.fp8_quant_mx(good, 4, 64, 32, 0, good, good, S) == fg.ERR_SHAPE
+    assert lib.fp8_quant_mx(good, 4, 64, 64, 5, good, good, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_quant_mx(good, 4, 64, 64, 0, good, None, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_quant_mx(odd, 4, 64, 64, 0, good, good, S) == fg.ERR_ALIGNMENT
+    assert lib.fp8_quant_mx(good, 4, 64, 68, 0, good, good, S) == fg.ERR_ALIGNMENT
+    assert lib.fp8_quant_mx(good, 4, 64, 64, 0, P(4100), good, S) == fg.ERR_ALIGNMENT
+    assert lib.fp8_quant_mx(None, 0, 64, 64, 1, None, None, S) == fg.OK
     assert lib.fp8_selftest_wait_timeout(0, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_device_status(S, None) == fg.ERR_INVALID_ARG
 
