@@ -413,6 +413,17 @@ class RowBench:
         if want("a1"):
             put(self.hbm("a1_quant_1x128", lambda: fg.quant_1x128(X, E, q, s), 3 * R * C + R * C // 32,
                          "X 8192x4096"))
+        if want("a17"):
+            # MXFP8 (next row) on the same X: 1x32 blocks with power-of-two scales; algorithmic bytes =
+            # X read once + the codes + one exponent byte per 32 elements.  Guarded so that a failure
+            # here is reported in its row instead of ending the whole measurement.
+            try:
+                qm, em = u8(R, C), u8(R, C // 32)
+                put(self.hbm("a17_mxfp8_quant_1x32", lambda: fg.quant_mx(X, E, qm, em), 3 * R * C + R * C // 32,
+                             "X 8192x4096, E4M3, 1x32 power-of-two scales"))
+                del qm, em
+            except Exception as exc:
+                out["a17_mxfp8_quant_1x32"] = {"error": f"{type(exc).__name__}: {exc}"}
         if want("a2"):
             R2, C2 = 8192, 28672
             G = _bf16_dev(synth.bf16_normal((R2, C2), 5, 1e-3), dev)
