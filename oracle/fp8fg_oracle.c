@@ -26,7 +26,7 @@
  *            (margin 0, history 16, max algorithm, HYBRID = E4M3 forward /
  *            E5M2 backward), E4M3 max +-448, E5M2 for gradients.
  *
- * Readings where the pages are silent (each is also listed in the design doc):
+ * Readings where the pages are silent:
  *  R1  FP8 encode: round to nearest, ties to even mantissa; |v| >= fmax
  *      saturates to +-fmax (never inf/NaN for a finite input); sign kept, so
  *      -0 -> 0x80; NaN -> 0x7F.

@@ -9,7 +9,7 @@ looking ahead" (hardware-accelerated block scaling replaces per-tensor
 scaling).
 
 The pages name the format but give neither the block size nor the scale
-encoding.  Readings (also listed in the design doc):
+encoding.  Readings:
   R13  A block is 32 consecutive elements along a row (the contraction
        dimension of the GEMM that consumes it), the block of the
        micro-scaling format the pages call MXFP8.

@@ -3,7 +3,7 @@
 Bar: |err| <= 1e-3 * max(|ref|, 1) on every compared output, plus the
 stricter gate 1e-3 * max(|ref|, rms(ref)) that still bites on the small
 dgrad / wgrad outputs; BF16 outputs get half a BF16 ulp of ref on top (the
-rounding of the FP32 result, see DESIGN.md).  BF16 outputs must also equal
+rounding of the FP32 result).  BF16 outputs must also equal
 the round-to-nearest-even of the FP32 outputs bit for bit."""
 import numpy as np
 import pytest
