@@ -72,6 +72,30 @@ inline cudaStream_t S(void *stream) { return static_cast<cudaStream_t>(stream); 
 
 }  // namespace
 
+namespace fp8fg {
+
+int check_pertensor_delayed_args(const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                                 const fp8_delayed_recipe_t *recipe, const float *amax_history, const int32_t *step,
+                                 const float *scale, const void *q, const void *qT, const fp8_stats_t *stats,
+                                 const void *workspace, bool workspace_required)
+{
+    if (!recipe || !fmt_ok(recipe->fmt)) return FP8_ERR_INVALID_ARG;
+    if (recipe->history_len < 1 || recipe->history_len > 1024) return FP8_ERR_INVALID_ARG;
+    if (recipe->margin < -126 || recipe->margin > 126) return FP8_ERR_INVALID_ARG;
+    if (recipe->algo != FP8_AMAX_MAX && recipe->algo != FP8_AMAX_MOST_RECENT) return FP8_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || cols % 128 != 0) return FP8_ERR_SHAPE;
+    if (qT && rows % 128 != 0) return FP8_ERR_SHAPE;
+    if (!amax_history || !step || !scale || (workspace_required && !workspace)) return FP8_ERR_INVALID_ARG;
+    if (rows > 0 && cols > 0 && (!x || !q)) return FP8_ERR_INVALID_ARG;
+    if (rows > 0 && cols > 0 && ldx < cols) return FP8_ERR_SHAPE;
+    if ((x && !aligned16(x)) || (q && !aligned16(q)) || ldx % 8 != 0) return FP8_ERR_ALIGNMENT;
+    if ((qT && !aligned16(qT)) || (workspace && !aligned16(workspace)) || (stats && !aligned16(stats)))
+        return FP8_ERR_ALIGNMENT;
+    return FP8_OK;
+}
+
+}  // namespace fp8fg
+
 extern "C" {
 
 FP8FG_API int fp8_abi_version(void) { return FP8FG_ABI_VERSION; }
@@ -174,17 +198,9 @@ FP8FG_API int fp8_quant_pertensor_delayed(const void *x, int64_t rows, int64_t c
                                           float *scale, void *q, void *qT, fp8_stats_t *stats, void *workspace,
                                           void *stream)
 {
-    if (!recipe || !fmt_ok(recipe->fmt)) return FP8_ERR_INVALID_ARG;
-    if (recipe->history_len < 1 || recipe->history_len > 1024) return FP8_ERR_INVALID_ARG;
-    if (recipe->margin < -126 || recipe->margin > 126) return FP8_ERR_INVALID_ARG;
-    if (recipe->algo != FP8_AMAX_MAX && recipe->algo != FP8_AMAX_MOST_RECENT) return FP8_ERR_INVALID_ARG;
-    if (rows < 0 || cols < 0 || cols % 128 != 0) return FP8_ERR_SHAPE;
-    if (qT && rows % 128 != 0) return FP8_ERR_SHAPE;
-    if (!amax_history || !step || !scale || !workspace) return FP8_ERR_INVALID_ARG;
-    if (rows > 0 && cols > 0 && (!x || !q)) return FP8_ERR_INVALID_ARG;
-    if (rows > 0 && cols > 0 && ldx < cols) return FP8_ERR_SHAPE;
-    if ((x && !aligned16(x)) || (q && !aligned16(q)) || ldx % 8 != 0) return FP8_ERR_ALIGNMENT;
-    if ((qT && !aligned16(qT)) || !aligned16(workspace) || (stats && !aligned16(stats))) return FP8_ERR_ALIGNMENT;
+    const int rc = check_pertensor_delayed_args(x, rows, cols, ldx, recipe, amax_history, step, scale, q, qT, stats,
+                                                workspace, true);
+    if (rc != FP8_OK) return rc;
     FP8FG_STATUS_OR_RETURN(st);
     return launch_pertensor_delayed(x, rows, cols, ldx, recipe->fmt, recipe->history_len, recipe->margin,
                                     recipe->algo, amax_history, step, scale, q, qT, stats, workspace, st, S(stream));

@@ -26,6 +26,14 @@ int launch_quant_128x128(const void *w, int64_t rows, int64_t cols, int64_t ldw,
 int launch_transpose_128x128(const void *q, const float *s, int64_t rows, int64_t cols, void *qT, float *sT,
                              cudaStream_t st, int batch = 1);
 
+// api.cu: the argument contract of the delayed-scaling step (recipe bounds,
+// shapes, required pointers, 16-byte alignment), shared by the entry point
+// with a caller workspace and the one without (workspace_required = false)
+int check_pertensor_delayed_args(const void *x, int64_t rows, int64_t cols, int64_t ldx,
+                                 const fp8_delayed_recipe_t *recipe, const float *amax_history, const int32_t *step,
+                                 const float *scale, const void *q, const void *qT, const fp8_stats_t *stats,
+                                 const void *workspace, bool workspace_required);
+
 // pertensor.cu
 size_t pertensor_workspace_bytes();
 int launch_pertensor_delayed(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, int hist_len,

@@ -58,19 +58,10 @@ extern "C" FP8FG_API int fp8_quant_pertensor_delayed_noalloc(const void *x, int6
 {
     const size_t need = pertensor_workspace_bytes();
     if (need > kNoAllocScratchBytes) return FP8_ERR_UNSUPPORTED;   // scratch block too small for this kernel
-    // same argument contract as fp8_quant_pertensor_delayed, minus the workspace
-    if (!recipe || (recipe->fmt != FP8_E4M3 && recipe->fmt != FP8_E5M2)) return FP8_ERR_INVALID_ARG;
-    if (recipe->history_len < 1 || recipe->history_len > 1024) return FP8_ERR_INVALID_ARG;
-    if (recipe->margin < -126 || recipe->margin > 126) return FP8_ERR_INVALID_ARG;
-    if (recipe->algo != FP8_AMAX_MAX && recipe->algo != FP8_AMAX_MOST_RECENT) return FP8_ERR_INVALID_ARG;
-    if (rows < 0 || cols < 0 || cols % 128 != 0) return FP8_ERR_SHAPE;
-    if (qT && rows % 128 != 0) return FP8_ERR_SHAPE;
-    if (!amax_history || !step || !scale) return FP8_ERR_INVALID_ARG;
-    if (rows > 0 && cols > 0 && (!x || !q)) return FP8_ERR_INVALID_ARG;
-    if (rows > 0 && cols > 0 && ldx < cols) return FP8_ERR_SHAPE;
-    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    if ((x && !al16(x)) || (q && !al16(q)) || ldx % 8 != 0) return FP8_ERR_ALIGNMENT;
-    if ((qT && !al16(qT)) || (stats && !al16(stats))) return FP8_ERR_ALIGNMENT;
+    // the argument contract of fp8_quant_pertensor_delayed (the same check), minus the workspace
+    const int arg_rc = check_pertensor_delayed_args(x, rows, cols, ldx, recipe, amax_history, step, scale, q, qT,
+                                                    stats, nullptr, false);
+    if (arg_rc != FP8_OK) return arg_rc;
 
     void *ws = nullptr;
     const int rc = noalloc_scratch(&ws);

@@ -25,3 +25,13 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _guard_bands(request):
+    """After every GPU test: the guard bands around the test's output buffers
+    are intact (no kernel wrote outside its output)."""
+    yield
+    if "gpu" in request.keywords:
+        import gpu_helpers
+        gpu_helpers.check_canaries()

@@ -1,10 +1,50 @@
 """Shared helpers for the GPU parity tests: host<->device marshalling of the
-seeded inputs and the GEMM tolerance check (the same numbers the oracle sees
-go to the CUDA library)."""
+seeded inputs, guard-banded output buffers, the stratified GEMM sample and
+the GEMM tolerance check (the same numbers the oracle sees go to the CUDA
+library).
+
+Guard bands stand in for a memory checker (compute-sanitizer is not
+available on the test machines): every output buffer made by ``empty_u8`` /
+``empty_f32`` / ``guarded`` lives inside a larger allocation whose bytes
+before and after it are filled with a sentinel, and the buffer itself starts
+out holding the sentinel too (so an element a kernel forgets to write shows
+up in the parity comparison).  ``check_canaries`` -- run by the test suite
+after every GPU test -- asserts that no kernel wrote into a band."""
 import numpy as np
 import torch
 
 import fp8_fine_grained_x128_gb300 as fg
+
+CANARY_BYTE = 0xA5
+CANARY_BAND = 1 << 14          # bytes on each side (keeps the 16-byte alignment of the buffer)
+_bands = []                    # (raw allocation, buffer bytes, label) of every live guarded buffer
+
+
+def guarded(shape, dtype, label=""):
+    """An uninitialised-looking output buffer with sentinel bands around it."""
+    esz = torch.empty((), dtype=dtype).element_size()
+    n = int(np.prod(shape)) if len(shape) else 1
+    nbytes = n * esz
+    raw = torch.full((2 * CANARY_BAND + nbytes,), CANARY_BYTE, dtype=torch.uint8, device="cuda")
+    t = raw[CANARY_BAND:CANARY_BAND + nbytes].view(dtype).view(shape)
+    _bands.append((raw, nbytes, label or f"{tuple(shape)} {dtype}"))
+    return t
+
+
+def check_canaries():
+    """Assert that every guard band registered since the last call is intact."""
+    global _bands
+    bands, _bands = _bands, []
+    if not bands:
+        return
+    torch.cuda.synchronize()
+    for raw, nbytes, label in bands:
+        lo = raw[:CANARY_BAND]
+        hi = raw[CANARY_BAND + nbytes:]
+        bad_lo = int((lo != CANARY_BYTE).sum().item())
+        bad_hi = int((hi != CANARY_BYTE).sum().item())
+        assert bad_lo == 0 and bad_hi == 0, (
+            f"guard band of the buffer {label} overwritten: {bad_lo} bytes before it, {bad_hi} after it")
 
 
 def dev_bf16(bits: np.ndarray) -> torch.Tensor:
@@ -28,11 +68,11 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def empty_u8(*shape):
-    return torch.empty(shape, dtype=torch.uint8, device="cuda")
+    return guarded(shape, torch.uint8)
 
 
 def empty_f32(*shape):
-    return torch.empty(shape, dtype=torch.float32, device="cuda")
+    return guarded(shape, torch.float32)
 
 
 def assert_status_ok():
@@ -78,3 +118,23 @@ def sample_points(M: int, N: int, n: int, seed: int = 0, tile_m: int = 128, tile
     pm = np.concatenate([corners_m, rng.integers(0, M, n)])
     pn = np.concatenate([corners_n, rng.integers(0, N, n)])
     return pm.astype(np.int64), pn.astype(np.int64)
+
+
+def sample_points_dense(M: int, N: int, per_tile: int = 16, total: int = 1 << 20, seed: int = 0,
+                        tile_m: int = 128, tile_n: int = 128):
+    """A seeded, stratified sample of output coordinates: every tile_m x tile_n
+    output tile is hit k = max(per_tile, ceil(total / tiles)) times -- its four
+    corners plus k - 4 points drawn uniformly inside it -- so the sample holds
+    at least ``total`` points and no tile is hit fewer than ``per_tile`` times."""
+    rng = np.random.default_rng(seed)
+    tm, tn = M // tile_m, N // tile_n
+    ntiles = tm * tn
+    k = max(per_tile, -(-total // ntiles))
+    mt, nt = np.meshgrid(np.arange(tm, dtype=np.int64) * tile_m, np.arange(tn, dtype=np.int64) * tile_n,
+                         indexing="ij")
+    mt, nt = mt.ravel(), nt.ravel()
+    cm = np.array([0, 0, tile_m - 1, tile_m - 1], np.int64)
+    cn = np.array([0, tile_n - 1, 0, tile_n - 1], np.int64)
+    pm = [mt[:, None] + cm[None, :], mt[:, None] + rng.integers(0, tile_m, (ntiles, k - 4))]
+    pn = [nt[:, None] + cn[None, :], nt[:, None] + rng.integers(0, tile_n, (ntiles, k - 4))]
+    return np.concatenate(pm, axis=1).ravel(), np.concatenate(pn, axis=1).ravel()

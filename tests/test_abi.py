@@ -49,6 +49,17 @@ def test_version_and_strings(lib):
     assert fg.workspace_bytes() >= 8192
 
 
+def test_pertensor_workspace_fits_the_noalloc_scratch(lib):
+    """The delayed-scaling step's workspace (ticket, amax, 65536-key presence
+    bitmap, 256-key bitmap) is 8240 bytes; the no-allocation entry point keeps
+    it in a fixed 16 KiB device block, so it must fit there."""
+    src = open(os.path.join(ROOT, "fp8_fine_grained_x128_gb300", "csrc", "noalloc.cu")).read()
+    block = int(re.search(r"kNoAllocScratchBytes\s*=\s*(\d+)", src).group(1))
+    assert block == 16384
+    assert fg.workspace_bytes() == 4 + 4 + 8 + 2048 * 4 + 8 * 4 == 8240
+    assert fg.workspace_bytes() <= block
+
+
 def test_host_validation_without_launch(lib):
     P = ctypes.c_void_p
     good = P(4096)            # a 16-byte aligned (never dereferenced) address

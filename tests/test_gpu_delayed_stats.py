@@ -47,7 +47,7 @@ def check_against_oracle(g: GpuDelayed, st: oracle.DelayedState, xb, fmt, margin
     assert np.array_equal(g.hist.cpu().numpy().view(np.uint32), st.hist.view(np.uint32))
     assert g.scale.cpu().numpy().view(np.uint32)[0] == st.scale.view(np.uint32)[0]
     assert int(g.step.item()) == int(st.step[0])
-    return q_ref, used
+    return q_ref, used, stats_ref
 
 
 @pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
@@ -68,13 +68,23 @@ def test_delayed_knobs():
             check_against_oracle(g, st, xb, oracle.E4M3, margin, algo)
 
 
-def test_delayed_full_size_three_steps():
+def test_delayed_full_size_32_steps():
+    """The delayed-scaling workload exactly as stated: a 16384 x 4096 Linear
+    over 32 steps of drifting signed-lognormal X (E4M3) and dY (E5M2), history
+    length 16, max algorithm, margin 0.  At every step codes, transposed
+    codes, the 16-slot history, the next scale, the step counter and the
+    fused monitor counts equal the oracle's; the drift steps (8, 16, 24)
+    saturate and the history window wraps at step 16."""
     gx, gd = GpuDelayed(oracle.E4M3), GpuDelayed(oracle.E5M2)
     sx, sd = oracle.DelayedState(16), oracle.DelayedState(16)
-    for t in (0, 1, 8):
+    sat = {}
+    for t in range(32):
         xb, dyb = synth.delayed_step_inputs(t)
-        check_against_oracle(gx, sx, xb, oracle.E4M3)
+        sat[t] = int(check_against_oracle(gx, sx, xb, oracle.E4M3)[2][2])
         check_against_oracle(gd, sd, dyb, oracle.E5M2)
+    assert all(sat[t] > 0 for t in (8, 16, 24)), sat       # the drift outruns the delayed scale
+    assert int(gx.step.item()) == 32 and int(gd.step.item()) == 32
+    assert np.all(sx.hist > 0) and np.all(sd.hist > 0)        # every slot of the window written
 
 
 def test_delayed_checkpoint_split_on_device():
@@ -135,7 +145,7 @@ def test_delayed_overflowing_quotients_saturate(fmt):
         g.scale.fill_(s0)
         st = oracle.DelayedState(16)
         st.scale[:] = np.float32(s0)
-        q_ref, _ = check_against_oracle(g, st, xb, fmt)
+        q_ref, _, _ = check_against_oracle(g, st, xb, fmt)
         assert (q_ref & 0x7F == (0x7E if fmt == oracle.E4M3 else 0x7B)).sum() > 0
 
 

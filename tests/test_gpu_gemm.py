@@ -12,8 +12,8 @@ import torch
 import fp8_fine_grained_x128_gb300 as fg
 import oracle
 import synth
-from gpu_helpers import (assert_status_ok, bf16_to_f64, dev_f32, dev_u8, gemm_tolerance_check,
-                         host_u16, sample_points)
+from gpu_helpers import (CANARY_BYTE, assert_status_ok, bf16_to_f64, dev_f32, dev_u8, gemm_tolerance_check,
+                         guarded, host_u16, sample_points_dense)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,7 +34,7 @@ def quantized_operand(rows, K, seed, gran, fmt=oracle.E4M3, std=1.0, outliers=Tr
 
 def run_gemm(qa, fa, sa, ga, qb, fb, sb, gb, out_dtype):
     M, N = qa.shape[0], qb.shape[0]
-    D = torch.empty((M, N), dtype=out_dtype, device="cuda")
+    D = guarded((M, N), out_dtype)
     fg.blockscaled_gemm(dev_u8(qa), fa, dev_f32(sa), ga, dev_u8(qb), fb, dev_f32(sb), gb, D)
     assert_status_ok()
     return D
@@ -82,7 +82,7 @@ def test_gemm_qkv_fprop_full_size_sampled():
     qb, sb, _ = oracle.quant_128x128(wb)
     D = run_gemm(qa, oracle.E4M3, sa, oracle.GRAN_1x128, qb, oracle.E4M3, sb, oracle.GRAN_128x128,
                  torch.bfloat16)
-    pm, pn = sample_points(8192, 6144, 1 << 16, seed=1)
+    pm, pn = sample_points_dense(8192, 6144, seed=1)
     ref = oracle.gemm_points(qa, oracle.E4M3, sa, oracle.GRAN_1x128, qb, oracle.E4M3, sb,
                              oracle.GRAN_128x128, pm, pn)
     got = bf16_to_f64(host_u16(D))[pm, pn]
@@ -98,7 +98,7 @@ def test_gemm_pertensor_full_size_sampled(fa):
     qa, sa = quantized_operand(M, K, 31, oracle.GRAN_TENSOR, fa)
     qb, sb = quantized_operand(N, K, 32, oracle.GRAN_TENSOR, oracle.E4M3, std=0.02)
     D = run_gemm(qa, fa, sa, oracle.GRAN_TENSOR, qb, oracle.E4M3, sb, oracle.GRAN_TENSOR, torch.bfloat16)
-    pm, pn = sample_points(M, N, 1 << 15, seed=3)
+    pm, pn = sample_points_dense(M, N, seed=3)
     ref = oracle.gemm_points(qa, fa, sa, oracle.GRAN_TENSOR, qb, oracle.E4M3, sb, oracle.GRAN_TENSOR, pm, pn)
     got = bf16_to_f64(host_u16(D))[pm, pn]
     gemm_tolerance_check(got, ref, bf16_out=True)
@@ -125,3 +125,31 @@ def test_gemm_repeated_calls_are_deterministic():
     d1 = run_gemm(qa, 0, sa, 0, qb, 0, sb, 1, torch.float32)
     d2 = run_gemm(qa, 0, sa, 0, qb, 0, sb, 1, torch.float32)
     assert torch.equal(d1, d2)
+
+
+LD_CASES = [
+    # name, M, N, K, ldD - N, out dtype: the BF16 tile leaves through shared memory and TMA
+    # stores (BN = 256, K <= 8192), straight from registers (BN = 256, K > 8192; BN = 128), FP32
+    ("bf16_tma_store_bn256", 384, 512, 1024, 64, torch.bfloat16),
+    ("bf16_direct_long_k", 256, 512, 8320, 64, torch.bfloat16),
+    ("bf16_bn128", 384, 384, 640, 32, torch.bfloat16),
+    ("f32_bn256", 256, 512, 512, 8, torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", LD_CASES, ids=[c[0] for c in LD_CASES])
+def test_gemm_output_leading_dimension(case):
+    """D given as a column slice of a wider matrix (ldD > N): the N columns of
+    every row match the oracle and the padding columns keep their sentinel,
+    whichever store path the output takes."""
+    name, M, N, K, pad, dt = case
+    qa, sa = quantized_operand(M, K, 41, oracle.GRAN_1x128)
+    qb, sb = quantized_operand(N, K, 42, oracle.GRAN_128x128, std=0.5)
+    ref = oracle.gemm_full(qa, 0, sa, oracle.GRAN_1x128, qb, 0, sb, oracle.GRAN_128x128)
+    full = guarded((M, N + pad), dt)
+    D = full[:, :N]
+    fg.blockscaled_gemm(dev_u8(qa), 0, dev_f32(sa), fg.GRAN_1x128, dev_u8(qb), 0, dev_f32(sb), fg.GRAN_128x128, D)
+    assert_status_ok()
+    gemm_tolerance_check(to_f64(D.contiguous()), ref, bf16_out=dt == torch.bfloat16)
+    padding = full[:, N:].contiguous().view(torch.uint8)
+    assert bool((padding == CANARY_BYTE).all()), "the GEMM wrote into the padding columns of D"

@@ -4,8 +4,9 @@ pass of ``bench.MlpStep`` (14 launches, the same kernels, shapes, layouts and
 launch configuration).
 
 Every one of the six GEMMs is compared with the oracle's unrounded FP64 value
-on a sample that hits each 128x128 output tile at its four corners plus 2^15
-uniform points, computed from the FP8 operands the step itself produced.
+on a stratified sample of at least 2^20 outputs that hits every 128x128
+output tile at least 16 times (its four corners among them), computed from
+the FP8 operands the step itself produced.
 Those operands are pinned separately: the quantizations of X, dY and W_gu
 equal the oracle's on whole 128-row blocks, and the on-demand weight
 transposes equal the byte / scale-grid transposes bit for bit.  (The SwiGLU-
@@ -18,7 +19,7 @@ import torch
 import bench
 import fp8_fine_grained_x128_gb300 as fg
 import oracle
-from gpu_helpers import assert_status_ok, bf16_to_f64, gemm_tolerance_check, host_u16, sample_points
+from gpu_helpers import assert_status_ok, bf16_to_f64, gemm_tolerance_check, host_u16, sample_points_dense
 
 pytestmark = pytest.mark.gpu
 
@@ -62,7 +63,8 @@ def test_step_gemm_sampled(step, i):
     M, K = A.shape
     N = B.shape[0]
     assert B.shape[1] == K and tuple(D.shape) == (M, N)
-    pm, pn = sample_points(M, N, 1 << 15, seed=100 + i)
+    pm, pn = sample_points_dense(M, N, per_tile=16, total=1 << 20, seed=100 + i)
+    assert pm.size >= 1 << 20
     ref = oracle.gemm_points(host(A), oracle.E4M3, host(getattr(step, sa)), ga,
                              host(B), oracle.E4M3, host(getattr(step, sb)), gb, pm, pn)
     gemm_tolerance_check(sampled(D, pm, pn), ref, bf16_out=D.dtype == torch.bfloat16)

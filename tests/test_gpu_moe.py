@@ -11,7 +11,7 @@ import fp8_fine_grained_x128_gb300 as fg
 import oracle
 import synth
 from gpu_helpers import (assert_status_ok, bf16_to_f64, dev_bf16, dev_f32, dev_u8, empty_f32, empty_u8,
-                         gemm_tolerance_check, host_u16, sample_points)
+                         gemm_tolerance_check, host_u16, sample_points_dense)
 
 pytestmark = pytest.mark.gpu
 
@@ -208,7 +208,7 @@ def test_moe_fprop_full_size():
     assert np.array_equal(qg.cpu().numpy()[:tot], qg_ref[:tot])
     assert np.array_equal(sg.cpu().numpy()[:, :tot], sg_ref[:, :tot])
     # stage: gate/up grouped GEMM
-    pm, pn = sample_points(tot, 2 * F, 1 << 15, seed=2)
+    pm, pn = sample_points_dense(tot, 2 * F, seed=2)
     ref_gu = oracle.grouped_gemm_points(offs_np, qg_ref, sg_ref, cap, qgu, sgu, pm, pn)
     gemm_tolerance_check(bf16_to_f64(host_u16(GU))[pm, pn], ref_gu, bf16_out=True)
     # stage: SwiGLU on the GPU's GU, then 1x128 quantization of the GPU's H (bit-exact)
@@ -219,9 +219,10 @@ def test_moe_fprop_full_size():
     assert np.max(np.abs(hi(h_host) - hi(h_ref))) <= 1
     qh_ref, sh_ref, _ = oracle.quant_1x128(h_host)
     assert np.array_equal(qh.cpu().numpy()[:tot], qh_ref)
+    assert np.array_equal(sh.cpu().numpy()[:, :tot].view(np.uint32), sh_ref.view(np.uint32))
     # stage: down grouped GEMM
     qh_full = np.zeros((cap, F), np.uint8); qh_full[:tot] = qh_ref
     sh_full = np.zeros((F // 128, cap), np.float32); sh_full[:, :tot] = sh_ref
-    pm, pn = sample_points(tot, Hd, 1 << 15, seed=3)
+    pm, pn = sample_points_dense(tot, Hd, seed=3)
     ref_y = oracle.grouped_gemm_points(offs_np, qh_full, sh_full, cap, qdn, sdn, pm, pn)
     gemm_tolerance_check(bf16_to_f64(host_u16(Y))[pm, pn], ref_y, bf16_out=True)
