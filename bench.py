@@ -583,8 +583,8 @@ class RowBench:
             del KV, qkv
         if want("a16"):
             # high-precision dw recompute of the down projection's wgrad (dW_down [4096, 14336]
-            # from dY [8192, 4096] and H [8192, 14336]): a cuBLAS BF16 GEMM plus this
-            # library's comparison kernel; reported against the measured bf16 peak
+            # from dY [8192, 4096] and H [8192, 14336]): the library's BF16 tensor-core GEMM with
+            # the comparison fused into its epilogue; reported against the measured bf16 peak
             Md, Nd, Kd = 8192, 4096, 14336
             dYm, Hm = bf(Md, Nd).normal_(0, 1e-3), bf(Md, Kd).normal_(0, 1.0)
             Dm, Rm, em = f32(Nd, Kd).normal_(0, 1.0), f32(Nd, Kd), fg.new_wgrad_err(dev)
@@ -592,7 +592,7 @@ class RowBench:
             tf = 2.0 * Md * Nd * Kd / t / 1e12
             out["a16_dw_recompute_monitor"] = {"time_us": t * 1e6, "achieved": tf, "unit": "TFLOP/s",
                                                "peak": self.pk["bf16"], "frac": tf / self.pk["bf16"],
-                                               "bound": "tensor (bf16, cuBLAS) + HBM (comparison)",
+                                               "bound": "tensor (bf16 kind::f16, comparison fused)",
                                                "note": "dW_down 4096x14336 over 8192 tokens"}
             del dYm, Hm, Dm, Rm
         if want("a11"):

@@ -326,15 +326,17 @@ FP8FG_API int fp8_wgrad_recompute_error(int64_t M, int64_t N, int64_t K, const v
 {
     if (M < 0 || N < 0 || K < 0 || M >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31))
         return FP8_ERR_SHAPE;
+    if (N % 128 != 0 || K % 128 != 0) return FP8_ERR_SHAPE;
     if (!err) return FP8_ERR_INVALID_ARG;
     if (N > 0 && K > 0) {
         if (ldD < K) return FP8_ERR_SHAPE;
         if (!D || !ref_workspace || (M > 0 && (!dY || !X))) return FP8_ERR_INVALID_ARG;
-        if ((M > 0 && (!aligned16(dY) || !aligned16(X))) || (reinterpret_cast<uintptr_t>(D) & 3u) ||
-            (reinterpret_cast<uintptr_t>(ref_workspace) & 3u) || (reinterpret_cast<uintptr_t>(err) & 7u))
+        if ((M > 0 && (!aligned16(dY) || !aligned16(X))) || !aligned16(D) || ldD % 4 != 0 ||
+            !aligned16(ref_workspace) || (reinterpret_cast<uintptr_t>(err) & 7u))
             return FP8_ERR_ALIGNMENT;
     }
-    return launch_wgrad_recompute_error(M, N, K, dY, X, D, ldD, ref_workspace, err, S(stream));
+    FP8FG_STATUS_OR_RETURN(st);
+    return launch_wgrad_recompute_error(M, N, K, dY, X, D, ldD, ref_workspace, err, st, S(stream));
 }
 
 FP8FG_API int fp8_adamw_step_fp8_states(float *param, const void *grad, uint8_t *m, float *m_scales, uint8_t *v,

@@ -66,13 +66,32 @@ __device__ __forceinline__ float scale_from_amax_bits(uint32_t amax_bf16_bits, i
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, fmax_of(fmt));
 }
 
+// Scales for which the quotient x / s is taken from the reciprocal with
+// Markstein's correction (below).  The correction needs the remainder
+// e = x - q0*s exactly: e is a multiple of ulp(q0)*ulp(s) below ulp(q0)*s, so
+// it fits binary32 while ulp(q0)*ulp(s) >= 2^-149, i.e. exponent(q) +
+// exponent(s) >= -103.  Every quotient that can decide an FP8 code lies at or
+// above 2^-18 (half of E5M2's smallest subnormal 2^-16 is 2^-17; E4M3's is
+// 2^-10), so s >= 2^-84 keeps those remainders exact; below it, or for a
+// smaller quotient, a misrounded q stays far from every code boundary.  With
+// s just above the binary32 normal range instead (2^-125), BF16 subnormal x
+// gave quotients one ulp off that changed 186 E4M3 / 92 E5M2 codes of the
+// exhaustive (amax, x) check.  Above 2^125, 1/s would be subnormal.
+constexpr float kFastDivMinScale = 0x1p-84f;
+constexpr float kFastDivMaxScale = 0x1p125f;
+__host__ __device__ __forceinline__ bool fast_div_scale(float s)
+{
+    return s >= kFastDivMinScale && s <= kFastDivMaxScale;
+}
+
 // Division x / s rounded to nearest binary32, computed from r = RN(1/s) with
 // Markstein's correction (P. Markstein, "Computation of elementary functions
 // on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
 // r within half an ulp of 1/s and q0 within one ulp of x/s, the remainder
 // e = x - q0*s is exact under FMA and RN(q0 + e*r) is the correctly rounded
-// quotient.  Valid while s and 1/s are normal and nothing overflows; callers
-// use it only when 2^-125 <= s <= 2^125 and fall back to __fdiv_rn otherwise.
+// quotient.  Valid while s and 1/s are normal, e does not underflow and
+// nothing overflows; callers use it only when fast_div_scale(s) and fall back
+// to __fdiv_rn otherwise.
 // A quotient that overflows (or x = +-Inf) turns q0 into +-Inf and q into NaN:
 // such a NaN from a non-NaN x is redone by __fdiv_rn.
 // The sign is forced from x so that -0 / s = -0 like the IEEE division.
@@ -81,7 +100,7 @@ struct Divider {
     bool fast;
     __device__ __forceinline__ explicit Divider(float s_) : s(s_)
     {
-        fast = (s_ >= 0x1p-125f) && (s_ <= 0x1p125f);
+        fast = fast_div_scale(s_);
         r = fast ? __frcp_rn(s_) : 0.0f;
     }
     __device__ __forceinline__ float operator()(float x) const
@@ -111,7 +130,7 @@ struct Divider2 {
     bool fast;
     __device__ __forceinline__ explicit Divider2(float s_) : s(s_)
     {
-        fast = (s_ >= 0x1p-125f) && (s_ <= 0x1p125f);
+        fast = fast_div_scale(s_);
         const float r = fast ? __frcp_rn(s_) : 0.0f;
         asm("mov.b64 %0, {%1, %1};" : "=l"(r2) : "f"(r));
         asm("mov.b64 %0, {%1, %1};" : "=l"(ns2) : "f"(-s_));
@@ -279,7 +298,7 @@ __device__ __forceinline__ GroupScale half_warp_scales8(const uint32_t (&m)[8], 
     g.amax = (l16 & 1) ? (K >> 16) : (K & 0xFFFFu);
     g.u = 2 * (l16 >> 2) + (l16 & 1);
     g.s = scale_from_amax_bits(g.amax, FMT);
-    g.r = (g.s >= 0x1p-125f && g.s <= 0x1p125f) ? __frcp_rn(g.s) : 0.0f;
+    g.r = fast_div_scale(g.s) ? __frcp_rn(g.s) : 0.0f;
     return g;
 }
 
@@ -428,6 +447,31 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// Bounded wait on an mbarrier phase shared by the roles of a warp-specialised
+// kernel: on a timeout the first role to give up records FP8_ERR_TIMEOUT and
+// raises the CTA's abort flag, which the other roles' waits poll.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              int *status)
+{
+    if (mbar_wait_bounded(bar, parity, abort_flag)) return true;
+    if (!*abort_flag) {
+        *abort_flag = 1;
+        set_status(status, FP8_ERR_TIMEOUT);
+    }
+    return false;
+}
+
+// One warp waits through lane 0; the outcome is broadcast so the warp stays
+// converged for the .sync.aligned tcgen05 instructions that follow.
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                   int *status)
+{
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, abort_flag, status) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+
 // ---------------------------------------------------------------------- TMA
 
 // 2-D tiled bulk tensor load global -> shared, completion counted in bytes
@@ -486,6 +530,19 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 
 // ------------------------------------------------------------------ tcgen05
 
+// Tiles are walked in bands of GM M-tiles, M fastest: a band's A rows stay in
+// L2 while every B tile is streamed through it once per band.
+__device__ __forceinline__ void tile_coords_raster(int tile, int num_mt, int num_nt, int GM, int &mt, int &nt)
+{
+    const int group = tile / (GM * num_nt);
+    const int first = group * GM;
+    const int gm = min(GM, num_mt - first);
+    const int local = tile - group * GM * num_nt;
+    mt = first + local % gm;
+    nt = local / gm;
+}
+
+
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
 {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
@@ -514,6 +571,19 @@ __device__ __forceinline__ void tc_mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, u
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D(tmem) (+)= A(smem desc) x B(smem desc)^T, 16-bit operands (F16 or BF16 as
+// the instruction descriptor says), FP32 accumulator.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -640,6 +710,34 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
     d |= (uint64_t)1u << 46;
     d |= (uint64_t)2u << 61;
     return d;
+}
+
+// Shared-memory matrix descriptor for an MN-major operand tile in the
+// 128-byte swizzle layout a TMA load writes from a row-major matrix whose
+// rows run along K: each K index is a 128-byte row of 64 consecutive M (or
+// N) elements (16-bit types), 8 such rows form a 1024-byte swizzle atom.
+// Stride byte offset = distance between atoms along K (1024 for consecutive
+// rows), leading byte offset = distance between the 64-element slabs along
+// M / N (one TMA box each).  Version 1, swizzle mode 2 = 128B; the base must
+// be 1024-byte aligned and a K step advances the start by whole atoms.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma .kind::f16 with BF16 A and B (type
+// code 1 at bits 7-9 and 10-12), an FP32 accumulator (bits 4-5 = 1), both
+// operands MN-major (bits 15 and 16), N/8 at bits 17-22, M/16 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_mnmajor(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
 }
 
 // Instruction descriptor of tcgen05.mma .kind::f8f6f4 with an FP32

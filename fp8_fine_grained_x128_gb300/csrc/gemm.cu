@@ -45,6 +45,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace fp8fg {
 
@@ -111,18 +112,6 @@ struct GemmSmem {
     static constexpr int kTmemCols = kNbuf * BN;
 };
 
-// Tiles are walked in bands of GM M-tiles, M fastest: a band's A rows stay in
-// L2 while every B tile is streamed through it once per band.
-__device__ __forceinline__ void tile_coords_raster(int tile, int num_mt, int num_nt, int GM, int &mt, int &nt)
-{
-    const int group = tile / (GM * num_nt);
-    const int first = group * GM;
-    const int gm = min(GM, num_mt - first);
-    const int local = tile - group * GM * num_nt;
-    mt = first + local % gm;
-    nt = local / gm;
-}
-
 // Largest g with off[g] <= row (skips empty groups).
 __device__ __forceinline__ int group_of_row(const int32_t *off, int G, int row)
 {
@@ -181,27 +170,6 @@ __device__ __forceinline__ TileInfo tile_info(int tile, int num_mt, int num_nt, 
     t.a_row = mt * 128;
     t.n0 = nt * BN;
     return t;
-}
-
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                              int *status)
-{
-    if (mbar_wait_bounded(bar, parity, abort_flag)) return true;
-    if (!*abort_flag) {
-        *abort_flag = 1;
-        set_status(status, FP8_ERR_TIMEOUT);
-    }
-    return false;
-}
-
-// One warp waits through lane 0; the outcome is broadcast so the warp stays
-// converged for the .sync.aligned tcgen05 instructions that follow.
-__device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                                   int *status)
-{
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, abort_flag, status) ? 1 : 0;
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 template <int NCOL>
@@ -628,19 +596,25 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D map over an FP8 (byte) matrix [rows][inner], box 128 (K) x box_rows,
-// 128-byte swizzle (the layout the MMA descriptors expect).
-static bool make_map(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t rows, uint32_t box_rows)
+bool make_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *ptr, uint64_t inner, uint64_t rows,
+                 uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapL2promotion l2)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner};
-    cuuint32_t box[2] = {128, box_rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return enc(map, dtype, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D map over an FP8 (byte) matrix [rows][inner], box 128 (K) x box_rows,
+// 128-byte swizzle (the layout the MMA descriptors expect).
+static bool make_map(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t rows, uint32_t box_rows)
+{
+    return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, inner, rows, inner, 128, box_rows,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 // 2-D map over a BF16 output matrix [rows][cols] with row stride ld
@@ -648,15 +622,8 @@ static bool make_map(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t
 // layout of the epilogue).
 static bool make_out_map(CUtensorMap *map, void *ptr, uint64_t cols, uint64_t rows, uint64_t ld)
 {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {ld * 2};
-    cuuint32_t box[2] = {64, 128};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+    return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, cols, rows, ld * 2, 64, 128,
+                       CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 template <int BN, int STAGES, bool PROMOTE, int SBG, int GMODE, bool TSTORE = false>

@@ -58,7 +58,7 @@ int launch_grouped_wgrad(int G, const int32_t *offsets, int64_t Mcap, int64_t N,
 
 // monitor_dw.cu
 int launch_wgrad_recompute_error(int64_t M, int64_t N, int64_t K, const void *dY, const void *X, const float *D,
-                                 int64_t ldD, float *R, fp8_wgrad_err_t *err, cudaStream_t st);
+                                 int64_t ldD, float *R, fp8_wgrad_err_t *err, int *status, cudaStream_t st);
 
 // optim.cu
 int launch_adamw_fp8(float *p, const void *g, uint8_t *qm, float *sm, uint8_t *qv, float *sv, int64_t n,

@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(256, fused_ctas_per_sm<SRC>()) k_quant_1x128_f
             ColDiv2 c;
             c.s0 = sc[0];
             c.s1 = sc[1];
-            c.fast = (sc[0] >= 0x1p-125f) && (sc[0] <= 0x1p125f) && (sc[1] >= 0x1p-125f) && (sc[1] <= 0x1p125f);
+            c.fast = fast_div_scale(sc[0]) && fast_div_scale(sc[1]);
             const float ra = c.fast ? __frcp_rn(sc[0]) : 0.0f, rb = c.fast ? __frcp_rn(sc[1]) : 0.0f;
             c.r2 = f2_pack(ra, rb);
             c.ns2 = f2_pack(-sc[0], -sc[1]);

@@ -319,13 +319,16 @@ typedef struct {
 /* High-precision dw recompute monitor ([Ling] "Where does the error come
  * from?": tensors flagged by the underflow / distortion monitors get their dw
  * recomputed in high precision and compared).  R = dY^T . X from the BF16
- * operands, token-major dY [M][N] and X [M][K], FP32 accumulation (a plain
- * BF16 GEMM, run by cuBLAS, which is loaded on the first call: without it
- * the call returns FP8_ERR_UNSUPPORTED), written to ref_workspace [N][K]
- * (caller-owned, N*K floats); then *err (DEVICE) = the statistics of D
- * [N][ldD] (FP32, e.g. fp8_blockscaled_gemm's wgrad output) against R.
- * The relative Frobenius error is sqrt(sum_sq_diff / sum_sq_ref).
- * dY, X 16-byte aligned; M, N, K < 2^31. */
+ * operands, token-major dY [M][N] and X [M][K] (row-major), products of BF16
+ * values accumulated in FP32 over the M tokens on the tensor cores (this
+ * library's kernel), written to ref_workspace [N][K] (caller-owned, N*K
+ * floats, row stride K); then *err (DEVICE) = the statistics of D [N][ldD]
+ * (FP32, e.g. fp8_blockscaled_gemm's wgrad output) against R: D - R in
+ * FP32, its square and R's in FP64 (exact), summed in FP64.  err is cleared
+ * by the call.  The relative Frobenius error is
+ * sqrt(sum_sq_diff / sum_sq_ref).  N, K % 128 == 0 (FP8_ERR_SHAPE), any M
+ * (0: R = 0); M, N, K < 2^31; dY, X, D, ref_workspace 16-byte aligned and
+ * ldD % 4 == 0 (FP8_ERR_ALIGNMENT). */
 FP8FG_API int fp8_wgrad_recompute_error(int64_t M, int64_t N, int64_t K, const void *dY, const void *X,
                                         const float *D, int64_t ldD, float *ref_workspace,
                                         fp8_wgrad_err_t *err, void *stream);

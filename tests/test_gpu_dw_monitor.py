@@ -9,7 +9,7 @@ import torch
 import fp8_fine_grained_x128_gb300 as fg
 import oracle
 import synth
-from gpu_helpers import assert_status_ok, dev_bf16
+from gpu_helpers import assert_status_ok, dev_bf16, guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 def monitor(dy_bits, x_bits, D):
     M, N = dy_bits.shape
     K = x_bits.shape[1]
-    R = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    R = guarded((N, K), torch.float32)
     err = fg.new_wgrad_err()
     fg.wgrad_recompute_error(dev_bf16(dy_bits), dev_bf16(x_bits), D, R, err)
     assert_status_ok()
@@ -34,6 +34,24 @@ def test_exact_wgrad_has_zero_error():
     assert np.array_equal(Rg.cpu().numpy(), R)
     assert sdd == 0.0 and mdd == 0.0
     assert srr == float((R.astype(np.float64) ** 2).sum()) and mrr == float(np.abs(R).max())
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 128, 384), (1000, 256, 512), (64, 384, 256), (8200, 128, 128)],
+                         ids=["bn128", "ragged_tokens_bn256", "one_stage", "long_ragged"])
+def test_exact_integer_reference_shapes(M, N, K):
+    """Small-integer operands make every product and partial sum exact in
+    FP32, so R must equal the integer matmul whatever the reduction order:
+    both tile widths, token counts that are not a multiple of the 64-token
+    stage (zero-filled), one stage, many stages."""
+    rng = np.random.default_rng(M + N + K)
+    dyi, xi = rng.integers(-8, 9, size=(M, N)), rng.integers(-8, 9, size=(M, K))
+    to_bf16 = lambda a: (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    R = (dyi.T.astype(np.int64) @ xi.astype(np.int64)).astype(np.float32)
+    D = torch.from_numpy(R + 1.0).cuda()
+    (sdd, srr, mdd, mrr), Rg = monitor(to_bf16(dyi), to_bf16(xi), D)
+    assert np.array_equal(Rg.cpu().numpy(), R)
+    assert sdd == float(N * K) and mdd == 1.0
+    assert mrr == float(np.abs(R).max())
 
 
 def test_fp8_wgrad_error_matches_oracle():
