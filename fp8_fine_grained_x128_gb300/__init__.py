@@ -92,6 +92,7 @@ _SIGS = {
     "fp8_quant_mx": (_INT, [_VP, _I64, _I64, _I64, _INT, _VP, _VP, _VP]),
     "fp8_blockscaled_gemm": (_INT, [_I64, _I64, _I64, _VP, _INT, _VP, _INT, _VP, _INT, _VP, _INT,
                                     _VP, _INT, _I64, _VP]),
+    "fp8_mx_gemm": (_INT, [_I64, _I64, _I64, _VP, _INT, _VP, _VP, _INT, _VP, _VP, _INT, _I64, _VP]),
     "fp8_grouped_gemm": (_INT, [_INT, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _INT, _I64,
                                 _VP]),
     "fp8_grouped_gemm_wgrad": (_INT, [_INT, _VP, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _INT, _VP, _VP, _INT,
@@ -346,6 +347,21 @@ def blockscaled_gemm(A, fmtA, sA, granA, B, fmtB, sB, granB, D, stream=None):
     _check("fp8_blockscaled_gemm",
            L.fp8_blockscaled_gemm(M, N, K, pA, fmtA, psA, granA, pB, fmtB, psB, granB, pD, out, ldD,
                                   _stream(stream)))
+
+
+def mx_gemm(A, fmtA, eA, B, fmtB, eB, D, stream=None):
+    """MXFP8 GEMM: D = A . B^T with codes A [M, K], B [N, K] and scale exponents eA [M, K/32],
+    eB [N, K/32] (uint8, X = 2^(e - 127), as quant_mx writes them)."""
+    L = lib()
+    M, K = _shape(A, "A", 2)
+    N, KB = _shape(B, "B", 2)
+    if KB != K:
+        raise ValueError(f"B: shape {(N, KB)}, expected [N][{K}]")
+    pA, pB = _buf(A, "A", _CODES, M * K), _buf(B, "B", _CODES, N * K)
+    peA = _buf(eA, "eA", (torch.uint8,), M * (K // 32))
+    peB = _buf(eB, "eB", (torch.uint8,), N * (K // 32))
+    pD, out, ldD = _out_mat(D, M, N)
+    _check("fp8_mx_gemm", L.fp8_mx_gemm(M, N, K, pA, fmtA, peA, pB, fmtB, peB, pD, out, ldD, _stream(stream)))
 
 
 def grouped_gemm(offsets, A, sA, B, sB, D, stream=None):

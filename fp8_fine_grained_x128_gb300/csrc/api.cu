@@ -276,6 +276,29 @@ FP8FG_API int fp8_blockscaled_gemm(int64_t M, int64_t N, int64_t K, const void *
     return launch_gemm(M, N, K, A, fmtA, sA, granA, B, fmtB, sB, granB, D, out_dtype, ldD, st, S(stream));
 }
 
+FP8FG_API int fp8_mx_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const uint8_t *eA,
+                          const void *B, int fmtB, const uint8_t *eB, void *D, int out_dtype, int64_t ldD,
+                          void *stream)
+{
+    if (!fmt_ok(fmtA) || !fmt_ok(fmtB)) return FP8_ERR_INVALID_ARG;
+    if (out_dtype != FP8_OUT_BF16 && out_dtype != FP8_OUT_F32) return FP8_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || M % 128 != 0 || N % 128 != 0 || K % 128 != 0) return FP8_ERR_SHAPE;
+    if (M >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31)) return FP8_ERR_SHAPE;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (!D) return FP8_ERR_INVALID_ARG;
+    if (ldD < N) return FP8_ERR_SHAPE;
+    const int64_t esz = out_dtype == FP8_OUT_F32 ? 4 : 2;
+    if (!aligned16(D) || (ldD * esz) % 16 != 0) return FP8_ERR_ALIGNMENT;
+    if (K > 0) {
+        if (!A || !B || !eA || !eB) return FP8_ERR_INVALID_ARG;
+        if (!aligned16(A) || !aligned16(B) || (reinterpret_cast<uintptr_t>(eA) & 3u) ||
+            (reinterpret_cast<uintptr_t>(eB) & 3u))
+            return FP8_ERR_ALIGNMENT;
+    }
+    FP8FG_STATUS_OR_RETURN(st);
+    return launch_gemm_mx(M, N, K, A, fmtA, eA, B, fmtB, eB, D, out_dtype, ldD, st, S(stream));
+}
+
 FP8FG_API int fp8_grouped_gemm(int G, const int32_t *group_offsets, int64_t M_capacity, int64_t N, int64_t K,
                                const void *A, const float *sA, const void *B, const float *sB, void *D, int out_dtype,
                                int64_t ldD, void *stream)

@@ -171,6 +171,13 @@ struct Divider2 {
     }
 };
 
+// MXFP8 block scale X = 2^(e8 - 127) from its 8-bit exponent code (e8 = 0 is
+// the subnormal 2^-127).
+__device__ __forceinline__ float mx_scale_value(uint32_t e8)
+{
+    return e8 ? __uint_as_float(e8 << 23) : __uint_as_float(0x00400000u);
+}
+
 // SwiGLU element math (SwiGLU(g, u) = g * sigmoid(g) * u and its gradients),
 // shared by the standalone SwiGLU kernels and the quantizers that compute
 // SwiGLU while loading, so both round identically.  The 8-wide forms below

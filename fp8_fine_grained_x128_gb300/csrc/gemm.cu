@@ -57,6 +57,7 @@ constexpr int kEpiWarp0 = 4;          // first epilogue warp (warpgroups 1 and 2
 // scales beside its accumulators)
 template <int SBG> struct RegSplit { static constexpr int kCtrl = 144, kEpi = 176; };
 template <> struct RegSplit<1> { static constexpr int kCtrl = 64, kEpi = 216; };
+template <> struct RegSplit<2> { static constexpr int kCtrl = 64, kEpi = 216; };
 // the split must fit the registers the CTA is launched with
 template <int SBG>
 constexpr int regs_needed_at_launch()
@@ -84,9 +85,18 @@ struct GemmArgs {
     int G;
     int *status;
     int raster_gm;        // M-tiles per raster band
+    const uint8_t *eA;    // MXFP8: scale exponents [M][K/32] and [N][K/32] (X = 2^(e - 127))
+    const uint8_t *eB;
+    int64_t ldE;          // K / 32
 };
 
-enum { SB_BLOCK = 0, SB_ROW = 1 };
+// Scale modes of the promotion: the 1x128 recipe with 128x128 B (one scalar
+// per column half), with 1x128 B (one value per column), and MXFP8 (one
+// power-of-two scale per 32-block of each row of A and of B: every MMA of
+// K = 32 is its own promotion chunk).
+enum { SB_BLOCK = 0, SB_ROW = 1, SB_MX = 2 };
+// MMAs (K = 32 each) per promotion chunk
+template <int SBG> constexpr int chunk_mmas() { return SBG == SB_MX ? 1 : 4; }
 // Grouping of the tiles: none; by rows of A (MoE forward/dgrad: each M tile
 // belongs to one expert, whose B it uses); by K (MoE wgrad: each expert's
 // output is a full M x N matrix contracted over that expert's K chunks only).
@@ -318,6 +328,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int kb = 0; kb < nk; ++kb) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
+                    if (SBG == SB_MX) {
+                        // each 32-deep block into an accumulator of its own
+                        if (!wait_or_abort(&full[s], ph, abort_flag, a.status)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(smem + s * L::kStage));
+                        const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * L::kStage + L::kA));
+                        for (int k = 0; k < 4 && ok; ++k) {
+                            buf = cc % L::kNbuf;
+                            if (!wait_or_abort(&tempty[buf], ((cc / L::kNbuf) & 1) ^ 1, abort_flag, a.status)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            tc_mma_f8f6f4(tmem_base + buf * BN, adesc + 2 * k, bdesc + 2 * k, idesc, 0u);
+                            tc_commit(&tfull[buf]);
+                            ++cc;
+                        }
+                        if (!ok) break;
+                        tc_commit(&empty[s]);
+                        ++it;
+                        continue;
+                    }
                     if (PROMOTE) {
                         buf = cc % L::kNbuf;
                         if (!wait_or_abort(&tempty[buf], ((cc / L::kNbuf) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
@@ -351,6 +383,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // every MMA issued by this thread completes before the CTA frees TMEM
             tc_commit(mma_done);
             mbar_wait_bounded(mma_done, 0, nullptr);
+        } else if (SBG == SB_MX && warp == 2) {
+            // -------------------------------------------------- MX scale producer
+            // The whole warp: per 128-deep stage it loads the 4 exponent bytes of
+            // each of the tile's 128 rows of A and BN rows of B (one 32-bit load
+            // per row: [rows][K/32] layout), then for each of the stage's four
+            // 32-blocks writes X = 2^(e - 127) of every row into a slot (rows of A
+            // at [0, 128), rows of B at [256, 256 + BN)).
+            uint32_t cs = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const TileInfo ti = tile_info<BN, GMODE>(tile, num_mt, num_nt, a, sh_off);
+                for (int kb = ti.kg0; kb < ti.kg0 + ti.nk && ok; ++kb) {
+                    uint32_t ea[4], eb[BN / 32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        ea[i] = *reinterpret_cast<const uint32_t *>(a.eA + (int64_t)(ti.a_row + lane + 32 * i) * a.ldE +
+                                                                    4 * kb);
+#pragma unroll
+                    for (int i = 0; i < BN / 32; ++i)
+                        eb[i] = *reinterpret_cast<const uint32_t *>(a.eB + (int64_t)(ti.b_row + lane + 32 * i) * a.ldE +
+                                                                    4 * kb);
+                    for (int j = 0; j < 4; ++j, ++cs) {
+                        const int slot = cs % kScaleDepth;
+                        if (!warp_wait_or_abort(&sc_empty[slot], ((cs / kScaleDepth) & 1) ^ 1, abort_flag, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        float *sv = scl + slot * L::kScaleSlotFloats;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) sv[lane + 32 * i] = mx_scale_value((ea[i] >> (8 * j)) & 0xFFu);
+#pragma unroll
+                        for (int i = 0; i < BN / 32; ++i)
+                            sv[256 + lane + 32 * i] = mx_scale_value((eb[i] >> (8 * j)) & 0xFFu);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sc_full[slot]);
+                    }
+                }
+            }
         } else if (PROMOTE && warp == 2 && lane == 0) {
             // -------------------------------------------------- scale producer
             // Slot layout: [0, 128) sA of the tile's rows (1x128 A) or [128]
@@ -413,7 +483,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 uint64_t acc[NP];
 #pragma unroll
                 for (int i = 0; i < NP; ++i) acc[i] = 0ull;
-                for (int kb = 0; kb < ti.nk; ++kb) {
+                const int nchunks = ti.nk * (4 / chunk_mmas<SBG>());
+                for (int kb = 0; kb < nchunks; ++kb) {
                     const uint32_t buf = cc % L::kNbuf;
                     const int slot = cc % kScaleDepth;
                     if (!warp_wait_or_abort(&sc_full[slot], (cc / kScaleDepth) & 1, abort_flag, a.status)) { ok = false; break; }
@@ -705,6 +776,46 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const 
         if (granB == FP8_GRAN_1x128) return run_gemm<128, 6, true, SB_ROW, G_NONE>(mA, mB, mA, idesc, g, grid, st);
         return run_gemm<128, 6, true, SB_BLOCK, G_NONE>(mA, mB, mA, idesc, g, grid, st);
     }
+}
+
+// MXFP8: every 32-deep block of K is multiplied into an accumulator of its own
+// and promoted with X_A(m, b) * X_B(n, b) = 2^(eA + eB - 254).
+int launch_gemm_mx(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const uint8_t *eA, const void *B,
+                   int fmtB, const uint8_t *eB, void *D, int out_dtype, int64_t ldD, int *status, cudaStream_t st)
+{
+    if (M == 0 || N == 0) return FP8_OK;
+    if (K == 0) {
+        const size_t esz = out_dtype == FP8_OUT_F32 ? 4 : 2;
+        return cudaMemset2DAsync(D, (size_t)ldD * esz, 0, (size_t)N * esz, (size_t)M, st) == cudaSuccess
+                   ? FP8_OK
+                   : FP8_ERR_CUDA;
+    }
+    const int BN = (N % 256 == 0) ? 256 : 128;
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, A, (uint64_t)K, (uint64_t)M, 128) || !make_map(&mB, B, (uint64_t)K, (uint64_t)N, BN))
+        return FP8_ERR_CUDA;
+    GemmArgs g{};
+    g.M = (int)M;
+    g.N = (int)N;
+    g.K = (int)K;
+    g.granA = FP8_GRAN_1x128;   // per-row scales of A in the slot
+    g.D = D;
+    g.ldD = ldD;
+    g.out_f32 = out_dtype == FP8_OUT_F32;
+    g.status = status;
+    g.eA = eA;
+    g.eB = eB;
+    g.ldE = K / 32;
+    {
+        int64_t gm = ((int64_t)32 << 20) / (128 * K);
+        gm = std::max<int64_t>(8, std::min<int64_t>(gm, M / 128));
+        g.raster_gm = (int)gm;
+    }
+    const int64_t ntiles = (M / 128) * (N / BN);
+    const int grid = (int)std::min<int64_t>(ntiles, sm_count());
+    const uint32_t idesc = idesc_f8f6f4(fmtA, fmtB, 128, BN);
+    if (BN == 256) return run_gemm<256, 4, true, SB_MX, G_NONE>(mA, mB, mA, idesc, g, grid, st);
+    return run_gemm<128, 6, true, SB_MX, G_NONE>(mA, mB, mA, idesc, g, grid, st);
 }
 
 int launch_grouped_gemm(int G, const int32_t *offsets, int64_t Mcap, int64_t N, int64_t K, const void *A,

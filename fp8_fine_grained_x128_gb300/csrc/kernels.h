@@ -49,6 +49,8 @@ int launch_selftest_wait(int timeout_ms, int *status, cudaStream_t st);
 int launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const float *sA, int granA,
                 const void *B, int fmtB, const float *sB, int granB, void *D, int out_dtype, int64_t ldD,
                 int *status, cudaStream_t st);
+int launch_gemm_mx(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const uint8_t *eA, const void *B,
+                   int fmtB, const uint8_t *eB, void *D, int out_dtype, int64_t ldD, int *status, cudaStream_t st);
 int launch_grouped_gemm(int G, const int32_t *offsets, int64_t Mcap, int64_t N, int64_t K, const void *A,
                         const float *sA, const void *B, const float *sB, void *D, int out_dtype, int64_t ldD,
                         int *status, cudaStream_t st);

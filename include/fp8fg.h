@@ -219,6 +219,23 @@ FP8FG_API int fp8_quant_pertensor_current(const void *x, int64_t rows, int64_t c
 FP8FG_API int fp8_quant_mx(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt,
                            void *q, uint8_t *e8, void *stream);
 
+/* MXFP8 GEMM ([Infra] "Scaling strategies and stability": per-block scaling,
+ * each block of a tensor with its own scale factor; "Blackwell MXFP8 and
+ * NVFP4: looking ahead"; block and scale encoding per the readings of
+ * fp8_quant_mx): D = A . B^T with A [M][K] and B [N][K] FP8 codes (fmtA,
+ * fmtB), K contiguous, and their scale exponents eA [M][K/32], eB [N][K/32]
+ * as fp8_quant_mx writes them (X = 2^(e - 127)):
+ *   D[m][n] = sum_b X_A(m, b) * X_B(n, b) * sum_{k in 32-block b} qA[m][k] * qB[n][k].
+ * Every 32-block is multiplied on the tensor cores into an FP32 accumulator
+ * of its own and promoted into an FP32 running sum with its two scales (the
+ * same scheme as fp8_blockscaled_gemm's 128-deep chunks, four times as
+ * often).  D [M][ldD] BF16 (RN) or FP32.  M, N, K % 128 == 0; A, B, D
+ * 16-byte aligned, eA, eB 4-byte aligned, ldD * element size a multiple of
+ * 16 bytes.  K == 0 writes zeros; M or N == 0 is a no-op. */
+FP8FG_API int fp8_mx_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const uint8_t *eA,
+                          const void *B, int fmtB, const uint8_t *eB, void *D, int out_dtype, int64_t ldD,
+                          void *stream);
+
 /* The same delayed-scaling step for callers that cannot allocate device
  * memory -- for example code that runs inside another framework's fixed
  * memory plan or arena, or a plugin that is handed buffers but no allocator.
