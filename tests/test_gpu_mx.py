@@ -91,3 +91,91 @@ def test_mx_quant_mlp_activation_full_size():
     assert_status_ok()
     rq, re8, _ = mx.quant_mx(xb, oracle.E4M3)
     assert np.array_equal(e8, re8) and np.array_equal(q, rq)
+
+
+# ---------------------------------------------------------------- MXFP8 GEMM
+
+def mx_operand(rows, K, seed, fmt, std=1.0):
+    xb = synth.bf16_normal((rows, K), seed, std, 1e-3, 50.0)
+    q, e8, st = mx.quant_mx(xb, fmt)
+    assert st == oracle.OK
+    return q, e8
+
+
+def run_mx_gemm(qa, ea, fa, qb, eb, fb, out_dtype):
+    from gpu_helpers import dev_u8, guarded
+    M, N = qa.shape[0], qb.shape[0]
+    D = guarded((M, N), out_dtype)
+    fg.mx_gemm(dev_u8(qa), fa, dev_u8(ea), dev_u8(qb), fb, dev_u8(eb), D)
+    assert_status_ok()
+    return D
+
+
+MX_CASES = [
+    # name, M, N, K, fmtA, fmtB: BN = 256 and BN = 128 tiles, several waves of tiles, E5M2 operands
+    ("bn256", 256, 512, 512, oracle.E4M3, oracle.E4M3),
+    ("bn128_tail", 384, 384, 640, oracle.E4M3, oracle.E4M3),
+    ("waves", 1024, 1536, 1024, oracle.E4M3, oracle.E4M3),
+    ("e5m2_a", 256, 256, 384, oracle.E5M2, oracle.E4M3),
+]
+
+
+@pytest.mark.parametrize("case", MX_CASES, ids=[c[0] for c in MX_CASES])
+def test_mx_gemm_full_compare(case):
+    """Every output against the oracle's exact per-32-block sum (R16), FP32
+    and BF16 outputs; the BF16 output is the RNE rounding of the FP32 one."""
+    from gpu_helpers import bf16_to_f64, gemm_tolerance_check, host_u16
+    name, M, N, K, fa, fb = case
+    qa, ea = mx_operand(M, K, 51, fa)
+    qb, eb = mx_operand(N, K, 52, fb, std=0.5)
+    ref = mx.mx_gemm_full(qa, ea, fa, qb, eb, fb)
+    d32 = run_mx_gemm(qa, ea, fa, qb, eb, fb, torch.float32)
+    gemm_tolerance_check(d32.cpu().numpy().astype(np.float64), ref, bf16_out=False)
+    d16 = run_mx_gemm(qa, ea, fa, qb, eb, fb, torch.bfloat16)
+    gemm_tolerance_check(bf16_to_f64(host_u16(d16)), ref, bf16_out=True)
+    assert torch.equal(d16, d32.to(torch.bfloat16))
+
+
+def test_mx_gemm_block_scales_are_applied_per_32_block():
+    """Operands whose 32-blocks carry very different exponents (2^-20 .. 2^20
+    within one row): a scale applied per 128-chunk or per row instead of per
+    32-block would be far off."""
+    from gpu_helpers import gemm_tolerance_check
+    rng = np.random.default_rng(5)
+    M, N, K = 256, 256, 256
+    qa = rng.integers(0, 0x7E, (M, K), dtype=np.uint8) | (rng.integers(0, 2, (M, K), dtype=np.uint8) << 7)
+    qb = rng.integers(0, 0x7E, (N, K), dtype=np.uint8) | (rng.integers(0, 2, (N, K), dtype=np.uint8) << 7)
+    ea = rng.integers(127 - 20, 127 + 20, (M, K // 32), dtype=np.uint8)
+    eb = rng.integers(127 - 20, 127 + 20, (N, K // 32), dtype=np.uint8)
+    ref = mx.mx_gemm_full(qa, ea, oracle.E4M3, qb, eb, oracle.E4M3)
+    d32 = run_mx_gemm(qa, ea, oracle.E4M3, qb, eb, oracle.E4M3, torch.float32)
+    gemm_tolerance_check(d32.cpu().numpy().astype(np.float64), ref, bf16_out=False)
+
+
+def test_mx_gemm_headline_shape_sampled():
+    """The block-scaled GEMM's headline shape, 8192 x 28672 x 4096: X and W_gu
+    of the MLP step quantized to MXFP8 on the GPU (the quantizer is pinned
+    bit-exactly above), then the GEMM against the oracle's exact per-block
+    sum from the GPU's own codes and exponents on >= 2^20 stratified outputs
+    (every 128 x 128 tile hit >= 16 times)."""
+    from gpu_helpers import bf16_to_f64, gemm_tolerance_check, host_u16, sample_points_dense
+    M, N, K = 8192, 28672, 4096
+    xb = synth.bf16_normal((M, K), 0, 1.0, 1e-3, 50.0)
+    wb = synth.bf16_normal((N, K), 1000, 0.02)
+    ops = []
+    for bits in (xb, wb):
+        R = bits.shape[0]
+        q = torch.empty((R, K), dtype=torch.uint8, device="cuda")
+        e8 = torch.empty((R, K // 32), dtype=torch.uint8, device="cuda")
+        fg.quant_mx(dev_bf16(bits), fg.E4M3, q, e8)
+        ops.append((q, e8))
+    assert_status_ok()
+    (qa, ea), (qb, eb) = ops
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    fg.mx_gemm(qa, fg.E4M3, ea, qb, fg.E4M3, eb, D)
+    assert_status_ok()
+    pm, pn = sample_points_dense(M, N, seed=9)
+    ref = mx.mx_gemm_points(qa.cpu().numpy(), ea.cpu().numpy(), oracle.E4M3, qb.cpu().numpy(), eb.cpu().numpy(),
+                            oracle.E4M3, pm, pn)
+    got = D[torch.from_numpy(pm).cuda(), torch.from_numpy(pn).cuda()]
+    gemm_tolerance_check(bf16_to_f64(host_u16(got)), ref, bf16_out=True)
