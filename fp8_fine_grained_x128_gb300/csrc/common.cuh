@@ -468,6 +468,76 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     return false;
 }
 
+// Barrier operations on a shared-memory address computed once (the hot loops
+// keep barrier and buffer addresses as 32-bit shared addresses).
+__device__ __forceinline__ bool mbar_try_wait_a(uint32_t addr, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive_a(uint32_t addr)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+// The slow path of warp_wait_a: every lane polls with the bounded-wait rules
+// of mbar_wait_bounded; out of line so the hot loop stays small.
+static __device__ __noinline__ bool warp_wait_slow_a(uint32_t addr, uint32_t parity, volatile int *abort_flag,
+                                                     int *status)
+{
+    const uint64_t t0 = globaltimer_ns();
+    bool ok = false;
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_a(addr, parity)) {
+            ok = true;
+            break;
+        }
+        if ((i & 63u) == 0u) {
+            if (*abort_flag) break;
+            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                if (!*abort_flag) {
+                    *abort_flag = 1;
+                    set_status(status, FP8_ERR_TIMEOUT);
+                }
+                break;
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// A whole warp waits on the barrier at `addr` (see warp_wait_or_abort).
+__device__ __forceinline__ bool warp_wait_a(uint32_t addr, uint32_t parity, volatile int *abort_flag, int *status)
+{
+    if (__all_sync(0xffffffffu, mbar_try_wait_a(addr, parity))) return true;
+    return warp_wait_slow_a(addr, parity, abort_flag, status);
+}
+
+// Shared-memory loads at a 32-bit shared address plus a constant offset.
+template <int OFF>
+__device__ __forceinline__ float lds_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(addr), "n"(OFF) : "memory");
+    return v;
+}
+
+template <int OFF>
+__device__ __forceinline__ uint64_t lds_b64(uint32_t addr)
+{
+    uint64_t v;
+    asm volatile("ld.shared.b64 %0, [%1+%2];" : "=l"(v) : "r"(addr), "n"(OFF) : "memory");
+    return v;
+}
+
 // A whole warp waits: every lane polls the barrier, so the warp never splits
 // into a single-lane spin loop, and a vote makes the outcome warp-uniform so
 // the warp stays converged for the .sync.aligned tcgen05 instructions that

@@ -473,6 +473,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int colbase = (ew >> 2) * HALF;
         const int row = lg * 32 + lane;
         const uint32_t tm_lane = tmem_base + ((uint32_t)(lg * 32) << 16);
+        // Addresses the chunk loop uses, computed once: barriers and the scale
+        // ring as 32-bit shared addresses, this thread's byte offsets inside a
+        // scale slot (row scale, column-half scale, the 4 row scales and the
+        // column-scale pairs of the 16x256b fragments), and its TMEM columns.
+        const uint32_t tfull_a = smem_u32(tfull), tempty_a = smem_u32(tempty);
+        const uint32_t scf_a = smem_u32(sc_full), sce_a = smem_u32(sc_empty);
+        const uint32_t scl_a = smem_u32(scl);
+        const uint32_t off_ra = 4u * (a.granA == FP8_GRAN_1x128 ? row : 128);
+        const uint32_t off_rb = 4u * (256 + (colbase >> 7));
+        const uint32_t off_rq = 4u * (a.granA == FP8_GRAN_1x128 ? (lg * 32 + (lane >> 2)) : 128);
+        const uint32_t rq_step = a.granA == FP8_GRAN_1x128 ? 32u : 0u;
+        const uint32_t off_col = 4u * (256 + colbase + 2 * (lane & 3));
+        const uint32_t tm_row = tm_lane + colbase;                          // 32x32b: this warp's lanes
+        const uint32_t tm_q0 = tm_lane + colbase, tm_q1 = tm_q0 + (16u << 16);   // 16x256b: lanes 0-15, 16-31
         uint32_t cc = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
@@ -485,24 +499,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int i = 0; i < NP; ++i) acc[i] = 0ull;
                 const int nchunks = ti.nk * (4 / chunk_mmas<SBG>());
                 for (int kb = 0; kb < nchunks; ++kb) {
-                    const uint32_t buf = cc % L::kNbuf;
-                    const int slot = cc % kScaleDepth;
-                    if (!warp_wait_or_abort(&sc_full[slot], (cc / kScaleDepth) & 1, abort_flag, a.status)) { ok = false; break; }
-                    const float *sv = scl + slot * L::kScaleSlotFloats;
-                    // 128x128 B: sA*sB of this thread's row and column half; 1x128 B: sA of the row
-                    float sr = sv[a.granA == FP8_GRAN_1x128 ? row : 128];
-                    if (SBG == SB_BLOCK) sr *= sv[256 + (ew >> 2)];
-                    if (!warp_wait_or_abort(&tfull[buf], (cc / L::kNbuf) & 1, abort_flag, a.status)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint64_t s2 = f2_pack(sr, sr);
+                    const uint32_t buf = cc & (L::kNbuf - 1);
+                    const uint32_t slot = cc & (kScaleDepth - 1);
+                    const uint32_t bpar = (cc / L::kNbuf) & 1, spar = (cc / kScaleDepth) & 1;
+                    if (!warp_wait_a(scf_a + 8 * slot, spar, abort_flag, a.status)) { ok = false; break; }
+                    const uint32_t sva = scl_a + slot * (L::kScaleSlotFloats * 4);
                     if (SBG == SB_BLOCK) {
+                        // sA * sB of this thread's row and column half
+                        const float sr = lds_f32<0>(sva + off_ra) * lds_f32<0>(sva + off_rb);
+                        if (!warp_wait_a(tfull_a + 8 * buf, bpar, abort_flag, a.status)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t s2 = f2_pack(sr, sr);
+                        const uint32_t tb = tm_row + buf * BN;
                         // 16 columns per wait: the 128 accumulator registers and the
                         // staging registers fit the epilogue's budget with room to spare
-                        // (two x32 loads per wait measured 8% slower, x8 loads 13%)
+                        // (two x32 loads per wait measured 8% slower, x8 loads 13%, and
+                        // loading the next 16 columns before this round's FMAs 12%)
 #pragma unroll
                         for (int j = 0; j < HALF / 16; ++j) {
                             uint32_t r0[16];
-                            tc_ld_32x32b_x16(tm_lane + buf * BN + colbase + j * 16, r0);
+                            tc_ld_32x32b_x16(tb + j * 16, r0);
                             tc_wait_ld();
 #pragma unroll
                             for (int i = 0; i < 8; ++i)
@@ -518,23 +534,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         uint64_t sa2[4];
 #pragma unroll
                         for (int rr = 0; rr < 4; ++rr) {
-                            const float v = sv[a.granA == FP8_GRAN_1x128 ? lg * 32 + rr * 8 + (lane >> 2) : 128];
+                            const float v = lds_f32<0>(sva + off_rq + rr * rq_step);
                             sa2[rr] = f2_pack(v, v);
                         }
+                        if (!warp_wait_a(tfull_a + 8 * buf, bpar, abort_flag, a.status)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t scol = sva + off_col;
 #pragma unroll
                         for (int c2 = 0; c2 < HALF / 32; ++c2) {
                             uint64_t sbv[4];   // column-scale pairs of this thread's 4 eight-column groups
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                sbv[i] = *reinterpret_cast<const uint64_t *>(sv + 256 + colbase + 32 * c2 + 8 * i +
-                                                                             2 * (lane & 3));
+                            sbv[0] = lds_b64<0>(scol + 128 * c2);
+                            sbv[1] = lds_b64<32>(scol + 128 * c2);
+                            sbv[2] = lds_b64<64>(scol + 128 * c2);
+                            sbv[3] = lds_b64<96>(scol + 128 * c2);
                             // one 16-lane half of the quarter (32 columns) per wait
 #pragma unroll
                             for (int hh = 0; hh < 2; ++hh) {
                                 uint32_t p0[16];
-                                tc_ld_16x256b_x4(tmem_base + ((uint32_t)(lg * 32 + 16 * hh) << 16) + buf * BN + colbase +
-                                                     32 * c2,
-                                                 p0);
+                                tc_ld_16x256b_x4((hh ? tm_q1 : tm_q0) + buf * BN + 32 * c2, p0);
                                 tc_wait_ld();
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
@@ -551,8 +568,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(&tempty[buf]);
-                        mbar_arrive(&sc_empty[slot]);
+                        mbar_arrive_a(tempty_a + 8 * buf);
+                        mbar_arrive_a(sce_a + 8 * slot);
                     }
                     ++cc;
                 }
