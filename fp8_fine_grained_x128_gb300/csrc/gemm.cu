@@ -528,9 +528,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         // per-column scales sB(n, kb).  16x256b fragments: each
                         // thread holds rows {16h + q, 16h + q + 8} (q = lane / 4,
                         // h = 0, 1) of its lane quarter and columns 8i + 2(lane % 4)
-                        // + {0, 1}, so it reads 1/4 of the column scales.  32
-                        // columns of one 16-lane half per wait (two 64-column x8
-                        // loads per wait were 13% slower on the grouped wgrad).
+                        // + {0, 1}, so it reads 1/4 of the column scales.  64
+                        // columns of one 16-lane half per wait (x8); 32 per wait
+                        // (x4) measured 4% slower on the dense wgrad.
                         uint64_t sa2[4];
 #pragma unroll
                         for (int rr = 0; rr < 4; ++rr) {
@@ -540,22 +540,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if (!warp_wait_a(tfull_a + 8 * buf, bpar, abort_flag, a.status)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t scol = sva + off_col;
+                        static_assert(HALF % 64 == 0, "the per-column drain reads 64 columns per load");
 #pragma unroll
-                        for (int c2 = 0; c2 < HALF / 32; ++c2) {
-                            uint64_t sbv[4];   // column-scale pairs of this thread's 4 eight-column groups
-                            sbv[0] = lds_b64<0>(scol + 128 * c2);
-                            sbv[1] = lds_b64<32>(scol + 128 * c2);
-                            sbv[2] = lds_b64<64>(scol + 128 * c2);
-                            sbv[3] = lds_b64<96>(scol + 128 * c2);
-                            // one 16-lane half of the quarter (32 columns) per wait
+                        for (int c4 = 0; c4 < HALF / 64; ++c4) {
+                            uint64_t sbv[8];   // column-scale pairs of this thread's 8 eight-column groups
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) sbv[i] = lds_b64<0>(scol + 256 * c4 + 32 * i);
 #pragma unroll
                             for (int hh = 0; hh < 2; ++hh) {
-                                uint32_t p0[16];
-                                tc_ld_16x256b_x4((hh ? tm_q1 : tm_q0) + buf * BN + 32 * c2, p0);
+                                uint32_t p0[32];
+                                tc_ld_16x256b_x8((hh ? tm_q1 : tm_q0) + buf * BN + 64 * c4, p0);
                                 tc_wait_ld();
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    uint64_t *ac = acc + 4 * c2 + i;
+                                for (int i = 0; i < 8; ++i) {
+                                    uint64_t *ac = acc + 8 * c4 + i;
                                     ac[(2 * hh) * (HALF / 8)] = f2_fma(f2_mul_bits(p0[4 * i], p0[4 * i + 1], sbv[i]),
                                                                        sa2[2 * hh], ac[(2 * hh) * (HALF / 8)]);
                                     ac[(2 * hh + 1) * (HALF / 8)] =
