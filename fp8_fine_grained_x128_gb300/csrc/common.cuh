@@ -615,9 +615,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 // ------------------------------------------------------------------ tcgen05
 
 // Tiles are walked in bands of GM M-tiles, M fastest: a band's A rows stay in
-// L2 while every B tile is streamed through it once per band.
+// L2 while every B tile is streamed through it once per band.  GM = 0 walks N
+// fastest instead (each M-tile's row of tiles in turn), which keeps all of B
+// in L2 and streams A once.
 __device__ __forceinline__ void tile_coords_raster(int tile, int num_mt, int num_nt, int GM, int &mt, int &nt)
 {
+    if (GM == 0) {
+        mt = tile / num_nt;
+        nt = tile - mt * num_nt;
+        return;
+    }
     const int group = tile / (GM * num_nt);
     const int first = group * GM;
     const int gm = min(GM, num_mt - first);

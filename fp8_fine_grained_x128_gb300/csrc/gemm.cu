@@ -84,7 +84,7 @@ struct GemmArgs {
     const int32_t *offsets;
     int G;
     int *status;
-    int raster_gm;        // M-tiles per raster band
+    int raster_gm;        // M-tiles per raster band (0: N fastest)
     const uint8_t *eA;    // MXFP8: scale exponents [M][K/32] and [N][K/32] (X = 2^(e - 127))
     const uint8_t *eB;
     int64_t ldE;          // K / 32
@@ -764,12 +764,7 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const 
     g.ldD = ldD;
     g.out_f32 = out_dtype == FP8_OUT_F32;
     g.status = status;
-    // the band's A rows (GM x 128 x K bytes) should stay well inside L2
-    {
-        int64_t gm = ((int64_t)32 << 20) / (128 * K);
-        gm = std::max<int64_t>(8, std::min<int64_t>(gm, M / 128));
-        g.raster_gm = (int)gm;
-    }
+    g.raster_gm = raster_band(M, M * K, N * K);
     const int64_t ntiles = (M / 128) * (N / BN);
     const int grid = (int)std::min<int64_t>(ntiles, sm_count());
     const bool tensor = granA == FP8_GRAN_TENSOR;
@@ -821,11 +816,7 @@ int launch_gemm_mx(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, con
     g.eA = eA;
     g.eB = eB;
     g.ldE = K / 32;
-    {
-        int64_t gm = ((int64_t)32 << 20) / (128 * K);
-        gm = std::max<int64_t>(8, std::min<int64_t>(gm, M / 128));
-        g.raster_gm = (int)gm;
-    }
+    g.raster_gm = raster_band(M, M * K, N * K);
     const int64_t ntiles = (M / 128) * (N / BN);
     const int grid = (int)std::min<int64_t>(ntiles, sm_count());
     const uint32_t idesc = idesc_f8f6f4(fmtA, fmtB, 128, BN);

@@ -312,12 +312,7 @@ int launch_wgrad_recompute_error(int64_t M, int64_t N, int64_t K, const void *dY
     g.ldD = ldD;
     g.err = err;
     g.status = status;
-    // a band of output rows keeps its dY columns (GM x 128 x M x 2 bytes) in L2
-    {
-        int64_t gm = ((int64_t)32 << 20) / (128 * 2 * M);
-        gm = std::max<int64_t>(1, std::min<int64_t>(gm, N / 128));
-        g.raster_gm = (int)gm;
-    }
+    g.raster_gm = raster_band(N, N * M * 2, K * M * 2);
     const int64_t ntiles = (N / 128) * (K / BN);
     const int grid = (int)std::min<int64_t>(ntiles, sm_count());
     if (BN == 256) return run_dw<256>(mA, mB, g, grid, st);
