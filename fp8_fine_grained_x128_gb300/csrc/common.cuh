@@ -215,6 +215,37 @@ __device__ __forceinline__ float min_gate8(uint4 g4)
     return m;
 }
 
+// Packed FP32 pair helpers for the SwiGLU gradient (each lane rounds like the
+// scalar instruction).  The gradient's eight multiplies and adds per value run
+// as four packed ones (the fused backward quantizer: 298 -> 287 us on dGU
+// 8192x28672); the forward's three are faster scalar (161 vs 170 us packed).
+__device__ __forceinline__ uint64_t p2(float lo, float hi)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ uint64_t p2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t p2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t p2_bf16(uint64_t v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return bf16x2_rn(lo, hi);
+}
+// the (lo, hi) BF16 halves of a word as a packed FP32 pair
+__device__ __forceinline__ uint64_t p2_bf16x2(uint32_t w) { return p2(bf16_lo(w), bf16_hi(w)); }
+
 template <bool LEFT>
 __device__ __forceinline__ uint4 swiglu8_impl(uint4 g4, uint4 u4)
 {
@@ -247,11 +278,23 @@ __device__ __forceinline__ Uint4x2 swiglu_grad8_impl(uint4 g4, uint4 u4, uint4 d
     uint32_t og[4], ou[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        float dg0, du0, dg1, du1;
-        swiglu_grad<LEFT>(bf16_lo(gw[k]), bf16_lo(uw[k]), bf16_lo(dw[k]), dg0, du0);
-        swiglu_grad<LEFT>(bf16_hi(gw[k]), bf16_hi(uw[k]), bf16_hi(dw[k]), dg1, du1);
-        og[k] = bf16x2_rn(dg0, dg1);
-        ou[k] = bf16x2_rn(du0, du1);
+        if (LEFT) {
+            float dg0, du0, dg1, du1;
+            swiglu_grad<true>(bf16_lo(gw[k]), bf16_lo(uw[k]), bf16_lo(dw[k]), dg0, du0);
+            swiglu_grad<true>(bf16_hi(gw[k]), bf16_hi(uw[k]), bf16_hi(dw[k]), dg1, du1);
+            og[k] = bf16x2_rn(dg0, dg1);
+            ou[k] = bf16x2_rn(du0, du1);
+        } else {
+            // dg = d * u * sig * (1 + g * (1 - sig)), du = d * g * sig on packed pairs
+            const float g0 = bf16_lo(gw[k]), g1 = bf16_hi(gw[k]);
+            const uint64_t g = p2(g0, g1), u = p2_bf16x2(uw[k]), d = p2_bf16x2(dw[k]);
+            const uint64_t sg = p2(swiglu_sigmoid<false>(g0), swiglu_sigmoid<false>(g1));
+            const uint64_t one = p2(1.0f, 1.0f);
+            const uint64_t oms = p2_fma(sg, p2(-1.0f, -1.0f), one);   // 1 - sig
+            const uint64_t w = p2_fma(g, oms, one);                   // 1 + g (1 - sig)
+            og[k] = p2_bf16(p2_mul(p2_mul(p2_mul(d, u), sg), w));
+            ou[k] = p2_bf16(p2_mul(p2_mul(d, g), sg));
+        }
     }
     return {make_uint4(og[0], og[1], og[2], og[3]), make_uint4(ou[0], ou[1], ou[2], ou[3])};
 }
