@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         // 16 columns per wait: the 128 accumulator registers and the
                         // staging registers fit the epilogue's budget with room to spare
                         // (two x32 loads per wait measured 8% slower, x8 loads 13%, and
-                        // loading the next 16 columns before this round's FMAs 12%)
+                        // loading the next 16 columns before the current group's FMAs 12%)
 #pragma unroll
                         for (int j = 0; j < HALF / 16; ++j) {
                             uint32_t r0[16];
