@@ -44,9 +44,14 @@ ERR_UNSUPPORTED = 4
 ERR_CUDA = 5
 ERR_NONFINITE = 6
 ERR_TIMEOUT = 7
+ERR_BOUNDS = 8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libfp8fg.so")
+# FP8FG_DEBUG=1 in the environment selects the index-checked debug build
+# (every kernel store checked against its buffer's extent; FP8_ERR_BOUNDS in
+# the status word on a miss), built by `python -m fp8_fine_grained_x128_gb300.build --debug`.
+DEBUG = os.environ.get("FP8FG_DEBUG", "0") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "libfp8fg_debug.so" if DEBUG else "libfp8fg.so")
 _lib = None
 
 
@@ -78,6 +83,8 @@ _SIGS = {
     "fp8_status_string": (ctypes.c_char_p, [_INT]),
     "fp8_device_status": (_INT, [_VP, ctypes.POINTER(_INT)]),
     "fp8_selftest_wait_timeout": (_INT, [_INT, _VP]),
+    "fp8_debug_build": (_INT, []),
+    "fp8_selftest_bounds": (_INT, [_VP, _I64, _I64, _VP]),
     "fp8_quant_1x128": (_INT, [_VP, _I64, _I64, _I64, _INT, _VP, _VP, _VP, _VP, _VP]),
     "fp8_quant_128x128": (_INT, [_VP, _I64, _I64, _I64, _INT, _VP, _VP, _VP, _VP, _VP]),
     "fp8_transpose_128x128": (_INT, [_VP, _VP, _I64, _I64, _VP, _VP, _VP]),
@@ -114,13 +121,16 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: run `python -m fp8_fine_grained_x128_gb300.build` "
+            flag = " --debug" if DEBUG else ""
+            raise RuntimeError(f"{LIB_PATH} is missing: run `python -m fp8_fine_grained_x128_gb300.build{flag}` "
                                "(there is no CPU fallback)")
         L = ctypes.CDLL(LIB_PATH)
         for name, (res, args) in _SIGS.items():
             fn = getattr(L, name)
             fn.restype = res
             fn.argtypes = args
+        if bool(L.fp8_debug_build()) != DEBUG:
+            raise RuntimeError(f"{LIB_PATH} is not the {'debug' if DEBUG else 'release'} build")
         _lib = L
     return _lib
 
@@ -216,6 +226,23 @@ def device_status(stream=None) -> int:
 
 def selftest_wait_timeout(timeout_ms: int, stream=None) -> None:
     _check("fp8_selftest_wait_timeout", lib().fp8_selftest_wait_timeout(timeout_ms, _stream(stream)))
+
+
+def debug_build() -> bool:
+    """True when the loaded library is the index-checked debug build."""
+    return bool(lib().fp8_debug_build())
+
+
+def selftest_bounds(buf: torch.Tensor, n_claimed: int, stream=None) -> None:
+    """Writes 1.0 to every element of the FP32 device buffer `buf` through the
+    checked store, against a claimed extent of `n_claimed` elements: the debug
+    build stops at n_claimed and records ERR_BOUNDS, the release build writes
+    all of `buf`."""
+    if not isinstance(buf, torch.Tensor):
+        raise TypeError("buf: expected a torch.Tensor (its size gives n_write)")
+    n = buf.numel()
+    _check("fp8_selftest_bounds", lib().fp8_selftest_bounds(_buf(buf, "buf", _F32, n), int(n_claimed), n,
+                                                             _stream(stream)))
 
 
 def workspace_bytes() -> int:

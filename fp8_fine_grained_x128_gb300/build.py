@@ -5,7 +5,13 @@ Every translation unit under csrc/ is compiled by nvcc in parallel with
 no fast-math), then linked into ``fp8_fine_grained_x128_gb300/libfp8fg.so``.
 ptxas register / spill reports are written to ``_build/ptxas.log``.
 
-    python -m fp8_fine_grained_x128_gb300.build [--force]
+``--debug`` builds the index-checked variant ``libfp8fg_debug.so`` instead
+(objects in ``_build_debug/``): the same sources compiled with
+``-DFP8FG_DEBUG``, in which every kernel store checks its index against the
+extent of the buffer it writes and records FP8_ERR_BOUNDS on a miss.  The
+binding loads it when FP8FG_DEBUG=1 is set in the environment.
+
+    python -m fp8_fine_grained_x128_gb300.build [--force] [--debug]
 """
 from __future__ import annotations
 
@@ -19,6 +25,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfp8fg.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libfp8fg_debug.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -48,36 +56,38 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src: str) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, build_dir: str, extra: list) -> tuple[str, str]:
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{p.stdout}\n{p.stderr}")
     return obj, p.stderr
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    extra = ["-DFP8FG_DEBUG"] if debug else []
+    os.makedirs(build_dir, exist_ok=True)
     deps = _deps()
-    if not force and not _stale(LIB, deps):
-        return LIB
+    if not force and not _stale(lib, deps):
+        return lib
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 1)) as ex:
-        results = list(ex.map(_compile, srcs))
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+        results = list(ex.map(lambda src: _compile(src, build_dir, extra), srcs))
+    with open(os.path.join(build_dir, "ptxas.log"), "w") as f:
         for (obj, log) in results:
             f.write(f"==== {os.path.basename(obj)}\n{log}\n")
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *[o for o, _ in results]]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError(f"link failed:\n{p.stdout}\n{p.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
-        print(f"built {LIB}")
-    return LIB
+        print(f"built {lib}")
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True)
+    build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv)

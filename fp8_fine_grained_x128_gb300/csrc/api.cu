@@ -111,6 +111,7 @@ FP8FG_API const char *fp8_status_string(int status)
     case FP8_ERR_CUDA: return "FP8_ERR_CUDA";
     case FP8_ERR_NONFINITE: return "FP8_ERR_NONFINITE";
     case FP8_ERR_TIMEOUT: return "FP8_ERR_TIMEOUT";
+    case FP8_ERR_BOUNDS: return "FP8_ERR_BOUNDS";
     default: return "FP8_ERR_UNKNOWN";
     }
 }
@@ -133,6 +134,24 @@ FP8FG_API int fp8_selftest_wait_timeout(int timeout_ms, void *stream)
     if (timeout_ms < 1 || timeout_ms > 2000) return FP8_ERR_INVALID_ARG;
     FP8FG_STATUS_OR_RETURN(st);
     return launch_selftest_wait(timeout_ms, st, S(stream));
+}
+
+FP8FG_API int fp8_debug_build(void)
+{
+#ifdef FP8FG_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+FP8FG_API int fp8_selftest_bounds(float *buf, int64_t n_claimed, int64_t n_write, void *stream)
+{
+    if (n_claimed < 0 || n_write < n_claimed) return FP8_ERR_INVALID_ARG;
+    if (n_write == 0) return FP8_OK;
+    if (!buf) return FP8_ERR_INVALID_ARG;
+    FP8FG_STATUS_OR_RETURN(st);
+    return launch_selftest_bounds(buf, n_claimed, n_write, st, S(stream));
 }
 
 FP8FG_API int fp8_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, void *q, float *s,

@@ -31,6 +31,37 @@ __device__ __forceinline__ void set_status(int *status, int code)
     if (status) atomicCAS(status, 0, code);
 }
 
+// ------------------------------------------------------------- debug build
+// In the debug build (compiled with FP8FG_DEBUG) every global store of the
+// kernels first checks its index against the extent of the buffer it writes,
+// so a write outside an output -- what a memory checker would report -- is
+// caught where it would happen: the check records FP8_ERR_BOUNDS in the
+// status word and the store is skipped.  In the release build the checks are
+// constant true and compile away.
+#ifdef FP8FG_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+// Elements [i, i + n) lie inside a buffer of `extent` elements.
+__device__ __forceinline__ bool dbg_span(int64_t i, int64_t n, int64_t extent, int *status)
+{
+    if (!kDebugChecks) return true;
+    const bool ok = i >= 0 && n >= 0 && i + n <= extent;
+    if (!ok) set_status(status, FP8_ERR_BOUNDS);
+    return ok;
+}
+
+// Row r and columns [c, c + n) lie inside a [rows][cols] matrix.
+__device__ __forceinline__ bool dbg_cell(int64_t r, int64_t c, int64_t n, int64_t rows, int64_t cols, int *status)
+{
+    if (!kDebugChecks) return true;
+    const bool ok = r >= 0 && r < rows && c >= 0 && n >= 0 && c + n <= cols;
+    if (!ok) set_status(status, FP8_ERR_BOUNDS);
+    return ok;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;

@@ -290,6 +290,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int num_nt = a.N / BN;
     const int num_mt = GMODE == G_ROWS ? sh_off[a.G] / 128 : a.M / 128;
     int ntiles = GMODE == G_K ? a.G * num_mt * num_nt : num_mt * num_nt;
+    const int64_t out_rows = GMODE == G_K ? (int64_t)a.G * a.M : (int64_t)a.M;   // rows of D
     if (GMODE != G_NONE && *bad_offsets) ntiles = 0;
 
     if (warp < kEpiWarp0) {
@@ -616,15 +617,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     float v[HALF];
 #pragma unroll
                     for (int i = 0; i < NP; ++i) f2_unpack(acc[i], v[2 * i], v[2 * i + 1]);
-                    store_row<HALF>(a.D, a.ldD, a.out_f32, (int64_t)m0 + row, (int64_t)n0 + colbase, v);
+                    if (dbg_cell((int64_t)m0 + row, (int64_t)n0 + colbase, HALF, out_rows, a.N, a.status))
+                        store_row<HALF>(a.D, a.ldD, a.out_f32, (int64_t)m0 + row, (int64_t)n0 + colbase, v);
                 } else {
 #pragma unroll
                     for (int rr = 0; rr < 4; ++rr) {
                         const int64_t orow = (int64_t)m0 + lg * 32 + rr * 8 + (lane >> 2);
 #pragma unroll
-                        for (int i = 0; i < HALF / 8; ++i)
-                            store_pair(a.D, a.ldD, a.out_f32, orow, (int64_t)n0 + colbase + 8 * i + 2 * (lane & 3),
-                                       acc[rr * (HALF / 8) + i]);
+                        for (int i = 0; i < HALF / 8; ++i) {
+                            const int64_t ocol = (int64_t)n0 + colbase + 8 * i + 2 * (lane & 3);
+                            if (dbg_cell(orow, ocol, 2, out_rows, a.N, a.status))
+                                store_pair(a.D, a.ldD, a.out_f32, orow, ocol, acc[rr * (HALF / 8) + i]);
+                        }
                     }
                 }
             } else {
@@ -640,7 +644,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * sab;
-                    store_row<32>(a.D, a.ldD, a.out_f32, (int64_t)m0 + row, (int64_t)n0 + colbase + j * 32, v);
+                    if (dbg_cell((int64_t)m0 + row, (int64_t)n0 + colbase + j * 32, 32, out_rows, a.N, a.status))
+                        store_row<32>(a.D, a.ldD, a.out_f32, (int64_t)m0 + row, (int64_t)n0 + colbase + j * 32, v);
                 }
                 tc_fence_before();
                 __syncwarp();

@@ -44,6 +44,7 @@ int launch_quant_stats(const void *x, int64_t rows, int64_t cols, int64_t ldx, c
 int launch_pertensor_current(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, float *scale, void *q,
                              void *ws, int *status, cudaStream_t st);
 int launch_selftest_wait(int timeout_ms, int *status, cudaStream_t st);
+int launch_selftest_bounds(float *buf, int64_t n_claimed, int64_t n_write, int *status, cudaStream_t st);
 
 // gemm.cu
 int launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const float *sA, int granA,

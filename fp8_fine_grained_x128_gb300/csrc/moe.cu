@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kFillThreads) k_moe_fill(const int32_t *__rest
 __global__ void __launch_bounds__(256) k_moe_gather(const uint8_t *__restrict__ q, const float *__restrict__ s,
                                                     int64_t T, int64_t K, const int32_t *__restrict__ row_token,
                                                     const int32_t *__restrict__ offsets, int E, int64_t Mcap,
-                                                    uint8_t *__restrict__ qg, float *__restrict__ sg)
+                                                    uint8_t *__restrict__ qg, float *__restrict__ sg, int *status)
 {
     const int lane = threadIdx.x & 31;
     const int64_t total = min((int64_t)offsets[E], Mcap);
@@ -262,27 +262,30 @@ __global__ void __launch_bounds__(256) k_moe_gather(const uint8_t *__restrict__ 
         if (t < 0 || t >= T) continue;
         const uint4 *src = reinterpret_cast<const uint4 *>(q + t * K);
         uint4 *dst = reinterpret_cast<uint4 *>(qg + r * K);
-        for (int64_t i = lane; i < K / 16; i += 32) dst[i] = src[i];
-        for (int64_t kb = lane; kb < K / 128; kb += 32) sg[kb * Mcap + r] = s[kb * T + t];
+        for (int64_t i = lane; i < K / 16; i += 32)
+            if (dbg_cell(r, i * 16, 16, Mcap, K, status)) dst[i] = src[i];
+        for (int64_t kb = lane; kb < K / 128; kb += 32)
+            if (dbg_cell(kb, r, 1, K / 128, Mcap, status)) sg[kb * Mcap + r] = s[kb * T + t];
     }
 }
 
 // ---------------------------------------------------------------- SwiGLU
 
 __global__ void __launch_bounds__(256) k_swiglu_fwd(const uint16_t *__restrict__ gu, int64_t rows, int64_t F,
-                                                    uint16_t *__restrict__ h)
+                                                    uint16_t *__restrict__ h, int *status)
 {
     const int64_t nvec = rows * (F / 8);
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / (F / 8), j = (i - r * (F / 8)) * 8;
         const uint4 g4 = *reinterpret_cast<const uint4 *>(gu + r * 2 * F + j);
         const uint4 u4 = *reinterpret_cast<const uint4 *>(gu + r * 2 * F + F + j);
-        *reinterpret_cast<uint4 *>(h + r * F + j) = swiglu8(g4, u4);
+        const uint4 hv = swiglu8(g4, u4);
+        if (dbg_cell(r, j, 8, rows, F, status)) *reinterpret_cast<uint4 *>(h + r * F + j) = hv;
     }
 }
 
 __global__ void __launch_bounds__(256) k_swiglu_bwd(const uint16_t *__restrict__ gu, const uint16_t *__restrict__ dh,
-                                                    int64_t rows, int64_t F, uint16_t *__restrict__ dgu)
+                                                    int64_t rows, int64_t F, uint16_t *__restrict__ dgu, int *status)
 {
     const int64_t nvec = rows * (F / 8);
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x) {
@@ -292,8 +295,10 @@ __global__ void __launch_bounds__(256) k_swiglu_bwd(const uint16_t *__restrict__
         const uint4 d4 = *reinterpret_cast<const uint4 *>(dh + r * F + j);
         uint4 dg4, du4;
         swiglu_grad8(g4, u4, d4, dg4, du4);
-        *reinterpret_cast<uint4 *>(dgu + r * 2 * F + j) = dg4;
-        *reinterpret_cast<uint4 *>(dgu + r * 2 * F + F + j) = du4;
+        if (dbg_cell(r, j, 8, rows, 2 * F, status) && dbg_cell(r, F + j, 8, rows, 2 * F, status)) {
+            *reinterpret_cast<uint4 *>(dgu + r * 2 * F + j) = dg4;
+            *reinterpret_cast<uint4 *>(dgu + r * 2 * F + F + j) = du4;
+        }
     }
 }
 
@@ -330,7 +335,7 @@ int launch_moe_gather(const void *q, const float *s, int64_t T, int64_t K, const
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     k_moe_gather<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint8_t *>(q), s, T, K, row_token, offsets, E,
-                                                   Mcap, static_cast<uint8_t *>(qg), sg);
+                                                   Mcap, static_cast<uint8_t *>(qg), sg, status_word_ptr());
     return check_launch();
 }
 
@@ -342,7 +347,7 @@ int launch_swiglu_fwd(const void *gu, int64_t rows, int64_t F, void *h, cudaStre
     const int64_t cap = (int64_t)sm_count() * 16;
     if (blocks > cap) blocks = cap;
     k_swiglu_fwd<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t *>(gu), rows, F,
-                                                   static_cast<uint16_t *>(h));
+                                                   static_cast<uint16_t *>(h), status_word_ptr());
     return check_launch();
 }
 
@@ -355,7 +360,7 @@ int launch_swiglu_bwd(const void *gu, const void *dh, int64_t rows, int64_t F, v
     if (blocks > cap) blocks = cap;
     k_swiglu_bwd<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t *>(gu),
                                                    static_cast<const uint16_t *>(dh), rows, F,
-                                                   static_cast<uint16_t *>(dgu));
+                                                   static_cast<uint16_t *>(dgu), status_word_ptr());
     return check_launch();
 }
 

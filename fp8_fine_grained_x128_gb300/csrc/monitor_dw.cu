@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kDwThreads, 1)
                     const float4 rv = make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]),
                                                   __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
                     const float4 dv = *reinterpret_cast<const float4 *>(Dp + c);   // read before R is written
-                    *reinterpret_cast<float4 *>(Rp + c) = rv;
+                    if (dbg_cell(row, col + c, 4, a.N, a.K, a.status)) *reinterpret_cast<float4 *>(Rp + c) = rv;
                     const float dd[4] = {dv.x - rv.x, dv.y - rv.y, dv.z - rv.z, dv.w - rv.w};
                     const float rr[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll

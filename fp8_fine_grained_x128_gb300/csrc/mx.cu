@@ -91,8 +91,9 @@ __global__ void __launch_bounds__(256) k_quant_mx(const uint16_t *__restrict__ x
             if (a >= 0x7F80u && (lane & 3) == 0) set_status(status, FP8_ERR_NONFINITE);
             const int e = a == 0 ? 0 : mx_exponent<FMT>(min(a, 0x7F7Fu));
             const float inv = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e in [-127, 120]
-            *reinterpret_cast<uint2 *>(q + i * 8) = mx_codes8<FMT>(v[u], inv);
-            if ((lane & 3) == 0) e8[i >> 2] = (uint8_t)(e + 127);
+            const uint2 codes = mx_codes8<FMT>(v[u], inv);
+            if (dbg_span(i * 8, 8, rows * cols, status)) *reinterpret_cast<uint2 *>(q + i * 8) = codes;
+            if ((lane & 3) == 0 && dbg_span(i >> 2, 1, rows * (cols / 32), status)) e8[i >> 2] = (uint8_t)(e + 127);
         }
     }
 }

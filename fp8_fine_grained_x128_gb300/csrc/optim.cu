@@ -80,7 +80,7 @@ __device__ __forceinline__ void load_block(AdamBlockIn &in, const float *p, cons
 __global__ void __launch_bounds__(256) k_adamw_fp8(float *__restrict__ p, const uint16_t *__restrict__ g,
                                                    uint8_t *__restrict__ qm, float *__restrict__ sm,
                                                    uint8_t *__restrict__ qv, float *__restrict__ sv, int64_t nblk,
-                                                   fp8_adamw_hparams_t h)
+                                                   fp8_adamw_hparams_t h, int *status)
 {
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -119,10 +119,12 @@ __global__ void __launch_bounds__(256) k_adamw_fp8(float *__restrict__ p, const 
         av = warp_max(av);
         const float nsm = am == 0.0f ? 1.0f : __fdiv_rn(am, 448.0f);
         const float nsv = av == 0.0f ? 1.0f : __fdiv_rn(av, 57344.0f);
-        __stcs(reinterpret_cast<float4 *>(p + k), make_float4(pp[0], pp[1], pp[2], pp[3]));
-        *reinterpret_cast<uint32_t *>(qm + k) = f32x4_to_fp8<FP8_E4M3>(m, Divider(nsm));
-        *reinterpret_cast<uint32_t *>(qv + k) = f32x4_to_fp8<FP8_E5M2>(v, Divider(nsv));
-        if (lane == 0) {
+        if (dbg_span(k, 4, nblk * 128, status)) {
+            __stcs(reinterpret_cast<float4 *>(p + k), make_float4(pp[0], pp[1], pp[2], pp[3]));
+            *reinterpret_cast<uint32_t *>(qm + k) = f32x4_to_fp8<FP8_E4M3>(m, Divider(nsm));
+            *reinterpret_cast<uint32_t *>(qv + k) = f32x4_to_fp8<FP8_E5M2>(v, Divider(nsv));
+        }
+        if (lane == 0 && dbg_span(b, 1, nblk, status)) {
             sm[b] = nsm;
             sv[b] = nsv;
         }
@@ -145,7 +147,8 @@ int launch_adamw_fp8(float *p, const void *g, uint8_t *qm, float *sm, uint8_t *q
     int64_t blocks = (nblk + 7) / 8;
     const int64_t cap = (int64_t)sm_count() * std::max(1, per_sm[dev & 63]);
     if (blocks > cap) blocks = cap;
-    k_adamw_fp8<<<(unsigned)blocks, 256, 0, st>>>(p, static_cast<const uint16_t *>(g), qm, sm, qv, sv, nblk, h);
+    k_adamw_fp8<<<(unsigned)blocks, 256, 0, st>>>(p, static_cast<const uint16_t *>(g), qm, sm, qv, sv, nblk, h,
+                                              status_word_ptr());
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

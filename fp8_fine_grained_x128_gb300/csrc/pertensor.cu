@@ -282,7 +282,8 @@ __global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__res
             if (r0 + row < rows) {
                 amax = max(amax, absmax8(v[i]));
                 const uint2 code = quant8_mon<FMT, STATS>(v[i], d, c, seen);
-                *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = code;
+                if (dbg_cell(r0 + row, c0 + g * 8, 8, rows, cols, status))
+                    *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = code;
                 if (TRANS) {
                     ct[row * 33 + 2 * g] = code.x;
                     ct[row * 33 + 2 * g + 1] = code.y;
@@ -304,6 +305,7 @@ __global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__res
                 const uint32_t t0 = __byte_perm(w0, w1, 0x5140), t1 = __byte_perm(w2, w3, 0x5140);
                 const uint32_t t2 = __byte_perm(w0, w1, 0x7362), t3 = __byte_perm(w2, w3, 0x7362);
                 uint8_t *dst = qT + (c0 + 4 * cw) * rows + r0 + 4 * mg;
+                if (!dbg_cell(c0 + 4 * cw + 3, r0 + 4 * mg, 4, cols, rows, status)) continue;
                 *reinterpret_cast<uint32_t *>(dst) = __byte_perm(t0, t1, 0x5410);
                 *reinterpret_cast<uint32_t *>(dst + rows) = __byte_perm(t0, t1, 0x7632);
                 *reinterpret_cast<uint32_t *>(dst + 2 * rows) = __byte_perm(t2, t3, 0x5410);
@@ -735,7 +737,8 @@ __global__ void __launch_bounds__(256) k_amax_scale(const uint16_t *__restrict__
 
 template <int FMT>
 __global__ void __launch_bounds__(256) k_quant_scale(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
-                                                     int64_t ldx, const float *scale, uint8_t *__restrict__ q)
+                                                     int64_t ldx, const float *scale, uint8_t *__restrict__ q,
+                                                     int *status)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const Divider2 d(*scale);
@@ -754,16 +757,22 @@ __global__ void __launch_bounds__(256) k_quant_scale(const uint16_t *__restrict_
                 for (int u = 0; u < U; ++u) l2_priority_normal(x + (i + u * stride) * 8);
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) *reinterpret_cast<uint2 *>(q + (i + u * stride) * 8) = quant8p<FMT>(v[u], d);
+            for (int u = 0; u < U; ++u) {
+                const uint2 c = quant8p<FMT>(v[u], d);
+                if (dbg_span((i + u * stride) * 8, 8, nvec * 8, status))
+                    *reinterpret_cast<uint2 *>(q + (i + u * stride) * 8) = c;
+            }
         }
         for (; i < nvec; i += stride) {
-            *reinterpret_cast<uint2 *>(q + i * 8) = quant8p<FMT>(ldg_stream(x + i * 8), d);
+            const uint2 c = quant8p<FMT>(ldg_stream(x + i * 8), d);
+            if (dbg_span(i * 8, 8, nvec * 8, status)) *reinterpret_cast<uint2 *>(q + i * 8) = c;
             if (keep) l2_priority_normal(x + i * 8);
         }
     } else {
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
             const int64_t r = i / vpr, c = (i - r * vpr) * 8;
-            *reinterpret_cast<uint2 *>(q + r * cols + c) = quant8p<FMT>(ldg_stream(x + r * ldx + c), d);
+            const uint2 code = quant8p<FMT>(ldg_stream(x + r * ldx + c), d);
+            if (dbg_cell(r, c, 8, rows, cols, status)) *reinterpret_cast<uint2 *>(q + r * cols + c) = code;
         }
     }
 }
@@ -785,6 +794,18 @@ __global__ void k_selftest_wait(uint64_t timeout_ns, int *status)
         mbar_arrive(&bar);
     }
     __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Index-check self-test: writes 1.0f to buf[0, n_write) through the checked
+// store, against a claimed extent of n_claimed elements.  The caller owns all
+// n_write elements, so every store lands inside real memory in either build;
+// the debug build skips those at and past n_claimed and records the error.
+// ---------------------------------------------------------------------------
+__global__ void k_selftest_bounds(float *buf, int64_t n_claimed, int64_t n_write, int *status)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_write; i += (int64_t)gridDim.x * blockDim.x)
+        if (dbg_span(i, 1, n_claimed, status)) buf[i] = 1.0f;
 }
 
 // ------------------------------------------------------------------ launchers
@@ -895,10 +916,10 @@ int launch_pertensor_current(const void *x, int64_t rows, int64_t cols, int64_t 
     cudaError_t e = cudaSuccess;
     if (fmt == FP8_E5M2) {
         k_amax_scale<FP8_E5M2><<<ba, 256, 0, st>>>(X, rows, cols, ldx, scale, W, status);
-        if (nvec > 0) e = cudaLaunchKernelEx(&cfg, k_quant_scale<FP8_E5M2>, X, rows, cols, ldx, S, Q);
+        if (nvec > 0) e = cudaLaunchKernelEx(&cfg, k_quant_scale<FP8_E5M2>, X, rows, cols, ldx, S, Q, status);
     } else {
         k_amax_scale<FP8_E4M3><<<ba, 256, 0, st>>>(X, rows, cols, ldx, scale, W, status);
-        if (nvec > 0) e = cudaLaunchKernelEx(&cfg, k_quant_scale<FP8_E4M3>, X, rows, cols, ldx, S, Q);
+        if (nvec > 0) e = cudaLaunchKernelEx(&cfg, k_quant_scale<FP8_E4M3>, X, rows, cols, ldx, S, Q, status);
     }
     if (e != cudaSuccess) return FP8_ERR_CUDA;
     return check_launch();
@@ -907,6 +928,13 @@ int launch_pertensor_current(const void *x, int64_t rows, int64_t cols, int64_t 
 int launch_selftest_wait(int timeout_ms, int *status, cudaStream_t st)
 {
     k_selftest_wait<<<1, 32, 0, st>>>((uint64_t)timeout_ms * 1000000ull, status);
+    return check_launch();
+}
+
+int launch_selftest_bounds(float *buf, int64_t n_claimed, int64_t n_write, int *status, cudaStream_t st)
+{
+    const int64_t blocks = std::min<int64_t>((n_write + 255) / 256, 1024);
+    k_selftest_bounds<<<(unsigned)blocks, 256, 0, st>>>(buf, n_claimed, n_write, status);
     return check_launch();
 }
 

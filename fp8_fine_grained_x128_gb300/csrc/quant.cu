@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256, 4) k_quant_1x128_rows(const uint16_t *__r
         const GroupScale gs = half_warp_scales8<FMT>(m, l16);
         if (!(l16 & 2) && c0 + gs.u < ncb) {
             if (gs.amax >= 0x7F80u) set_status(status, FP8_ERR_NONFINITE);
-            s[(int64_t)(c0 + gs.u) * rows + r] = gs.s;
+            if (dbg_cell(c0 + gs.u, r, 1, ncb, rows, status)) s[(int64_t)(c0 + gs.u) * rows + r] = gs.s;
         }
         const int hbase = threadIdx.x & 16;
 #pragma unroll
@@ -68,7 +68,9 @@ __global__ void __launch_bounds__(256, 4) k_quant_1x128_rows(const uint16_t *__r
             const uint32_t cb = c0 + u;
             if (cb < ncb) {
                 const Divider2 d(su, ru);
-                *reinterpret_cast<uint2 *>(q + (int64_t)r * cols + (int64_t)cb * 128 + l16 * 8) = quant8p<FMT>(v[u], d);
+                const uint2 c = quant8p<FMT>(v[u], d);
+                if (dbg_cell(r, (int64_t)cb * 128 + l16 * 8, 8, rows, cols, status))
+                    *reinterpret_cast<uint2 *>(q + (int64_t)r * cols + (int64_t)cb * 128 + l16 * 8) = c;
             }
         }
     }
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(256, fused_ctas_per_sm<SRC>()) k_quant_1x128_f
         }
         if (!(g & 2)) {
             if (gs.amax >= 0x7F80u) set_status(status, FP8_ERR_NONFINITE);
-            s[cb * rows + r0 + rr + 16 * gs.u] = gs.s;
+            if (dbg_cell(cb, r0 + rr + 16 * gs.u, 1, cols / 128, rows, status)) s[cb * rows + r0 + rr + 16 * gs.u] = gs.s;
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -221,7 +223,9 @@ __global__ void __launch_bounds__(256, fused_ctas_per_sm<SRC>()) k_quant_1x128_f
             const float si = __shfl_sync(0xffffffffu, gs.s, (lane & 16) + half_group_lane(i));
             const float ri = __shfl_sync(0xffffffffu, gs.r, (lane & 16) + half_group_lane(i));
             const Divider2 d(si, ri);
-            *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = quant8p<FMT>(v[i], d);
+            const uint2 code = quant8p<FMT>(v[i], d);
+            if (dbg_cell(r0 + row, c0 + g * 8, 8, rows, cols, status))
+                *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = code;
             *reinterpret_cast<uint4 *>(tile + row * 256 + ((g ^ ((row >> 2) & 7)) << 4)) = v[i];
             cm0 = bf16x2_absmax(cm0, bf16x2_abs(v[i].x));
             cm1 = bf16x2_absmax(cm1, bf16x2_abs(v[i].y));
@@ -259,7 +263,8 @@ __global__ void __launch_bounds__(256, fused_ctas_per_sm<SRC>()) k_quant_1x128_f
             c.r2 = f2_pack(ra, rb);
             c.ns2 = f2_pack(-sc[0], -sc[1]);
             cdiv[t] = c;
-            *reinterpret_cast<float2 *>(sT + mb * cols + c0 + 2 * t) = make_float2(sc[0], sc[1]);
+            if (dbg_cell(mb, c0 + 2 * t, 2, rows / 128, cols, status))
+                *reinterpret_cast<float2 *>(sT + mb * cols + c0 + 2 * t) = make_float2(sc[0], sc[1]);
         }
         __syncthreads();
         // the next unit's loads fly during the transposed quantization
@@ -293,10 +298,12 @@ __global__ void __launch_bounds__(256, fused_ctas_per_sm<SRC>()) k_quant_1x128_f
             const uint32_t t0 = __byte_perm(rw[0], rw[1], 0x5140), t1 = __byte_perm(rw[2], rw[3], 0x5140);
             const uint32_t t2 = __byte_perm(rw[0], rw[1], 0x7362), t3 = __byte_perm(rw[2], rw[3], 0x7362);
             uint8_t *dst = qT + (c0 + 4 * cw) * rows + r0 + 4 * mg;
-            *reinterpret_cast<uint32_t *>(dst) = __byte_perm(t0, t1, 0x5410);
-            *reinterpret_cast<uint32_t *>(dst + rows) = __byte_perm(t0, t1, 0x7632);
-            *reinterpret_cast<uint32_t *>(dst + 2 * rows) = __byte_perm(t2, t3, 0x5410);
-            *reinterpret_cast<uint32_t *>(dst + 3 * rows) = __byte_perm(t2, t3, 0x7632);
+            if (dbg_cell(c0 + 4 * cw + 3, r0 + 4 * mg, 4, cols, rows, status)) {
+                *reinterpret_cast<uint32_t *>(dst) = __byte_perm(t0, t1, 0x5410);
+                *reinterpret_cast<uint32_t *>(dst + rows) = __byte_perm(t0, t1, 0x7632);
+                *reinterpret_cast<uint32_t *>(dst + 2 * rows) = __byte_perm(t2, t3, 0x5410);
+                *reinterpret_cast<uint32_t *>(dst + 3 * rows) = __byte_perm(t2, t3, 0x7632);
+            }
         }
         __syncthreads();   // the tile buffer is rewritten by the next iteration
     };
@@ -349,7 +356,7 @@ __global__ void __launch_bounds__(256, fused_ctas_per_sm<SRC>()) k_quant_1x128_f
 // gives full 32-byte segments on the global stores.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void store_code_tile_transposed(const uint32_t *ct, uint8_t *qT, int64_t ldT,
-                                                           int64_t c0, int64_t r0)
+                                                           int64_t c0, int64_t r0, int64_t qt_rows, int *status)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int cw = (lane >> 3) + 4 * warp;
@@ -363,6 +370,7 @@ __device__ __forceinline__ void store_code_tile_transposed(const uint32_t *ct, u
         const uint32_t t0 = __byte_perm(w0, w1, 0x5140), t1 = __byte_perm(w2, w3, 0x5140);
         const uint32_t t2 = __byte_perm(w0, w1, 0x7362), t3 = __byte_perm(w2, w3, 0x7362);
         uint8_t *dst = qT + (c0 + 4 * cw) * ldT + r0 + 4 * mg;
+        if (!dbg_cell(c0 + 4 * cw + 3, r0 + 4 * mg, 4, qt_rows, ldT, status)) continue;
         *reinterpret_cast<uint32_t *>(dst) = __byte_perm(t0, t1, 0x5410);
         *reinterpret_cast<uint32_t *>(dst + ldT) = __byte_perm(t0, t1, 0x7632);
         *reinterpret_cast<uint32_t *>(dst + 2 * ldT) = __byte_perm(t2, t3, 0x5410);
@@ -408,19 +416,20 @@ __global__ void __launch_bounds__(256) k_quant_128x128(const uint16_t *__restric
     for (int i = 0; i < 8; ++i) {
         const int row = rr + 16 * i;
         const uint2 c = quant8p<FMT>(v[i], d);
-        *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = c;
+        if (dbg_cell(r0 + row, c0 + g * 8, 8, rows, cols, status))
+            *reinterpret_cast<uint2 *>(q + (r0 + row) * cols + c0 + g * 8) = c;
         if (TRANS) {
             ct[row * 33 + 2 * g] = c.x;
             ct[row * 33 + 2 * g + 1] = c.y;
         }
     }
     if (t == 0) {
-        s[rb * ncb + cb] = sc;
-        if (TRANS) sT[cb * nrb + rb] = sc;
+        if (dbg_span(rb * ncb + cb, 1, nrb * ncb, status)) s[rb * ncb + cb] = sc;
+        if (TRANS && dbg_span(cb * nrb + rb, 1, nrb * ncb, status)) sT[cb * nrb + rb] = sc;
     }
     if (TRANS) {
         __syncthreads();
-        store_code_tile_transposed(ct, qT, rows, c0, r0);
+        store_code_tile_transposed(ct, qT, rows, c0, r0, cols, status);
     }
 }
 
@@ -429,7 +438,7 @@ __global__ void __launch_bounds__(256) k_quant_128x128(const uint16_t *__restric
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_transpose_128x128(const uint8_t *__restrict__ q, const float *__restrict__ s,
                                                            int64_t rows, int64_t cols, uint8_t *__restrict__ qT,
-                                                           float *__restrict__ sT)
+                                                           float *__restrict__ sT, int *status)
 {
     __shared__ uint32_t ct[128 * 33];
     const int t = threadIdx.x;
@@ -449,9 +458,10 @@ __global__ void __launch_bounds__(256) k_transpose_128x128(const uint8_t *__rest
         uint32_t *p = ct + row * 33 + ch * 4;
         p[0] = v.x; p[1] = v.y; p[2] = v.z; p[3] = v.w;
     }
-    if (t == 0) sT[cb * (rows / 128) + rb] = s[rb * (cols / 128) + cb];
+    if (t == 0 && dbg_span(cb * (rows / 128) + rb, 1, (rows / 128) * (cols / 128), status))
+        sT[cb * (rows / 128) + rb] = s[rb * (cols / 128) + cb];
     __syncthreads();
-    store_code_tile_transposed(ct, qT, rows, c0, r0);
+    store_code_tile_transposed(ct, qT, rows, c0, r0, cols, status);
 }
 
 // ------------------------------------------------------------------ launchers
@@ -546,7 +556,7 @@ int launch_transpose_128x128(const void *q, const float *s, int64_t rows, int64_
     if (rows == 0 || cols == 0 || batch == 0) return FP8_OK;
     dim3 grid((unsigned)(cols / 128), (unsigned)(rows / 128), (unsigned)batch);
     k_transpose_128x128<<<grid, 256, 0, st>>>(static_cast<const uint8_t *>(q), s, rows, cols,
-                                              static_cast<uint8_t *>(qT), sT);
+                                              static_cast<uint8_t *>(qT), sT, status_word_ptr());
     return check_launch();
 }
 

@@ -66,7 +66,9 @@ enum {
     FP8_ERR_UNSUPPORTED = 4, /* format / granularity combination not provided */
     FP8_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, attribute, query) */
     FP8_ERR_NONFINITE = 6,   /* device: a scaling group held Inf or NaN */
-    FP8_ERR_TIMEOUT = 7      /* device: a bounded pipeline wait gave up (about 1 s) */
+    FP8_ERR_TIMEOUT = 7,     /* device: a bounded pipeline wait gave up (about 1 s) */
+    FP8_ERR_BOUNDS = 8       /* device, debug build only: a kernel's store fell outside its buffer
+                                (the store was skipped) */
 };
 
 typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format_t;
@@ -125,6 +127,21 @@ FP8FG_API int fp8_device_status(void *stream, int *out);
  * milliseconds (1 .. 2000), after which it records FP8_ERR_TIMEOUT in the
  * device status word and returns.  The CUDA context stays usable. */
 FP8FG_API int fp8_selftest_wait_timeout(int timeout_ms, void *stream);
+
+/* 1 when this library is the index-checked debug build (compiled with
+ * FP8FG_DEBUG: every kernel store checks its index against the extent of the
+ * buffer it writes, records FP8_ERR_BOUNDS and skips the store if outside),
+ * 0 for the release build, in which the checks compile away. */
+FP8FG_API int fp8_debug_build(void);
+
+/* Self-test of the debug build's store check: writes 1.0f to buf[i] for
+ * 0 <= i < n_write (device FP32 buffer of at least n_write elements, owned by
+ * the caller) through the checked store, against a claimed extent of
+ * n_claimed elements (0 <= n_claimed <= n_write, else FP8_ERR_INVALID_ARG).
+ * The debug build writes only buf[0, n_claimed) and, when n_write > n_claimed,
+ * records FP8_ERR_BOUNDS; the release build writes all n_write elements.
+ * Every store stays inside the caller's buffer in both builds. */
+FP8FG_API int fp8_selftest_bounds(float *buf, int64_t n_claimed, int64_t n_write, void *stream);
 
 /* ----------------------------------------------------------- quantizers */
 

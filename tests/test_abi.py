@@ -37,6 +37,28 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
 
 
+def test_debug_build_exports_the_same_abi_and_says_so(lib):
+    """The index-checked variant (FP8FG_DEBUG) builds from the same sources,
+    exports every declared entry point and reports itself as the debug build;
+    the release library reports 0."""
+    path = fgbuild.build(debug=True)
+    dbg = ctypes.CDLL(path)
+    for n in declared_symbols():
+        assert hasattr(dbg, n), f"{n} missing from the debug build"
+    assert dbg.fp8_debug_build() == 1
+    assert lib.fp8_debug_build() == 0
+    assert fg.status_string(fg.ERR_BOUNDS) == "FP8_ERR_BOUNDS"
+
+
+def test_selftest_bounds_validates_extents_on_the_host(lib):
+    S = ctypes.c_void_p(0)
+    f = lib.fp8_selftest_bounds
+    assert f(None, -1, 4, S) == fg.ERR_INVALID_ARG
+    assert f(None, 5, 4, S) == fg.ERR_INVALID_ARG
+    assert f(None, 0, 0, S) == fg.OK              # nothing to write
+    assert f(None, 0, 4, S) == fg.ERR_INVALID_ARG
+
+
 def test_binding_covers_the_abi():
     assert set(declared_symbols()) <= set(fg._SIGS), set(declared_symbols()) - set(fg._SIGS)
 
