@@ -223,6 +223,13 @@ class Clocks:
 
 
 
+def _nvtx(name):
+    """An NVTX range around a phase, for a profiler's timeline (a no-op cost
+    when no profiler is attached)."""
+    import torch
+    return torch.cuda.nvtx.range(name)
+
+
 def _bf16_dev(bits, dev):
     import torch
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -272,24 +279,25 @@ class MlpStep:
                 fg.blockscaled_gemm(A, E, sA, gA, B, E, sB, gB, D)
 
         # weights (quantized once per weight update)
-        fg.quant_128x128(self.Wgu, E, self.qWgu, self.sWgu)
-        fg.quant_128x128(self.Wd, E, self.qWd, self.sWd)
-        # fprop
-        fg.quant_1x128(self.X, E, self.qX, self.sX, self.qXT, self.sXT)
-        gemm("fprop_gate_up", self.qX, self.sX, B1, self.qWgu, self.sWgu, BB, self.GU)
-        # H = SwiGLU(GU), quantized 1x128 and 128x1 as it is computed (H never stored)
-        fg.swiglu_quant_fwd(self.GU, E, self.qH, self.sH, self.qHT, self.sHT)
-        gemm("fprop_down", self.qH, self.sH, B1, self.qWd, self.sWd, BB, self.Y)
-        # dgrad (W^T on demand)
-        fg.quant_1x128(self.dY, E, self.qdY, self.sdY, self.qdYT, self.sdYT)
-        fg.transpose_128x128(self.qWd, self.sWd, self.qWdT, self.sWdT)
-        gemm("dgrad_down", self.qdY, self.sdY, B1, self.qWdT, self.sWdT, BB, self.dH)
-        fg.swiglu_bwd_quant(self.GU, self.dH, E, self.qdGU, self.sdGU, self.qdGUT, self.sdGUT)
-        fg.transpose_128x128(self.qWgu, self.sWgu, self.qWguT, self.sWguT)
-        gemm("dgrad_gate_up", self.qdGU, self.sdGU, B1, self.qWguT, self.sWguT, BB, self.dX)
-        # wgrad from the 128x1 (transposed) copies
-        gemm("wgrad_down", self.qdYT, self.sdYT, B1, self.qHT, self.sHT, B1, self.dWd)
-        gemm("wgrad_gate_up", self.qdGUT, self.sdGUT, B1, self.qXT, self.sXT, B1, self.dWgu)
+        with _nvtx("weights"):
+            fg.quant_128x128(self.Wgu, E, self.qWgu, self.sWgu)
+            fg.quant_128x128(self.Wd, E, self.qWd, self.sWd)
+        with _nvtx("fprop"):
+            fg.quant_1x128(self.X, E, self.qX, self.sX, self.qXT, self.sXT)
+            gemm("fprop_gate_up", self.qX, self.sX, B1, self.qWgu, self.sWgu, BB, self.GU)
+            # H = SwiGLU(GU), quantized 1x128 and 128x1 as it is computed (H never stored)
+            fg.swiglu_quant_fwd(self.GU, E, self.qH, self.sH, self.qHT, self.sHT)
+            gemm("fprop_down", self.qH, self.sH, B1, self.qWd, self.sWd, BB, self.Y)
+        with _nvtx("dgrad"):   # W^T on demand
+            fg.quant_1x128(self.dY, E, self.qdY, self.sdY, self.qdYT, self.sdYT)
+            fg.transpose_128x128(self.qWd, self.sWd, self.qWdT, self.sWdT)
+            gemm("dgrad_down", self.qdY, self.sdY, B1, self.qWdT, self.sWdT, BB, self.dH)
+            fg.swiglu_bwd_quant(self.GU, self.dH, E, self.qdGU, self.sdGU, self.qdGUT, self.sdGUT)
+            fg.transpose_128x128(self.qWgu, self.sWgu, self.qWguT, self.sWguT)
+            gemm("dgrad_gate_up", self.qdGU, self.sdGU, B1, self.qWguT, self.sWguT, BB, self.dX)
+        with _nvtx("wgrad"):   # from the 128x1 (transposed) copies
+            gemm("wgrad_down", self.qdYT, self.sdYT, B1, self.qHT, self.sHT, B1, self.dWd)
+            gemm("wgrad_gate_up", self.qdGUT, self.sdGUT, B1, self.qXT, self.sXT, B1, self.dWgu)
         return ev
 
     IN_NAMES = ("X", "dY", "Wgu", "Wd")
@@ -659,8 +667,9 @@ def run_ours(args):
     fp8_peak_burst = pk["bf16"] * FP8_OVER_BF16
 
     step = MlpStep(dev, seed=rank)
-    for _ in range(args.warmup):
-        step.run()
+    with _nvtx("warmup"):
+        for _ in range(args.warmup):
+            step.run()
     barrier()
 
     gpu_id = str(local)
@@ -676,8 +685,9 @@ def run_ours(args):
     barrier()
     clocks.mark("start")
     t_start.record(stream)
-    for _ in range(args.steps):
-        ev.append(step.run(timed=True))
+    with _nvtx("timed_steps"):
+        for _ in range(args.steps):
+            ev.append(step.run(timed=True))
     t_end.record(stream)
     barrier()
     clocks.mark("end")
@@ -722,7 +732,8 @@ def run_ours(args):
                                       f"{clk.get('sm_mhz')} MHz): sustained peak bf16 {pk['bf16_sus']} x {FP8_OVER_BF16}")
 
     # end to end: host buffers, H2D of the step's inputs and D2H of its results
-    e2e = step.e2e(args.steps)
+    with _nvtx("e2e_steps"):
+        e2e = step.e2e(args.steps)
     e2e_val = job_tflops(world, flops, slowest_rank_ms(e2e["ms"], world, dev))
 
     line = {
@@ -741,7 +752,8 @@ def run_ours(args):
         "gpu_launches": step.launches_per_step * args.steps,
     }
     if rank == 0:
-        rows = RowBench(dev, pk).run_all(only=None if not args.no_rows else "quantizers")
+        with _nvtx("rows"):
+            rows = RowBench(dev, pk).run_all(only=None if not args.no_rows else "quantizers")
         # the "quantize GB/s" half of the metric: the quantizer rows, each against the HBM roofline
         roofline["quantizers"] = {
             k: {"time_us": round(v["time_us"], 2), "GB/s": round(v["achieved"], 1), "frac": round(v["frac"], 4)}
