@@ -363,33 +363,41 @@ __global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__res
 // Monitors of an existing quantization.
 // ---------------------------------------------------------------------------
 
-// Saturation test |x / s| > fmax without a division for almost every element:
-// with t = fmax * s rounded, |x| <= t (1 - 2^-20) can only give a quotient below
-// fmax and |x| >= t (1 + 2^-20) only one above it (the quotient's and t's
-// roundings are each within 2^-24 relative, and the next binary32 above fmax is
-// far closer than 2^-21 fmax).  Between the two bounds, and for scales whose t
-// is not a normal number well inside the range, the exact quotient decides.
-struct SatTest {
-    float lo, hi, s;
-    __device__ __forceinline__ explicit SatTest(float s_, float fm) : s(s_)
-    {
-        const float t = __fmul_rn(fm, s_);
-        if (t >= 0x1p-100f && t <= 0x1p100f) {
-            lo = __fmul_rn(t, 1.0f - 0x1p-20f);
-            hi = __fmul_rn(t, 1.0f + 0x1p-20f);
-        } else {
-            lo = -1.0f;                          // every element takes the exact path
-            hi = __uint_as_float(0x7FC00000u);   // NaN: the fast "saturated" branch never fires
-        }
-    }
-    __device__ __forceinline__ bool operator()(uint32_t xb, float fm) const
-    {
-        const float ax = __uint_as_float((xb & 0x7FFFu) << 16);
-        if (ax >= hi) return true;
-        if (!(ax > lo)) return false;
-        return fabsf(Divider(s)(__uint_as_float(xb << 16))) > fm;
-    }
-};
+// Saturation of a scaling group without a division.  |x / s| rounded to
+// binary32 exceeds fmax exactly when the real quotient exceeds
+// fmax + ulp(fmax) / 2 (a tie rounds to fmax, whose last significand bit is
+// 0), i.e. when |x| > |s| (fmax + ulp(fmax) / 2).  That product has at most
+// 24 + 25 significant bits, so it is exact in binary64; the largest BF16 at or
+// below it is its toward-zero binary32 rounding with the low 16 bits cut off,
+// and |x| exceeds the product exactly when its BF16 magnitude bits exceed
+// those.  Returned as the per-half addend of sat_bits, (0x8000 - T) in both
+// halves with T = those bits + 1.  Scales of 0 (every nonzero x saturates),
+// Inf (only a quotient Inf / Inf = NaN could reach it: none does) and NaN
+// (T = 0x8000: none) follow from the same rule.
+template <int FMT>
+__device__ __forceinline__ uint32_t sat_addend(float s)
+{
+    const double b = FMT == FP8_E4M3 ? 448.0 + 0x1p-16 : 57344.0 + 0x1p-9;
+    const uint32_t hi = __float_as_uint(__double2float_rz(fabs((double)s) * b)) >> 16;
+    const uint32_t t = min(hi + 1u, 0x8000u);
+    return (0x8000u - t) * 0x00010001u;
+}
+
+// Bits 15 and 31: the BF16 halves of w that saturate, T <= |x| <= Inf (a NaN
+// x gives a NaN quotient, which never exceeds fmax).  Neither sum carries
+// across the halves: each half of the magnitude is at most 0x7FFF.
+__device__ __forceinline__ uint32_t sat_bits(uint32_t w, uint32_t addend)
+{
+    const uint32_t t = w & 0x7FFF7FFFu;
+    return (t + addend) & ~(t + 0x007F007Fu) & 0x80008000u;
+}
+
+// Bit 7 of byte e: element e of the 4 BF16 values (w0 = x0, x1; w1 = x2, x3)
+// from the per-half flags at bits 15 and 31 of f0 / f1.
+__device__ __forceinline__ uint32_t halves_to_bytes(uint32_t f0, uint32_t f1)
+{
+    return __byte_perm(f0, f1, 0x7531) & 0x80808080u;
+}
 
 // Per-warp scratch of the 128-element group monitors: a presence bitmap of the
 // 65536 BF16 keys and one flag byte per FP8 key.  Both are all zero between
@@ -399,41 +407,45 @@ struct GroupScratch {
     uint32_t fq[64];
 };
 
-// Monitors of one group of 128 elements, 4 per lane (x as BF16 bits, q as FP8
-// codes, element e of the lane in half e of xv / byte e of qv).  The order of
-// the elements within the group does not matter.  A BF16 key counts as
-// distinct for the lane whose atomic OR set its bit first.
-template <int FMT>
-__device__ __forceinline__ void mon_group(uint2 xv, uint32_t qv, float sc, GroupScratch &g, int lane, uint32_t &nz,
-                                          uint32_t &uf, uint32_t &sat, uint32_t &din, uint32_t &dout)
+// Monitors of one group of 128 elements, 4 per lane: x as BF16 bits
+// (elements 0, 1 in xv.x and 2, 3 in xv.y, low half first) and q as FP8 codes
+// (byte e = element e); the order of the elements within the group does not
+// matter.  Nonzero, underflow and saturation are counted four elements at a
+// time on packed flags.  A BF16 key counts as distinct for the lane whose
+// atomic OR set its bit first (bitmap word from the key's low 11 bits, bit
+// from its top 5: a group's values share a few binades, and this spreads them
+// over words and banks); the distinct FP8 keys are the flag bytes set.
+__device__ __forceinline__ void mon_group(uint2 xv, uint32_t qv, uint32_t sat_add, GroupScratch &g, int lane,
+                                          uint32_t &nz, uint32_t &uf, uint32_t &sat, uint32_t &din, uint32_t &dout)
 {
-    const float fm = fmax_of(FMT);
-    const SatTest st(sc, fm);
-    uint8_t *fqb = reinterpret_cast<uint8_t *>(g.fq);
-    const uint32_t xs[4] = {xv.x & 0xFFFFu, xv.x >> 16, xv.y & 0xFFFFu, xv.y >> 16};
-    uint32_t kx[4];
+    const uint32_t n0 = (xv.x & 0x7FFF7FFFu) + 0x7FFF7FFFu;   // bit 15 of a half: that x is nonzero
+    const uint32_t n1 = (xv.y & 0x7FFF7FFFu) + 0x7FFF7FFFu;
+    const uint32_t nzb = halves_to_bytes(n0, n1);
+    const uint32_t qn = (qv & 0x7F7F7F7Fu) + 0x7F7F7F7Fu;      // bit 7 of a byte: that code is nonzero
+    nz += __popc(nzb);
+    uf += __popc(nzb & ~qn);
+    sat += __popc(halves_to_bytes(sat_bits(xv.x, sat_add), sat_bits(xv.y, sat_add)));
+    // keys: -0 -> +0 on both sides
+    const uint32_t k0 = xv.x & (n0 | 0x7FFF7FFFu), k1 = xv.y & (n1 | 0x7FFF7FFFu);
+    const uint32_t kq = qv & (qn | 0x7F7F7F7Fu);
+    const uint32_t key[4] = {k0, k0 >> 16, k1, k1 >> 16};     // bits above 15 of the low keys are masked below
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const uint32_t code = (qv >> (8 * e)) & 0xFFu;
-        const bool nzero = (xs[e] & 0x7FFFu) != 0;
-        nz += nzero;
-        uf += nzero && ((code & 0x7Fu) == 0);
-        sat += st(xs[e], fm);
-        kx[e] = key_bf16(xs[e]);
-        // word from the key's low 11 bits, bit from its top 5 (sign and high
-        // exponent bits): a group's values share a few binades, and this
-        // spreads them over words and banks instead of stacking them on a few
-        const uint32_t bit = 1u << (kx[e] >> 11);
-        din += (atomicOr(&g.bx[kx[e] & 2047u], bit) & bit) == 0;
-        fqb[key_fp8(code)] = 1;
+        const uint32_t bit = __funnelshift_l(1u, 1u, key[e] >> 11);   // 1 << bits 11..15 of the key
+        din += (atomicOr(&g.bx[key[e] & 2047u], bit) & bit) == 0;
     }
+    uint8_t *fqb = reinterpret_cast<uint8_t *>(g.fq);
+    fqb[kq & 0xFFu] = 1;
+    fqb[(kq >> 8) & 0xFFu] = 1;
+    fqb[(kq >> 16) & 0xFFu] = 1;
+    fqb[kq >> 24] = 1;
     __syncwarp();
-    const uint32_t f0 = g.fq[lane], f1 = g.fq[lane + 32];
-    dout += __popc(f0) + __popc(f1);          // flag bytes are 0 or 1
-    g.fq[lane] = 0;
-    g.fq[lane + 32] = 0;
+    uint2 *fq2 = reinterpret_cast<uint2 *>(g.fq);
+    const uint2 f = fq2[lane];
+    dout += __popc(f.x) + __popc(f.y);                         // flag bytes are 0 or 1
+    fq2[lane] = make_uint2(0u, 0u);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) g.bx[kx[e] & 2047u] = 0;
+    for (int e = 0; e < 4; ++e) g.bx[key[e] & 2047u] = 0;
     __syncwarp();
 }
 
@@ -466,8 +478,12 @@ __device__ __forceinline__ void clear_group_scratch(GroupScratch &g, int lane)
     __syncwarp();
 }
 
-// 1x128 groups (one row, 128 consecutive columns): one warp per group, four
-// groups loaded ahead of their processing.
+// 1x128 groups (one row, 128 consecutive columns): one warp per group.  Each
+// warp takes a contiguous range of groups in the order of the scales
+// S[C/128][R] (group i = row i % R of column block i / R) and walks it in
+// batches of 32: lane j computes the saturation threshold of the batch's
+// group j from one coalesced load of scales, and four groups are loaded
+// ahead of their processing.
 template <int FMT>
 __global__ void __launch_bounds__(kG128Warps * 32) k_stats_1x128(const uint16_t *__restrict__ x, int64_t rows,
                                                                  int64_t cols, int64_t ldx,
@@ -480,41 +496,41 @@ __global__ void __launch_bounds__(kG128Warps * 32) k_stats_1x128(const uint16_t 
     clear_group_scratch(g, lane);
     const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t ncb = cols / 128, ngroups = rows * ncb;
+    const int64_t ngroups = rows * (cols / 128);
+    const int64_t gbeg = ngroups * warp0 / nwarps, gend = ngroups * (warp0 + 1) / nwarps;
     constexpr int U = 4;
     uint32_t nz = 0, uf = 0, sat = 0, din = 0, dout = 0;
-    // group gi = r * ncb + cb; stepping gi by nwarps moves (r, cb) by (dq, dr)
-    // with one carry, so no division runs per group
-    const int64_t dq = nwarps / ncb, dr = nwarps - dq * ncb;
-    int64_t r = warp0 / ncb, cb = warp0 - r * ncb;
-    for (int64_t base = warp0; base < ngroups; base += U * nwarps) {
-        uint2 xv[U];
-        uint32_t qv[U];
-        float sc[U];
+    int64_t cb = gbeg / rows, r = gbeg - cb * rows;
+    for (int64_t b0 = gbeg; b0 < gend; b0 += 32) {
+        const int n = gend - b0 < 32 ? (int)(gend - b0) : 32;
+        const uint32_t add_l = lane < n ? sat_addend<FMT>(s[b0 + lane]) : 0u;
+        for (int j = 0; j < n; j += U) {
+            uint2 xv[U];
+            uint32_t qv[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (base + u * nwarps < ngroups) {
-                xv[u] = __ldcs(reinterpret_cast<const uint2 *>(x + r * ldx + cb * 128) + lane);
-                qv[u] = __ldcs(reinterpret_cast<const uint32_t *>(q + r * cols + cb * 128) + lane);
-                sc[u] = s[cb * rows + r];
+            for (int u = 0; u < U; ++u) {
+                if (j + u < n) {
+                    xv[u] = __ldcs(reinterpret_cast<const uint2 *>(x + r * ldx + cb * 128) + lane);
+                    qv[u] = __ldcs(reinterpret_cast<const uint32_t *>(q + r * cols + cb * 128) + lane);
+                }
+                if (++r == rows) {
+                    r = 0;
+                    ++cb;
+                }
             }
-            r += dq;
-            cb += dr;
-            if (cb >= ncb) {
-                cb -= ncb;
-                ++r;
-            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (j + u < n)
+                    mon_group(xv[u], qv[u], __shfl_sync(0xffffffffu, add_l, j + u), g, lane, nz, uf, sat, din, dout);
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (base + u * nwarps < ngroups) mon_group<FMT>(xv[u], qv[u], sc[u], g, lane, nz, uf, sat, din, dout);
     }
     warp_stats_flush(stats, lane, nz, uf, sat, din, dout);
 }
 
 // 128x1 groups (128 rows of one column; q is the transposed copy qT[C][R] and
 // s is S[R/128][C]).  A CTA stages 128 rows x 32 columns of x in shared
-// memory, transposed, so that every warp reads its columns contiguously.
+// memory, transposed, so that every warp reads its columns contiguously; lane
+// j computes the saturation threshold of the tile's column j.
 template <int FMT>
 __global__ void __launch_bounds__(kG128Warps * 32) k_stats_128x1(const uint16_t *__restrict__ x, int64_t rows,
                                                                  int64_t cols, int64_t ldx,
@@ -536,6 +552,7 @@ __global__ void __launch_bounds__(kG128Warps * 32) k_stats_128x1(const uint16_t 
 #pragma unroll
         for (int p = 0; p < 4; ++p)                // row p*32 + t/4, columns (t%4)*8 .. +7
             v[p] = ldg_stream(x + (mb * 128 + p * 32 + (t >> 2)) * ldx + c0 + (t & 3) * 8);
+        const uint32_t add_l = sat_addend<FMT>(s[mb * cols + c0 + lane]);
         __syncthreads();                           // the previous tile's columns are consumed
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
@@ -551,7 +568,7 @@ __global__ void __launch_bounds__(kG128Warps * 32) k_stats_128x1(const uint16_t 
             const int c = warp * (32 / kG128Warps) + j;
             const uint2 xv = make_uint2(xs[c * kPitch + 2 * lane], xs[c * kPitch + 2 * lane + 1]);
             const uint32_t qv = __ldcs(reinterpret_cast<const uint32_t *>(q + (c0 + c) * rows + mb * 128) + lane);
-            mon_group<FMT>(xv, qv, s[mb * cols + c0 + c], g, lane, nz, uf, sat, din, dout);
+            mon_group(xv, qv, __shfl_sync(0xffffffffu, add_l, c), g, lane, nz, uf, sat, din, dout);
         }
     }
     warp_stats_flush(stats, lane, nz, uf, sat, din, dout);
@@ -570,7 +587,6 @@ __global__ void __launch_bounds__(256) k_stats_blocks(const uint16_t *__restrict
     __shared__ uint32_t red[32];
     __shared__ int is_last;
     const int t = threadIdx.x, g = t & 15, rr = t >> 4;
-    const float fm = fmax_of(FMT);
     const int64_t ncb = cols / 128, nrb = rows / 128, ntiles = ncb * nrb;
     Counts c;
     uint32_t din = 0, dout = 0;
@@ -587,7 +603,7 @@ __global__ void __launch_bounds__(256) k_stats_blocks(const uint16_t *__restrict
             if (t < 8) bmq[t] = 0;
             __syncthreads();
         }
-        const SatTest sat_test(TENSOR ? s[0] : s[rb * ncb + cb], fm);
+        const uint32_t sat_add = sat_addend<FMT>(TENSOR ? s[0] : s[rb * ncb + cb]);
 #pragma unroll 2
         for (int i = 0; i < 8; ++i) {
             const int64_t r = rb * 128 + rr + 16 * i;
@@ -595,15 +611,22 @@ __global__ void __launch_bounds__(256) k_stats_blocks(const uint16_t *__restrict
             const uint2 qq = *reinterpret_cast<const uint2 *>(q + r * cols + cb * 128 + g * 8);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t xb = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
-                const uint32_t code = ((e < 4 ? qq.x : qq.y) >> (8 * (e & 3))) & 0xFFu;
-                const bool nzero = (xb & 0x7FFFu) != 0;
-                c.nz += nzero;
-                c.uf += nzero && ((code & 0x7Fu) == 0);
-                c.sat += sat_test(xb, fm);
-                bitmap_set(bmx, key_bf16(xb));
-                bitmap_set(bmq, key_fp8(code));
+            for (int h = 0; h < 2; ++h) {   // four elements at a time, as in mon_group
+                const uint32_t w0 = w[2 * h], w1 = w[2 * h + 1], cw = h ? qq.y : qq.x;
+                const uint32_t n0 = (w0 & 0x7FFF7FFFu) + 0x7FFF7FFFu, n1 = (w1 & 0x7FFF7FFFu) + 0x7FFF7FFFu;
+                const uint32_t nzb = halves_to_bytes(n0, n1);
+                const uint32_t qn = (cw & 0x7F7F7F7Fu) + 0x7F7F7F7Fu;
+                c.nz += __popc(nzb);
+                c.uf += __popc(nzb & ~qn);
+                c.sat += __popc(halves_to_bytes(sat_bits(w0, sat_add), sat_bits(w1, sat_add)));
+                const uint32_t k0 = w0 & (n0 | 0x7FFF7FFFu), k1 = w1 & (n1 | 0x7FFF7FFFu);
+                const uint32_t kq = cw & (qn | 0x7F7F7F7Fu);
+                bitmap_set(bmx, k0 & 0xFFFFu);
+                bitmap_set(bmx, k0 >> 16);
+                bitmap_set(bmx, k1 & 0xFFFFu);
+                bitmap_set(bmx, k1 >> 16);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) bitmap_set(bmq, (kq >> (8 * e)) & 0xFFu);
             }
         }
         if (!TENSOR) {

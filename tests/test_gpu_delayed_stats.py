@@ -233,15 +233,20 @@ def test_quant_stats_all_granularities(fmt):
         assert np.array_equal(stats.cpu().numpy().astype(np.uint64), ref), (gran, stats, ref)
 
 
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
 @pytest.mark.parametrize("gran", [oracle.GRAN_1x128, oracle.GRAN_128x1, oracle.GRAN_128x128])
-def test_quant_stats_saturation_boundary_and_odd_scales(gran):
+def test_quant_stats_saturation_boundary_and_odd_scales(gran, fmt):
     """Scales that put |x / s| within a few ulps of fmax (the saturation count
     is decided by the exact binary32 quotient), and scales far outside the
-    normal range (0, subnormal, huge, 2^-125 where x / s overflows)."""
-    fmt = oracle.E4M3
+    normal range (0, -0, subnormal, huge, FLT_MAX, Inf, NaN, negative, 2^-125
+    where x / s overflows); x holds +-Inf, NaN and -0 among its values."""
     R, C = 256, 512
-    rng = np.random.default_rng(5)
+    fm = np.float32(oracle.fmax(fmt))
+    rng = np.random.default_rng(5 + fmt)
     xb = synth.bf16_signed_lognormal((R, C), 23, 0.0, 1.5)
+    specials = np.array([0x7F80, 0xFF80, 0x7FC0, 0x8000, 0x7F7F, 0x0001], np.uint16)   # Inf, -Inf, NaN, -0, max, min subnormal
+    where = rng.choice(R * C, size=64, replace=False)
+    xb.ravel()[where] = specials[np.arange(64) % len(specials)]
     xf = synth.bf16_bits_to_f32(xb)
     if gran == oracle.GRAN_1x128:
         shape, pick = (C // 128, R), lambda i, j: xf[j, i * 128:(i + 1) * 128]
@@ -253,12 +258,17 @@ def test_quant_stats_saturation_boundary_and_odd_scales(gran):
     for i in range(shape[0]):
         for j in range(shape[1]):
             grp = np.abs(pick(i, j)).ravel()
+            grp = grp[np.isfinite(grp)]
             v = grp[rng.integers(0, grp.size)]                  # one element of the group at |x/s| ~ fmax
-            s[i, j] = np.float32(v) / np.float32(448.0)
+            s[i, j] = np.float32(v) / fm
             s[i, j] = np.nextafter(s[i, j], np.float32(rng.choice([-1, 1]) * np.inf), dtype=np.float32) \
                 if rng.random() < 0.5 else s[i, j]
-    odd = np.float32([0.0, 1e-40, 2.0 ** -125, 2.0 ** -124, 3e37, np.float32(np.inf)])
-    s.ravel()[:len(odd)] = odd
+            if rng.random() < 0.25:
+                s[i, j] = -s[i, j]                              # |x / s| does not see the sign of s
+    odd = np.float32([0.0, 1e-40, 2.0 ** -125, 2.0 ** -124, 3e37, np.inf, -0.0, np.nan, np.finfo(np.float32).max,
+                      -2.0 ** -130])
+    n = min(len(odd), s.size)
+    s.ravel()[:n] = odd[:n]
     q = rng.integers(0, 256, size=(C, R) if gran == oracle.GRAN_128x1 else (R, C), dtype=np.uint8)
     stats = fg.new_stats()
     fg.quant_stats(dev_bf16(xb), dev_u8(q), dev_f32(s), gran, fmt, stats)
