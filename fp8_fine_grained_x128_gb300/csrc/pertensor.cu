@@ -414,7 +414,9 @@ struct GroupScratch {
 // time on packed flags.  A BF16 key counts as distinct for the lane whose
 // atomic OR set its bit first (bitmap word from the key's low 11 bits, bit
 // from its top 5: a group's values share a few binades, and this spreads them
-// over words and banks); the distinct FP8 keys are the flag bytes set.
+// over words and banks); the distinct FP8 keys are the flag bytes set, at the
+// code rotated left by one so that +-c share a word (a store of both signs of
+// one magnitude is then no bank conflict).
 __device__ __forceinline__ void mon_group(uint2 xv, uint32_t qv, uint32_t sat_add, GroupScratch &g, int lane,
                                           uint32_t &nz, uint32_t &uf, uint32_t &sat, uint32_t &din, uint32_t &dout)
 {
@@ -434,11 +436,12 @@ __device__ __forceinline__ void mon_group(uint2 xv, uint32_t qv, uint32_t sat_ad
         const uint32_t bit = __funnelshift_l(1u, 1u, key[e] >> 11);   // 1 << bits 11..15 of the key
         din += (atomicOr(&g.bx[key[e] & 2047u], bit) & bit) == 0;
     }
+    const uint32_t rq = ((kq << 1) & 0xFEFEFEFEu) | ((kq >> 7) & 0x01010101u);
     uint8_t *fqb = reinterpret_cast<uint8_t *>(g.fq);
-    fqb[kq & 0xFFu] = 1;
-    fqb[(kq >> 8) & 0xFFu] = 1;
-    fqb[(kq >> 16) & 0xFFu] = 1;
-    fqb[kq >> 24] = 1;
+    fqb[rq & 0xFFu] = 1;
+    fqb[(rq >> 8) & 0xFFu] = 1;
+    fqb[(rq >> 16) & 0xFFu] = 1;
+    fqb[rq >> 24] = 1;
     __syncwarp();
     uint2 *fq2 = reinterpret_cast<uint2 *>(g.fq);
     const uint2 f = fq2[lane];
