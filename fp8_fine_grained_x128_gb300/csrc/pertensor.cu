@@ -180,9 +180,10 @@ __device__ bool merge_and_ticket(const Counts &c, uint32_t amax, const uint32_t 
 }
 
 // In the last CTA of a delayed-scaling step: the codes of the distinct inputs
-// are marked in the workspace's code bitmap before the counts are taken.
+// are marked in the workspace's code bitmap before the counts are taken, one
+// key at a time (the path for scales outside (0, Inf)).
 template <int FMT>
-__device__ void mark_codes_of_distinct_inputs(PtWorkspace *ws, const Divider2 &d)
+__device__ void mark_codes_per_key(PtWorkspace *ws, const Divider2 &d)
 {
     uint32_t m[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // this thread's 256-bit code set
     for (int i = threadIdx.x; i < 2048; i += blockDim.x) {
@@ -206,6 +207,89 @@ __device__ void mark_codes_of_distinct_inputs(PtWorkspace *ws, const Divider2 &d
         if ((threadIdx.x & 31) == 0 && m[j]) atomicOr(&ws->bmq[j], m[j]);
     }
     __syncthreads();
+}
+
+// The distinct counts of a delayed-scaling step in its last CTA, for a scale s
+// in (0, Inf), with the code set found by intervals instead of key by key.
+// The code of |x| is a non-decreasing function of |x| over the finite and
+// infinite magnitudes 0 .. 0x7F80 (an IEEE quotient by s, then a rounding,
+// saturating conversion), so the magnitudes of code c form an interval
+// [L_c, L_c+1) and c occurs with sign b exactly when the merged presence
+// bitmap holds a key of sign b in it.  128 threads find the interval starts by
+// bisection (15 IEEE quotients each) while the bitmap loads are in flight;
+// prefix popcounts give each interval's key count in O(1).  NaN keys, whose
+// code is the conversion's NaN code, are checked per sign apart.  The
+// bitmap is read once: counted, copied to shared memory and zeroed for the
+// next call.  Shared scratch: words[2048], pre[2049], L[129], cq[8].
+template <int FMT>
+__device__ void delayed_distinct_by_intervals(PtWorkspace *ws, float s, fp8_stats_t *stats, uint32_t *words,
+                                              uint32_t *pre, uint32_t *L, uint32_t *cq, uint32_t *red)
+{
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;   // 256 threads
+    uint32_t wv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) wv[j] = __ldcg(&ws->bmx[8 * t + j]);
+    if (t < 8) cq[t] = 0;
+    if (t < 128) {
+        uint32_t lo = 0, hi = 0x7F81u;   // L_t: the smallest magnitude whose code is >= t
+        while (lo < hi) {
+            const uint32_t mid = (lo + hi) >> 1;
+            const uint32_t c = cvt2<FMT>(__fdiv_rn(__uint_as_float(mid << 16), s), 0.0f) & 0xFFu;
+            if (c >= (uint32_t)t) hi = mid;
+            else lo = mid + 1;
+        }
+        L[t] = lo;
+    }
+    if (t == 0) L[128] = 0x7F81u;
+    uint32_t loc[8], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        words[8 * t + j] = wv[j];
+        ws->bmx[8 * t + j] = 0;
+        loc[j] = sum;
+        sum += __popc(wv[j]);
+    }
+    uint32_t incl = sum;   // inclusive scan of the per-thread sums
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) red[warp] = incl;
+    __syncthreads();
+    uint32_t base = incl - sum, total = 0;
+    for (int w = 0; w < 8; ++w) {
+        if (w < warp) base += red[w];
+        total += red[w];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) pre[8 * t + j] = base + loc[j];
+    if (t == 255) pre[2048] = base + sum;
+    __syncthreads();
+    auto below = [&](uint32_t k) -> uint32_t {   // present keys < k, 0 <= k <= 65536
+        const uint32_t w = k >> 5, b = k & 31;
+        return b ? pre[w] + __popc(words[w] & ((1u << b) - 1u)) : pre[w];
+    };
+    const uint32_t sg = (uint32_t)t >> 7, c = (uint32_t)t & 127;   // sign, magnitude code
+    if (L[c] < L[c + 1] && below((sg << 15) | L[c + 1]) > below((sg << 15) | L[c])) {
+        const uint32_t code = key_fp8((sg << 7) | c);
+        atomicOr(&cq[code >> 5], 1u << (code & 31));
+    }
+    if (t < 2 && below(((uint32_t)t << 15) + 0x8000u) > below(((uint32_t)t << 15) | 0x7F81u)) {
+        const float nan = __uint_as_float(((uint32_t)t << 31) | 0x7FC00000u);
+        const uint32_t code = key_fp8((cvt2<FMT>(__fdiv_rn(nan, s), 0.0f) & 0xFFu) | ((uint32_t)t << 7));
+        atomicOr(&cq[code >> 5], 1u << (code & 31));
+    }
+    __syncthreads();
+    if (t == 0) {
+        // +0 and -0 are one value: bit 0 of words 0 and 1024 (keys 0x0000, 0x8000)
+        const uint32_t din = total - (words[0] & words[1024] & 1u);
+        uint32_t dout = 0;
+        for (int j = 0; j < 8; ++j) dout += __popc(cq[j]);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&stats->distinct_in), (unsigned long long)din);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&stats->distinct_out), (unsigned long long)dout);
+        ws->ticket = 0;
+    }
 }
 
 // In the last CTA: distinct counts from the merged bitmaps, workspace reset.
@@ -240,7 +324,7 @@ __device__ void finalize_distinct_and_reset(fp8_stats_t *stats, PtWorkspace *ws,
 // Delayed-scaling quantization of one tensor, one step.
 // ---------------------------------------------------------------------------
 template <int FMT, bool TRANS, bool STATS>
-__global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
+__global__ void __launch_bounds__(256, STATS ? 2 : 4) k_pertensor_delayed(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
                                                            int64_t ldx, int hist_len, int margin, int algo,
                                                            float *hist, int32_t *step, float *scale,
                                                            uint8_t *__restrict__ q, uint8_t *__restrict__ qT,
@@ -267,14 +351,38 @@ __global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__res
     uint32_t amax = 0;
     const int64_t ncb = cols / 128, nrb = (rows + 127) / 128;
     const int64_t ntiles = nrb * ncb;
+    // With monitors (two CTAs per SM, held back by the 64 KB presence table)
+    // the next tile is loaded into registers while this one is processed.
+    uint4 vn[8];
+    if (STATS && blockIdx.x < ntiles) {
+        const int64_t rbn = blockIdx.x / ncb, cbn = blockIdx.x - rbn * ncb;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int64_t r = rbn * 128 + rr + 16 * i;
+            vn[i] = r < rows ? ldg_stream(x + r * ldx + cbn * 128 + g * 8) : make_uint4(0, 0, 0, 0);
+        }
+    }
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int64_t rb = tile / ncb, cb = tile - rb * ncb;
         const int64_t r0 = rb * 128, c0 = cb * 128;
         uint4 v[8];
+        if (STATS) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int64_t r = r0 + rr + 16 * i;
-            v[i] = r < rows ? ldg_stream(x + r * ldx + c0 + g * 8) : make_uint4(0, 0, 0, 0);
+            for (int i = 0; i < 8; ++i) v[i] = vn[i];
+            if (tile + gridDim.x < ntiles) {
+                const int64_t tn = tile + gridDim.x, rbn = tn / ncb, cbn = tn - rbn * ncb;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int64_t r = rbn * 128 + rr + 16 * i;
+                    vn[i] = r < rows ? ldg_stream(x + r * ldx + cbn * 128 + g * 8) : make_uint4(0, 0, 0, 0);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int64_t r = r0 + rr + 16 * i;
+                v[i] = r < rows ? ldg_stream(x + r * ldx + c0 + g * 8) : make_uint4(0, 0, 0, 0);
+            }
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -322,20 +430,28 @@ __global__ void __launch_bounds__(256) k_pertensor_delayed(const uint16_t *__res
             const uint4 a = reinterpret_cast<const uint4 *>(seen)[2 * i], b = reinterpret_cast<const uint4 *>(seen)[2 * i + 1];
             const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
             uint32_t bits = 0;
+            // bytes b0..b3 of 0 / 1: the product's top byte is b0 + 2 b1 + 4 b2 + 8 b3 (b_i lands
+            // on bit 24 + i; every other partial product is below bit 24 and on a bit of its own,
+            // or above bit 31)
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                bits |= ((wv[j] & 1u) | ((wv[j] >> 7) & 2u) | ((wv[j] >> 14) & 4u) | ((wv[j] >> 21) & 8u)) << (4 * j);
+            for (int j = 0; j < 8; ++j) bits |= ((wv[j] * 0x01020408u) >> 24) << (4 * j);
             bmx[i] = bits;
         }
     }
     if (!merge_and_ticket<STATS>(c, amax, bmx, bmq, stats, ws, red, &is_last)) return;
 
     // ---- last CTA: state update (history slot, next scale, step) ----
-    if (STATS) {
+    if (STATS && s_t > 0.0f && s_t < __uint_as_float(0x7F800000u)) {
         __threadfence();
-        mark_codes_of_distinct_inputs<FMT>(ws, d);
+        uint32_t *scratch = reinterpret_cast<uint32_t *>(seen);
+        delayed_distinct_by_intervals<FMT>(ws, s_t, stats, bmx, scratch, scratch + 2049, scratch + 2049 + 129, red);
+    } else {
+        if (STATS) {
+            __threadfence();
+            mark_codes_per_key<FMT>(ws, d);
+        }
+        finalize_distinct_and_reset<STATS>(stats, ws, red);
     }
-    finalize_distinct_and_reset<STATS>(stats, ws, red);
     if (t == 0) {
         const uint32_t a = atomicExch(&ws->amax_bits, 0u);
         if (a >= 0x7F80u) {
