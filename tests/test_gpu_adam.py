@@ -69,3 +69,31 @@ def test_adamw_fp8_full_size_one_step():
     assert same(st["p"], ref[0], np.uint32)
     assert same(st["m"], ref[1]) and same(st["v"], ref[3])
     assert same(st["sm"], ref[2], np.uint32) and same(st["sv"], ref[4], np.uint32)
+
+
+@pytest.mark.parametrize("step", [1, 7, 100, 5000])
+def test_adamw_fp8_random_moments_bit_exact(step):
+    """One step from random moment codes and scales (magnitudes over many
+    binades, both signs of m, zero codes and zero blocks among them) at step
+    numbers whose bias corrections run from 0.1 / 0.05 to 1: the bias-corrected
+    moments m / bc1 and v / bc2 are divided through the corrections'
+    reciprocals, and must match the oracle's IEEE quotients bit for bit."""
+    n = 128 * 2048
+    rng = np.random.default_rng(100 + step)
+    p = rng.normal(0, 0.02, n).astype(np.float32)
+    qm = rng.integers(0, 256, n, dtype=np.uint8)
+    qm[(qm & 0x7F) == 0x7F] = 0x7E                       # no NaN codes in the state (E4M3 S.1111.111)
+    qv = rng.integers(0, 0x7C, n, dtype=np.uint8)        # E5M2 v >= 0: finite codes, zeros included
+    qm[:128 * 3] = 0
+    qv[:128 * 3] = 0
+    sm = (2.0 ** rng.uniform(-40, 2, n // 128)).astype(np.float32)
+    sv = (2.0 ** rng.uniform(-60, 0, n // 128)).astype(np.float32)
+    g = synth.bf16_normal((n,), 200 + step, 1e-3, 1e-3, 30.0)
+    st = dict(p=torch.from_numpy(p.copy()).cuda(), m=torch.from_numpy(qm.copy()).cuda(),
+              sm=torch.from_numpy(sm.copy()).cuda(), v=torch.from_numpy(qv.copy()).cuda(),
+              sv=torch.from_numpy(sv.copy()).cuda())
+    gpu_step(st, g, step)
+    ref = oracle.adam_fp8_step(p, g, qm, sm, qv, sv, hyper(step))
+    assert same(st["p"], ref[0], np.uint32)
+    assert same(st["m"], ref[1]) and same(st["v"], ref[3])
+    assert same(st["sm"], ref[2], np.uint32) and same(st["sv"], ref[4], np.uint32)
