@@ -52,7 +52,8 @@ struct Counts {
 // Quantize 8 BF16 values with one scale and (optionally) account the monitors.
 // The distinct-code count of a quantization done here needs no per-element
 // code bitmap: q = enc(x / s) is a function of x, so the distinct codes are the
-// image of the distinct inputs, which the last CTA encodes once.
+// image of the distinct inputs, which the last CTA derives once from the merged
+// presence bitmap.
 struct Quot8 {
     float q[8];
 };
