@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kFillThreads) k_moe_fill(const int32_t *__rest
             for (int k = 0; k < 8; ++k)
                 if (v[k] == e) k_hit[i] = k;
         }
-        // the next round's loads fly during the scan
+        // the next iteration's loads fly during the scan
 #pragma unroll
         for (int i = 0; i < kFillTokens; ++i)
             choices(tb + (int64_t)kFillThreads * kFillTokens + i, cv[i][0], cv[i][1]);
