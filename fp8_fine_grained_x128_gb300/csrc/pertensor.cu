@@ -70,6 +70,17 @@ __device__ __noinline__ Quot8 quot8_ieee(uint4 v, float s)
     return r;
 }
 
+// NaN codes carry no sign: every byte that encodes a NaN (E4M3 S.1111.111,
+// E5M2 S.11111.xx with xx != 0) becomes 0x7F, whatever the sign of x.
+template <int FMT>
+__device__ __forceinline__ uint32_t canon_nan4(uint32_t w)
+{
+    constexpr uint32_t kAdd = FMT == FP8_E4M3 ? 0x01010101u : 0x03030303u;   // bit 7 set <=> low 7 bits are a NaN
+    const uint32_t nan7 = ((w & 0x7F7F7F7Fu) + kAdd) & 0x80808080u;
+    const uint32_t m = (nan7 >> 7) * 0xFFu;                                    // 0xFF in every NaN byte
+    return (w & ~m) | (m & 0x7F7F7F7Fu);
+}
+
 template <int FMT, bool STATS>
 __device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &c, uint8_t *seen)
 {
@@ -92,8 +103,8 @@ __device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &
         const Quot8 r = quot8_ieee(v, d.s);
 #pragma unroll
         for (int e = 0; e < 8; ++e) qv[e] = r.q[e];
-        out.x = (cvt2<FMT>(qv[0], qv[1]) | (cvt2<FMT>(qv[2], qv[3]) << 16)) | sign_bits4(v.x, v.y);
-        out.y = (cvt2<FMT>(qv[4], qv[5]) | (cvt2<FMT>(qv[6], qv[7]) << 16)) | sign_bits4(v.z, v.w);
+        out.x = canon_nan4<FMT>((cvt2<FMT>(qv[0], qv[1]) | (cvt2<FMT>(qv[2], qv[3]) << 16)) | sign_bits4(v.x, v.y));
+        out.y = canon_nan4<FMT>((cvt2<FMT>(qv[4], qv[5]) | (cvt2<FMT>(qv[6], qv[7]) << 16)) | sign_bits4(v.z, v.w));
     }
     if (STATS) {
         // four elements at a time: bit 7 of byte i flags element i
@@ -196,7 +207,7 @@ __device__ void mark_codes_per_key(PtWorkspace *ws, const Divider2 &d)
             float lo, hi;
             d(key, lo, hi);                                   // the key is the low half of the word
             if (lo != lo) lo = __fdiv_rn(__uint_as_float(key << 16), d.s);   // overflow, Inf or NaN
-            const uint32_t code = key_fp8(cvt2<FMT>(lo, lo) & 0xFFu);
+            const uint32_t code = key_fp8(canon_nan4<FMT>(cvt2<FMT>(lo, lo) & 0xFFu) & 0xFFu);
 #pragma unroll
             for (int j = 0; j < 8; ++j) m[j] |= ((code >> 5) == (uint32_t)j) ? (1u << (code & 31)) : 0u;
         }
@@ -277,8 +288,9 @@ __device__ void delayed_distinct_by_intervals(PtWorkspace *ws, float s, fp8_stat
         atomicOr(&cq[code >> 5], 1u << (code & 31));
     }
     if (t < 2 && below(((uint32_t)t << 15) + 0x8000u) > below(((uint32_t)t << 15) | 0x7F81u)) {
+        // a NaN key of either sign: its quotient is NaN, whose code is 0x7F
         const float nan = __uint_as_float(((uint32_t)t << 31) | 0x7FC00000u);
-        const uint32_t code = key_fp8((cvt2<FMT>(__fdiv_rn(nan, s), 0.0f) & 0xFFu) | ((uint32_t)t << 7));
+        const uint32_t code = key_fp8(canon_nan4<FMT>(cvt2<FMT>(__fdiv_rn(nan, s), 0.0f) & 0xFFu) & 0xFFu);
         atomicOr(&cq[code >> 5], 1u << (code & 31));
     }
     __syncthreads();

@@ -149,22 +149,26 @@ def test_delayed_overflowing_quotients_saturate(fmt):
         assert (q_ref & 0x7F == (0x7E if fmt == oracle.E4M3 else 0x7B)).sum() > 0
 
 
-def test_delayed_nonfinite_codes_follow_ieee_quotients():
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+@pytest.mark.parametrize("nans", [(0x7FC1,), (0xFFC1,), (0x7FC1, 0xFFC1, 0xFF81)], ids=["pos_nan", "neg_nan", "both_nans"])
+def test_delayed_nonfinite_codes_follow_ieee_quotients(fmt, nans):
     """A step holding Inf and NaN still writes its codes and monitors like the
-    IEEE quotients say (Inf -> +-fmax, NaN -> the NaN code)."""
-    g = GpuDelayed(oracle.E4M3)
+    IEEE quotients say (Inf -> +-fmax, NaN of either sign -> the NaN code 0x7F)."""
+    g = GpuDelayed(fmt)
     xb, _ = synth.delayed_step_inputs(0, m=256, hidden=256, n_out=256)
     g.run(xb)
     st = oracle.DelayedState(16)
-    oracle.delayed_step(xb, st, oracle.E4M3)
+    oracle.delayed_step(xb, st, fmt)
     bad = xb.copy()
-    bad[3, 3], bad[7, 200], bad[100, 5] = 0x7F80, 0xFF80, 0x7FC1      # +Inf, -Inf, NaN
+    bad[3, 3], bad[7, 200] = 0x7F80, 0xFF80                          # +Inf, -Inf
+    for i, nb in enumerate(nans):
+        bad[100 + i, 5 + 7 * i] = nb
     q = empty_u8(256, 256)
     qT = empty_u8(256, 256)
     stats = fg.new_stats()
     fg.quant_pertensor_delayed(dev_bf16(bad), g.recipe, g.hist, g.step, g.scale, q, g.ws, qT, stats)
     assert fg.device_status() == fg.ERR_NONFINITE
-    q_ref, _, stats_ref, code = oracle.delayed_step(bad, st, oracle.E4M3)
+    q_ref, _, stats_ref, code = oracle.delayed_step(bad, st, fmt)
     assert code == oracle.NONFINITE
     assert np.array_equal(q.cpu().numpy(), q_ref) and np.array_equal(qT.cpu().numpy(), q_ref.T)
     assert np.array_equal(stats.cpu().numpy().astype(np.uint64), stats_ref)
