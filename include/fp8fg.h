@@ -192,7 +192,8 @@ FP8FG_API size_t fp8_pertensor_workspace_bytes(void);
  * Engine" DelayedScaling and "Scaling strategies": the scale comes from the
  * amax seen in earlier iterations).  State is caller-owned device memory:
  *   amax_history[recipe->history_len], *step (starts at 0), *scale (s_t,
- *   start it at 1).
+ *   start it at 1; any s_t >= 0 including +Inf is handled, the codes for a
+ *   negative or NaN s_t are unspecified).
  * The call quantizes q = RNE_satfinite(x / s_t), writes this step's amax to
  * amax_history[step % L], sets *scale = s_{t+1} = m * 2^margin / fmax with
  * m = max(history) (or this step's amax for FP8_AMAX_MOST_RECENT; unchanged

@@ -289,3 +289,20 @@ def test_quant_stats_full_size_1x128():
     fg.quant_stats(dev_bf16(xb), dev_u8(q), dev_f32(s), fg.GRAN_1x128, fg.E4M3, stats)
     assert_status_ok()
     assert np.array_equal(stats.cpu().numpy().astype(np.uint64), oracle.quant_stats(xb, q, s, oracle.GRAN_1x128))
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+@pytest.mark.parametrize("s0", [0.0, float("inf")], ids=["zero", "inf"])
+def test_delayed_zero_and_infinite_carried_scale(fmt, s0):
+    """A carried-over scale of 0 (x / 0 = +-Inf saturates, 0 / 0 is NaN) or +Inf
+    (every finite x / Inf is +-0): codes, monitors (the distinct codes then
+    come from the key-by-key path) and the state update follow the oracle."""
+    R, C = 256, 384
+    xb = synth.bf16_signed_lognormal((R, C), 19, 0.0, 2.0)
+    xb[:4, :7] = 0x0000
+    xb[4:6, :5] = 0x8000                                        # +-0 among the values
+    g = GpuDelayed(fmt)
+    g.scale.fill_(s0)
+    st = oracle.DelayedState(16)
+    st.scale[:] = np.float32(s0)
+    check_against_oracle(g, st, xb, fmt)
