@@ -390,7 +390,8 @@ typedef struct {
  *   param = param - lr * (u + weight_decay * param)
  * and m, v are re-quantized with their blocks' new scales -- all in place, one
  * pass.  param: FP32 master weights [n].  n % 128 == 0; param, grad, m, v
- * 16-byte aligned. */
+ * 16-byte aligned.  Gradients, parameters and moments are finite; the results
+ * for a block holding Inf or NaN are unspecified. */
 FP8FG_API int fp8_adamw_step_fp8_states(float *param, const void *grad, uint8_t *m, float *m_scales,
                                         uint8_t *v, float *v_scales, int64_t n,
                                         const fp8_adamw_hparams_t *hparams, void *stream);
@@ -411,7 +412,8 @@ FP8FG_API int fp8_adamw_step_fp8_states(float *param, const void *grad, uint8_t 
  * M_capacity get row_token = -1, row_prob = 0.  The total must fit
  * M_capacity and every padded count must be reachable with distinct tokens
  * (else FP8_ERR_INVALID_ARG on the device); T*topk + E*(align-1) always fits
- * M_capacity.  1 <= topk <= min(E, 8), align in {1..1024}. */
+ * M_capacity.  1 <= topk <= min(E, 8), align in {1..1024}.  The logits are
+ * finite; the routing of a token with an Inf or NaN logit is unspecified. */
 FP8FG_API int fp8_moe_route_pad(const float *logits, int64_t T, int E, int topk, int align,
                                 int64_t M_capacity, int32_t *topk_idx, float *topk_prob,
                                 int32_t *counts, int32_t *group_offsets, int32_t *row_token,
