@@ -442,19 +442,29 @@ class RowBench:
                 out["a17_mxfp8_quant_1x32"] = {"error": f"{type(exc).__name__}: {exc}"}
         if want("a17_mxfp8_gemm"):
             # MXFP8 GEMM on the block-scaled GEMM's headline shape (X and W_gu quantized in 1x32
-            # blocks): every 32-deep block promoted on its own, against a5's 128-deep chunks
+            # blocks): the tensor cores apply the 1x32 power-of-two scales themselves; the scale
+            # codes in the GEMM-ready tile layout (bulk-copied beside the operands), and as a
+            # second row row-major (reordered by a warp of the GEMM)
             try:
                 Xm = _bf16_dev(synth.bf16_normal((8192, 4096), 0, 1.0, 1e-3, 50.0), dev)
                 Wm = _bf16_dev(synth.bf16_normal((28672, 4096), 1000, 0.02), dev)
-                qxm, exm, qwm, ewm = u8(8192, 4096), u8(8192, 128), u8(28672, 4096), u8(28672, 128)
+                qxm, qwm = u8(8192, 4096), u8(28672, 4096)
+                exm, ewm = u8(8192, 128), u8(28672, 128)
+                ext, ewt = u8(8192 * 128), u8(28672 * 128)
                 fg.quant_mx(Xm, E, qxm, exm)
                 fg.quant_mx(Wm, E, qwm, ewm)
+                fg.quant_mx_tiled(Xm, E, qxm, ext)
+                fg.quant_mx_tiled(Wm, E, qwm, ewt)
                 del Xm, Wm
                 Dm = bf(8192, 28672)
                 put(self.tensor("a17_mxfp8_gemm_8192x28672x4096",
+                                lambda: fg.mx_gemm_tiled(qxm, E, ext, qwm, E, ewt, Dm), 2.0 * 8192 * 28672 * 4096,
+                                "MXFP8 1x32 x 1x32, BF16 out, block-scaled tcgen05 MMA (kind::mxf8f6f4), "
+                                "tiled scale codes"))
+                put(self.tensor("a17_mxfp8_gemm_rowmajor_scales_8192x28672x4096",
                                 lambda: fg.mx_gemm(qxm, E, exm, qwm, E, ewm, Dm), 2.0 * 8192 * 28672 * 4096,
-                                "MXFP8 1x32 x 1x32, BF16 out, a promotion per 32-deep block"))
-                del qxm, exm, qwm, ewm, Dm
+                                "as a17_mxfp8_gemm with row-major scale codes"))
+                del qxm, exm, qwm, ewm, ext, ewt, Dm
             except Exception as exc:
                 out["a17_mxfp8_gemm_8192x28672x4096"] = {"error": f"{type(exc).__name__}: {exc}"}
         if want("a2"):

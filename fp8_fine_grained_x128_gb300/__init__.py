@@ -97,9 +97,11 @@ _SIGS = {
     "fp8_quant_pertensor_current": (_INT, [_VP, _I64, _I64, _I64, _INT, _VP, _VP, _VP, _VP]),
     "fp8_quant_stats": (_INT, [_VP, _I64, _I64, _I64, _VP, _VP, _INT, _INT, _VP, _VP, _VP]),
     "fp8_quant_mx": (_INT, [_VP, _I64, _I64, _I64, _INT, _VP, _VP, _VP]),
+    "fp8_quant_mx_tiled": (_INT, [_VP, _I64, _I64, _I64, _INT, _VP, _VP, _VP]),
     "fp8_blockscaled_gemm": (_INT, [_I64, _I64, _I64, _VP, _INT, _VP, _INT, _VP, _INT, _VP, _INT,
                                     _VP, _INT, _I64, _VP]),
     "fp8_mx_gemm": (_INT, [_I64, _I64, _I64, _VP, _INT, _VP, _VP, _INT, _VP, _VP, _INT, _I64, _VP]),
+    "fp8_mx_gemm_tiled": (_INT, [_I64, _I64, _I64, _VP, _INT, _VP, _VP, _INT, _VP, _VP, _INT, _I64, _VP]),
     "fp8_grouped_gemm": (_INT, [_INT, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _INT, _I64,
                                 _VP]),
     "fp8_grouped_gemm_wgrad": (_INT, [_INT, _VP, _I64, _I64, _I64, _VP, _INT, _VP, _VP, _INT, _VP, _VP, _INT,
@@ -352,6 +354,15 @@ def quant_mx(x, fmt, q, e8, stream=None):
     _check("fp8_quant_mx", L.fp8_quant_mx(px, R, C, ld, fmt, *args, _stream(stream)))
 
 
+def quant_mx_tiled(x, fmt, q, e8t, stream=None):
+    """MXFP8 with the scale codes in the GEMM's 512-byte tile layout (R, C multiples of 128):
+    e8t holds R * C / 32 uint8 codes, any shape."""
+    L = lib()
+    px, R, C, ld = _mat(x, "x", _BF16)
+    args = (_buf(q, "q", _CODES, R * C), _buf(e8t, "e8t", (torch.uint8,), R * (C // 32)))
+    _check("fp8_quant_mx_tiled", L.fp8_quant_mx_tiled(px, R, C, ld, fmt, *args, _stream(stream)))
+
+
 # ------------------------------------------------------------------ GEMMs
 
 def _out_mat(D, rows, cols):
@@ -389,6 +400,22 @@ def mx_gemm(A, fmtA, eA, B, fmtB, eB, D, stream=None):
     peB = _buf(eB, "eB", (torch.uint8,), N * (K // 32))
     pD, out, ldD = _out_mat(D, M, N)
     _check("fp8_mx_gemm", L.fp8_mx_gemm(M, N, K, pA, fmtA, peA, pB, fmtB, peB, pD, out, ldD, _stream(stream)))
+
+
+def mx_gemm_tiled(A, fmtA, eAt, B, fmtB, eBt, D, stream=None):
+    """MXFP8 GEMM with the scale codes of A and B in the tiled layout quant_mx_tiled writes
+    (M * K / 32 and N * K / 32 uint8 codes, 16-byte aligned)."""
+    L = lib()
+    M, K = _shape(A, "A", 2)
+    N, KB = _shape(B, "B", 2)
+    if KB != K:
+        raise ValueError(f"B: shape {(N, KB)}, expected [N][{K}]")
+    pA, pB = _buf(A, "A", _CODES, M * K), _buf(B, "B", _CODES, N * K)
+    peA = _buf(eAt, "eAt", (torch.uint8,), M * (K // 32))
+    peB = _buf(eBt, "eBt", (torch.uint8,), N * (K // 32))
+    pD, out, ldD = _out_mat(D, M, N)
+    _check("fp8_mx_gemm_tiled",
+           L.fp8_mx_gemm_tiled(M, N, K, pA, fmtA, peA, pB, fmtB, peB, pD, out, ldD, _stream(stream)))
 
 
 def grouped_gemm(offsets, A, sA, B, sB, D, stream=None):

@@ -248,7 +248,20 @@ FP8FG_API int fp8_quant_mx(const void *x, int64_t rows, int64_t cols, int64_t ld
     if (ldx < cols) return FP8_ERR_SHAPE;
     if (!aligned16(x) || ldx % 8 != 0 || (reinterpret_cast<uintptr_t>(q) & 7u)) return FP8_ERR_ALIGNMENT;
     FP8FG_STATUS_OR_RETURN(st);
-    return launch_quant_mx(x, rows, cols, ldx, fmt, q, e8, st, S(stream));
+    return launch_quant_mx(x, rows, cols, ldx, fmt, q, e8, false, st, S(stream));
+}
+
+FP8FG_API int fp8_quant_mx_tiled(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, void *q,
+                                 uint8_t *e8_tiled, void *stream)
+{
+    if (!fmt_ok(fmt)) return FP8_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || rows % 128 != 0 || cols % 128 != 0) return FP8_ERR_SHAPE;
+    if (rows == 0 || cols == 0) return FP8_OK;
+    if (!x || !q || !e8_tiled) return FP8_ERR_INVALID_ARG;
+    if (ldx < cols) return FP8_ERR_SHAPE;
+    if (!aligned16(x) || ldx % 8 != 0 || (reinterpret_cast<uintptr_t>(q) & 7u)) return FP8_ERR_ALIGNMENT;
+    FP8FG_STATUS_OR_RETURN(st);
+    return launch_quant_mx(x, rows, cols, ldx, fmt, q, e8_tiled, true, st, S(stream));
 }
 
 FP8FG_API int fp8_quant_stats(const void *x, int64_t rows, int64_t cols, int64_t ldx, const void *q, const float *s,
@@ -295,9 +308,9 @@ FP8FG_API int fp8_blockscaled_gemm(int64_t M, int64_t N, int64_t K, const void *
     return launch_gemm(M, N, K, A, fmtA, sA, granA, B, fmtB, sB, granB, D, out_dtype, ldD, st, S(stream));
 }
 
-FP8FG_API int fp8_mx_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const uint8_t *eA,
-                          const void *B, int fmtB, const uint8_t *eB, void *D, int out_dtype, int64_t ldD,
-                          void *stream)
+static int mx_gemm_checked(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const uint8_t *eA,
+                           const void *B, int fmtB, const uint8_t *eB, bool tiled, void *D, int out_dtype,
+                           int64_t ldD, void *stream)
 {
     if (!fmt_ok(fmtA) || !fmt_ok(fmtB)) return FP8_ERR_INVALID_ARG;
     if (out_dtype != FP8_OUT_BF16 && out_dtype != FP8_OUT_F32) return FP8_ERR_INVALID_ARG;
@@ -310,12 +323,27 @@ FP8FG_API int fp8_mx_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fm
     if (!aligned16(D) || (ldD * esz) % 16 != 0) return FP8_ERR_ALIGNMENT;
     if (K > 0) {
         if (!A || !B || !eA || !eB) return FP8_ERR_INVALID_ARG;
-        if (!aligned16(A) || !aligned16(B) || (reinterpret_cast<uintptr_t>(eA) & 3u) ||
-            (reinterpret_cast<uintptr_t>(eB) & 3u))
+        const uintptr_t emask = tiled ? 15u : 3u;   // tiles are fetched by 16-byte bulk copies
+        if (!aligned16(A) || !aligned16(B) || (reinterpret_cast<uintptr_t>(eA) & emask) ||
+            (reinterpret_cast<uintptr_t>(eB) & emask))
             return FP8_ERR_ALIGNMENT;
     }
     FP8FG_STATUS_OR_RETURN(st);
-    return launch_gemm_mx(M, N, K, A, fmtA, eA, B, fmtB, eB, D, out_dtype, ldD, st, S(stream));
+    return launch_gemm_mx(M, N, K, A, fmtA, eA, B, fmtB, eB, tiled, D, out_dtype, ldD, st, S(stream));
+}
+
+FP8FG_API int fp8_mx_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const uint8_t *eA,
+                          const void *B, int fmtB, const uint8_t *eB, void *D, int out_dtype, int64_t ldD,
+                          void *stream)
+{
+    return mx_gemm_checked(M, N, K, A, fmtA, eA, B, fmtB, eB, false, D, out_dtype, ldD, stream);
+}
+
+FP8FG_API int fp8_mx_gemm_tiled(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const uint8_t *eA_tiled,
+                                const void *B, int fmtB, const uint8_t *eB_tiled, void *D, int out_dtype,
+                                int64_t ldD, void *stream)
+{
+    return mx_gemm_checked(M, N, K, A, fmtA, eA_tiled, B, fmtB, eB_tiled, true, D, out_dtype, ldD, stream);
 }
 
 FP8FG_API int fp8_grouped_gemm(int G, const int32_t *group_offsets, int64_t M_capacity, int64_t N, int64_t K,

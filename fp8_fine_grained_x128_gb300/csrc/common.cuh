@@ -202,13 +202,6 @@ struct Divider2 {
     }
 };
 
-// MXFP8 block scale X = 2^(e8 - 127) from its 8-bit exponent code (e8 = 0 is
-// the subnormal 2^-127).
-__device__ __forceinline__ float mx_scale_value(uint32_t e8)
-{
-    return e8 ? __uint_as_float(e8 << 23) : __uint_as_float(0x00400000u);
-}
-
 // SwiGLU element math (SwiGLU(g, u) = g * sigmoid(g) * u and its gradients),
 // shared by the standalone SwiGLU kernels and the quantizers that compute
 // SwiGLU while loading, so both round identically.  The 8-wide forms below
@@ -740,6 +733,31 @@ __device__ __forceinline__ void tc_mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, u
         : "memory");
 }
 
+// D(tmem) (+)= A(smem desc) x B(smem desc)^T with MXFP8 block scaling: FP8
+// operands, one UE8M0 scale per 32-deep block of every row of A and of B read
+// from tensor memory (sfa_tmem, sfb_tmem; which byte of the 32-bit word is in
+// the instruction descriptor), FP32 accumulator.
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Shared memory -> tensor memory: 32 rows of 16 bytes (row r at byte 16 r of
+// the source) land in lane r of every one of the four lane quarters, columns
+// [col, col + 4).  Ordered before the tcgen05.mma instructions this thread
+// issues after it.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // D(tmem) (+)= A(smem desc) x B(smem desc)^T, 16-bit operands (F16 or BF16 as
 // the instruction descriptor says), FP32 accumulator.
 __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -881,6 +899,19 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
     return d;
 }
 
+// Shared-memory descriptor of a plain (unswizzled) source for tcgen05.cp:
+// rows of 16 bytes stored contiguously, 8-row core matrices 128 bytes apart
+// (both byte offsets 128), version 1, no swizzle; 16-byte aligned start.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    return d;
+}
+
 // Shared-memory matrix descriptor for an MN-major operand tile in the
 // 128-byte swizzle layout a TMA load writes from a row-major matrix whose
 // rows run along K: each K index is a 128-byte row of 64 consecutive M (or
@@ -917,6 +948,21 @@ __host__ __device__ constexpr uint32_t idesc_f8f6f4(int fmtA, int fmtB, int M, i
 {
     return (1u << 4) | ((uint32_t)(fmtA == FP8_E5M2 ? 1 : 0) << 7) | ((uint32_t)(fmtB == FP8_E5M2 ? 1 : 0) << 10) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor of tcgen05.mma .kind::mxf8f6f4.block_scale: A type
+// bits 7-9 and B type bits 10-12 (0 = E4M3, 1 = E5M2), both operands K-major,
+// dense, N/8 at bits 17-22, scale type UE8M0 (bit 23 = 1), M/16 at bits
+// 24-28.  The byte of the 32-bit scale word each operand reads goes in bits
+// 29-30 (A) and 4-5 (B): idesc_mx_block(d, j) for the j-th 32-deep block.
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4(int fmtA, int fmtB, int M, int N)
+{
+    return ((uint32_t)(fmtA == FP8_E5M2 ? 1 : 0) << 7) | ((uint32_t)(fmtB == FP8_E5M2 ? 1 : 0) << 10) |
+           ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_mx_block(uint32_t idesc, uint32_t j)
+{
+    return idesc | (j << 4) | (j << 29);
 }
 
 }  // namespace fp8fg

@@ -9,7 +9,10 @@
 // running sum in registers with the chunk's two scales:
 //     acc[m][n] += sA(m, kb) * sB(n, kb) * P_kb[m][n].
 // For per-tensor scales (the coarse delayed-scaling recipe) the whole K is
-// accumulated in tensor memory and sA*sB applied once.
+// accumulated in tensor memory and sA*sB applied once.  MXFP8 (power-of-two
+// scales per 32-deep block of every row) needs no promotion in registers:
+// the tensor cores apply the scales themselves (kind::mxf8f6f4.block_scale)
+// and the whole K accumulates in one tensor-memory accumulator.
 //
 // Structure (one persistent CTA per SM, 384 threads = 3 warpgroups):
 //   warp 0      TMA producer: A tile 128x128 B and B tile BNx128 B per stage,
@@ -57,7 +60,7 @@ constexpr int kEpiWarp0 = 4;          // first epilogue warp (warpgroups 1 and 2
 // scales beside its accumulators)
 template <int SBG> struct RegSplit { static constexpr int kCtrl = 144, kEpi = 176; };
 template <> struct RegSplit<1> { static constexpr int kCtrl = 64, kEpi = 216; };
-template <> struct RegSplit<2> { static constexpr int kCtrl = 64, kEpi = 216; };
+template <> struct RegSplit<2> { static constexpr int kCtrl = 128, kEpi = 184; };  // MXFP8: the scale warp prefetches
 // the split must fit the registers the CTA is launched with
 template <int SBG>
 constexpr int regs_needed_at_launch()
@@ -88,15 +91,15 @@ struct GemmArgs {
     const uint8_t *eA;    // MXFP8: scale exponents [M][K/32] and [N][K/32] (X = 2^(e - 127))
     const uint8_t *eB;
     int64_t ldE;          // K / 32
+    int mx_vec;           // MXFP8: rows of exponents 16-byte aligned (16-byte loads of four chunks)
+    int mx_tiled;         // MXFP8: exponents in 512-byte tiles, fetched by the TMA producer
 };
 
-// Scale modes of the promotion: the 1x128 recipe with 128x128 B (one scalar
-// per column half), with 1x128 B (one value per column), and MXFP8 (one
-// power-of-two scale per 32-block of each row of A and of B: every MMA of
-// K = 32 is its own promotion chunk).
+// Scale modes: the 1x128 recipe with 128x128 B (one scalar per column half)
+// and with 1x128 B (one value per column), both promoted in registers; and
+// MXFP8 (one power-of-two scale per 32-block of each row of A and of B),
+// applied by the tensor cores from scale words staged in tensor memory.
 enum { SB_BLOCK = 0, SB_ROW = 1, SB_MX = 2 };
-// MMAs (K = 32 each) per promotion chunk
-template <int SBG> constexpr int chunk_mmas() { return SBG == SB_MX ? 1 : 4; }
 // Grouping of the tiles: none; by rows of A (MoE forward/dgrad: each M tile
 // belongs to one expert, whose B it uses); by K (MoE wgrad: each expert's
 // output is a full M x N matrix contracted over that expert's K chunks only).
@@ -104,7 +107,7 @@ enum { G_NONE = 0, G_ROWS = 1, G_K = 2 };
 
 constexpr int kScaleDepth = 4;     // chunks of scales staged ahead of the epilogue
 
-template <int BN, int STAGES, bool TSTORE>
+template <int BN, int STAGES, bool TSTORE, bool MX = false>
 struct GemmSmem {
     static constexpr int kA = 128 * 128;
     static constexpr int kB = BN * 128;
@@ -113,13 +116,25 @@ struct GemmSmem {
     static constexpr int kStg = TSTORE ? 128 * BN * 2 : 0;
     // per scale slot: row values for the two column halves + BN column values
     static constexpr int kScaleSlotFloats = 2 * 128 + BN;
-    static constexpr int kScaleBytes = kScaleDepth * kScaleSlotFloats * 4;
-    // TMEM accumulators of BN columns that alternate per chunk: all 512 columns
-    static constexpr int kNbuf = 512 / BN;
+    // MXFP8: per operand stage, one 32-bit word of four block exponents for
+    // each of the 128 rows of A and BN rows of B, in blocks of 128 rows laid
+    // out for tcgen05.cp 32x128b.warpx4 (row i at byte 512 (i / 128) +
+    // 16 (i % 32) + 4 ((i / 32) % 4))
+    static constexpr int kSfStage = (128 + BN) * 4;
+    static constexpr int kScaleBytes = MX ? STAGES * kSfStage : kScaleDepth * kScaleSlotFloats * 4;
+    // TMEM accumulators of BN columns: for the promotion modes two or four
+    // alternating per chunk over all 512 columns; for MXFP8 one (BN = 256) or
+    // two (BN = 128) per tile, followed by a ring of scale words, one set per
+    // operand stage: A in 4 columns (row m at lane m, column m / 32), B in
+    // BN / 32 columns (row n at lane n % 32 of every lane quarter, column n / 32)
+    static constexpr int kNbuf = MX ? (BN == 256 ? 1 : 2) : 512 / BN;
+    static constexpr int kSfCol0 = kNbuf * BN;
+    static constexpr int kSfCols = 4 + BN / 32;
+    static_assert(!MX || kSfCol0 + STAGES * kSfCols <= 512, "MXFP8 scale ring beyond the tensor memory");
     static constexpr int kBars = 2 * STAGES + 2 * kNbuf + 1 + 2 * kScaleDepth;
     static constexpr int kCtrl = kBars * 8 + 16;
     static constexpr int kBytes = 1024 + STAGES * kStage + kStg + kScaleBytes + kCtrl + 4 * (kMaxGroups + 1);
-    static constexpr int kTmemCols = kNbuf * BN;
+    static constexpr int kTmemCols = 512;
 };
 
 // Largest g with off[g] <= row (skips empty groups).
@@ -214,18 +229,72 @@ __device__ __forceinline__ void store_pair(void *D, int64_t ldD, int out_f32, in
     else *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(D) + row * ldD + col) = bf16x2_rn(lo, hi);
 }
 
+// MXFP8 scale words of one group of up to four consecutive 128-deep chunks
+// [c0, c0 + size) of a tile: w[i] holds, for this lane's row of slot i (rows
+// lane + 32 i of A for i < 4, rows lane + 32 (i - 4) of B after), the words of
+// the group's chunks in .x .. .w -- one 16-byte load per row when the rows are
+// 16-byte aligned and the group is whole, else one 4-byte load per chunk.
+template <int BN>
+__device__ __forceinline__ void mx_load_group(uint4 (&w)[4 + BN / 32], const GemmArgs &a, const TileInfo &ti, int c0,
+                                              int size, int lane)
+{
+    const bool vec = a.mx_vec && size == 4;
+#pragma unroll
+    for (int i = 0; i < 4 + BN / 32; ++i) {
+        const int64_t r = i < 4 ? ti.a_row + lane + 32 * i : ti.b_row + lane + 32 * (i - 4);
+        const uint8_t *p = (i < 4 ? a.eA : a.eB) + r * a.ldE + 4 * c0;
+        if (vec) {
+            w[i] = __ldg(reinterpret_cast<const uint4 *>(p));
+        } else {
+            const uint32_t *q = reinterpret_cast<const uint32_t *>(p);
+            w[i].x = __ldg(q);
+            w[i].y = size > 1 ? __ldg(q + 1) : 0u;
+            w[i].z = size > 2 ? __ldg(q + 2) : 0u;
+            w[i].w = size > 3 ? __ldg(q + 3) : 0u;
+        }
+    }
+}
+
+// Writes the group's stages [it0, it0 + size) into their shared-memory slots
+// in the tcgen05.cp layout, each once its stage is free, and arrives on the
+// stage's full barrier.  False on an abort.
+template <int BN, int STAGES>
+__device__ __forceinline__ bool mx_write_group(const uint4 (&w)[4 + BN / 32], uint32_t it0, int size, uint8_t *sfw,
+                                               int sf_stage_bytes, uint64_t *full, uint64_t *empty,
+                                               volatile int *abort_flag, int *status, int lane)
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (j >= size) break;
+        const uint32_t it = it0 + j;
+        const int s = it % STAGES;
+        if (!warp_wait_or_abort(&empty[s], ((it / STAGES) & 1) ^ 1, abort_flag, status)) return false;
+        uint4 *dst = reinterpret_cast<uint4 *>(sfw + s * sf_stage_bytes);
+#pragma unroll
+        for (int b = 0; b < 1 + BN / 128; ++b) {
+            const uint32_t *c0 = &w[4 * b].x, *c1 = &w[4 * b + 1].x, *c2 = &w[4 * b + 2].x, *c3 = &w[4 * b + 3].x;
+            dst[32 * b + lane] = make_uint4(c0[j], c1[j], c2[j], c3[j]);
+        }
+        fence_proxy_async_smem();   // visible to the tensor memory copy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+    }
+    return true;
+}
+
 template <int BN, int STAGES, bool PROMOTE, int SBG, int GMODE, bool TSTORE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmD, uint32_t idesc, GemmArgs a)
 {
-    using L = GemmSmem<BN, STAGES, TSTORE>;
+    using L = GemmSmem<BN, STAGES, TSTORE, SBG == SB_MX>;
     constexpr int HALF = BN / 2;        // columns per epilogue thread
     constexpr int NP = HALF / 2;        // packed FP32 pairs per epilogue thread
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stg = smem + STAGES * L::kStage;                                  // TMA-store staging
     float *scl = reinterpret_cast<float *>(stg + L::kStg);                    // [kScaleDepth][slot floats]
+    uint8_t *sfw = stg + L::kStg;                                             // MXFP8: [STAGES][kSfStage]
     uint64_t *full = reinterpret_cast<uint64_t *>(stg + L::kStg + L::kScaleBytes);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
@@ -243,7 +312,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            // MXFP8 with row-major exponents: the stage's scale words arrive
+            // from warp 2 beside the TMA bytes
+            mbar_init(&full[s], SBG == SB_MX && !a.mx_tiled ? 2 : 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < L::kNbuf; ++b) {
@@ -306,9 +377,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!wait_or_abort(&empty[s], ph ^ 1, abort_flag, a.status)) { ok = false; break; }
                     uint8_t *st = smem + s * L::kStage;
-                    mbar_arrive_expect_tx(&full[s], L::kStage);
+                    const bool sf_bulk = SBG == SB_MX && a.mx_tiled;
+                    mbar_arrive_expect_tx(&full[s], L::kStage + (sf_bulk ? L::kSfStage : 0));
                     tma_load_2d(st, &tmA, &full[s], (ti.kg0 + kb) * 128, ti.a_row);
                     tma_load_2d(st + L::kA, &tmB, &full[s], (ti.kg0 + kb) * 128, ti.b_row);
+                    if (sf_bulk) {
+                        // MXFP8, tiled exponents: the chunk's 512-byte tile of A's 128 rows
+                        // and the BN / 128 consecutive tiles of B's rows, already in the
+                        // tcgen05.cp layout
+                        const int64_t kc = ti.kg0 + kb;
+                        bulk_load(sfw + s * L::kSfStage, a.eA + (kc * (a.M / 128) + ti.a_row / 128) * 512, 512,
+                                  &full[s]);
+                        bulk_load(sfw + s * L::kSfStage + 512, a.eB + (kc * (a.N / 128) + ti.b_row / 128) * 512,
+                                  BN * 4, &full[s]);
+                    }
                     ++it;
                 }
             }
@@ -329,28 +411,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int kb = 0; kb < nk; ++kb) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
-                    if (SBG == SB_MX) {
-                        // each 32-deep block into an accumulator of its own
-                        if (!wait_or_abort(&full[s], ph, abort_flag, a.status)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(smem + s * L::kStage));
-                        const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * L::kStage + L::kA));
-                        for (int k = 0; k < 4 && ok; ++k) {
-                            buf = cc % L::kNbuf;
-                            if (!wait_or_abort(&tempty[buf], ((cc / L::kNbuf) & 1) ^ 1, abort_flag, a.status)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            tc_mma_f8f6f4(tmem_base + buf * BN, adesc + 2 * k, bdesc + 2 * k, idesc, 0u);
-                            tc_commit(&tfull[buf]);
-                            ++cc;
-                        }
-                        if (!ok) break;
-                        tc_commit(&empty[s]);
-                        ++it;
-                        continue;
-                    }
                     if (PROMOTE) {
                         buf = cc % L::kNbuf;
                         if (!wait_or_abort(&tempty[buf], ((cc / L::kNbuf) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
@@ -360,11 +420,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t d_tmem = tmem_base + buf * BN;
                     const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(smem + s * L::kStage));
                     const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smem + s * L::kStage + L::kA));
+                    if (SBG == SB_MX) {
+                        // the stage's scale words into its tensor-memory slot (ordered
+                        // before the MMAs below), then one block-scaled MMA per
+                        // 32-deep block reading byte k of every row's word
+                        const uint32_t sf_a = tmem_base + L::kSfCol0 + s * L::kSfCols, sf_b = sf_a + 4;
+                        const uint64_t sd = sdesc_rows16(smem_u32(sfw + s * L::kSfStage));
+                        tc_cp_32x128b_warpx4(sf_a, sd);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        // advance 32 bytes (K = 32 FP8) inside the 128-byte swizzled row
-                        tc_mma_f8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
-                                      (k > 0 || (!PROMOTE && kb > 0)) ? 1u : 0u);
+                        for (int b = 0; b < BN / 128; ++b) tc_cp_32x128b_warpx4(sf_b + 4 * b, sd + 32 * (1 + b));
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma_mx(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mx_block(idesc, k), sf_a, sf_b,
+                                      (k > 0 || kb > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            // advance 32 bytes (K = 32 FP8) inside the 128-byte swizzled row
+                            tc_mma_f8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+                                          (k > 0 || (!PROMOTE && kb > 0)) ? 1u : 0u);
+                        }
                     }
                     // the stage goes back to the producer as soon as these MMAs
                     // have read it, whatever the epilogue is doing
@@ -384,44 +459,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // every MMA issued by this thread completes before the CTA frees TMEM
             tc_commit(mma_done);
             mbar_wait_bounded(mma_done, 0, nullptr);
-        } else if (SBG == SB_MX && warp == 2) {
+        } else if (SBG == SB_MX && warp == 2 && !a.mx_tiled) {
             // -------------------------------------------------- MX scale producer
-            // The whole warp: per 128-deep stage it loads the 4 exponent bytes of
-            // each of the tile's 128 rows of A and BN rows of B (one 32-bit load
-            // per row: [rows][K/32] layout), then for each of the stage's four
-            // 32-blocks writes X = 2^(e - 127) of every row into a slot (rows of A
-            // at [0, 128), rows of B at [256, 256 + BN)).
-            uint32_t cs = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                const TileInfo ti = tile_info<BN, GMODE>(tile, num_mt, num_nt, a, sh_off);
-                for (int kb = ti.kg0; kb < ti.kg0 + ti.nk && ok; ++kb) {
-                    uint32_t ea[4], eb[BN / 32];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        ea[i] = *reinterpret_cast<const uint32_t *>(a.eA + (int64_t)(ti.a_row + lane + 32 * i) * a.ldE +
-                                                                    4 * kb);
-#pragma unroll
-                    for (int i = 0; i < BN / 32; ++i)
-                        eb[i] = *reinterpret_cast<const uint32_t *>(a.eB + (int64_t)(ti.b_row + lane + 32 * i) * a.ldE +
-                                                                    4 * kb);
-                    for (int j = 0; j < 4; ++j, ++cs) {
-                        const int slot = cs % kScaleDepth;
-                        if (!warp_wait_or_abort(&sc_empty[slot], ((cs / kScaleDepth) & 1) ^ 1, abort_flag, a.status)) {
-                            ok = false;
-                            break;
-                        }
-                        float *sv = scl + slot * L::kScaleSlotFloats;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) sv[lane + 32 * i] = mx_scale_value((ea[i] >> (8 * j)) & 0xFFu);
-#pragma unroll
-                        for (int i = 0; i < BN / 32; ++i)
-                            sv[256 + lane + 32 * i] = mx_scale_value((eb[i] >> (8 * j)) & 0xFFu);
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&sc_full[slot]);
-                    }
+            // The whole warp, in step with the operand stages: per 128-deep stage
+            // it writes the 32-bit word of four block exponents of each of the
+            // tile's 128 rows of A and BN rows of B ([rows][K/32] bytes) in the
+            // tcgen05.cp layout -- lane j stores the words of rows j, j + 32,
+            // j + 64, j + 96 of each block of 128 rows as one 16-byte row -- once
+            // the stage is free, then arrives on the stage's full barrier (the
+            // second of its two arrivals).  The words are loaded a group of four
+            // stages at a time (one 16-byte load per row: each row's word sits
+            // in a line of its own, so per-stage 4-byte loads cost four times
+            // the requests), double-buffered in registers: the next group's
+            // loads are in flight while this group is written.
+            constexpr int kW = 4 + BN / 32;
+            const int nk = a.K / 128, ng = (nk + 3) / 4;   // chunks and groups per tile
+            const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+            const int ngroups = my_tiles * ng;
+            uint4 w0[kW], w1[kW];
+            // group g: tile g / ng of this CTA, chunks [4 (g % ng), +4) of it
+#define FP8FG_MX_GROUP(g, tl, q, ti) \
+    const int tl = (g) / ng, q = (g) - tl * ng; \
+    const TileInfo ti = tile_info<BN, GMODE>(blockIdx.x + tl * gridDim.x, num_mt, num_nt, a, sh_off)
+            if (ngroups > 0) {
+                FP8FG_MX_GROUP(0, tl, q, ti);
+                mx_load_group<BN>(w0, a, ti, 4 * q, min(4, nk - 4 * q), lane);
+            }
+            for (int g = 0; g < ngroups; g += 2) {
+                if (g + 1 < ngroups) {
+                    FP8FG_MX_GROUP(g + 1, tl, q, ti);
+                    mx_load_group<BN>(w1, a, ti, 4 * q, min(4, nk - 4 * q), lane);
+                }
+                {
+                    FP8FG_MX_GROUP(g, tl, q, ti);
+                    if (!mx_write_group<BN, STAGES>(w0, (uint32_t)(tl * nk + 4 * q), min(4, nk - 4 * q), sfw,
+                                                    L::kSfStage, full, empty, abort_flag, a.status, lane))
+                        break;
+                }
+                if (g + 1 >= ngroups) break;
+                if (g + 2 < ngroups) {
+                    FP8FG_MX_GROUP(g + 2, tl, q, ti);
+                    mx_load_group<BN>(w0, a, ti, 4 * q, min(4, nk - 4 * q), lane);
+                }
+                {
+                    FP8FG_MX_GROUP(g + 1, tl, q, ti);
+                    if (!mx_write_group<BN, STAGES>(w1, (uint32_t)(tl * nk + 4 * q), min(4, nk - 4 * q), sfw,
+                                                    L::kSfStage, full, empty, abort_flag, a.status, lane))
+                        break;
                 }
             }
+#undef FP8FG_MX_GROUP
         } else if (PROMOTE && warp == 2 && lane == 0) {
             // -------------------------------------------------- scale producer
             // Slot layout: [0, 128) sA of the tile's rows (1x128 A) or [128]
@@ -498,7 +585,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 uint64_t acc[NP];
 #pragma unroll
                 for (int i = 0; i < NP; ++i) acc[i] = 0ull;
-                const int nchunks = ti.nk * (4 / chunk_mmas<SBG>());
+                const int nchunks = ti.nk;
                 for (int kb = 0; kb < nchunks; ++kb) {
                     const uint32_t buf = cc & (L::kNbuf - 1);
                     const uint32_t slot = cc & (kScaleDepth - 1);
@@ -631,6 +718,70 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         }
                     }
                 }
+            } else if (SBG == SB_MX) {
+                // The tile's accumulator is read into registers at once and handed
+                // back, so the next tile's MMAs run while this one is converted
+                // and stored.
+                const uint32_t buf = cc % L::kNbuf;
+                uint32_t r[HALF / 32][32];
+                if (warp_wait_or_abort(&tfull[buf], (cc / L::kNbuf) & 1, abort_flag, a.status)) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int j = 0; j < HALF / 32; ++j) tc_ld_32x32b_x32(tm_row + buf * BN + 32 * j, r[j]);
+                    tc_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[buf]);
+                    ++cc;
+                } else {
+                    ok = false;
+                }
+                if (TSTORE) {
+                    // same protocol as the promotion modes' staged store
+                    const bool elected = threadIdx.x == kEpiWarp0 * 32;
+                    if (elected) bulk_wait_read_all();
+                    named_bar_sync(1, kEpiWarps * 32);
+                    if (ok) {
+#pragma unroll
+                        for (int k = 0; k < HALF / 8; ++k) {
+                            const int col = colbase + 8 * k;
+                            const uint32_t *v = &r[k / 4][8 * (k % 4)];
+                            const uint4 w = make_uint4(
+                                bf16x2_rn(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                                bf16x2_rn(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                                bf16x2_rn(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                                bf16x2_rn(__uint_as_float(v[6]), __uint_as_float(v[7])));
+                            *reinterpret_cast<uint4 *>(stg + (col >> 6) * 16384 + row * 128 +
+                                                       ((((col >> 3) & 7) ^ (row & 7)) << 4)) = w;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    named_bar_sync(1, kEpiWarps * 32);
+                    if (elected) {
+                        const int go = *abort_flag == 0;
+                        *tile_go = go;
+                        if (go) {
+#pragma unroll
+                            for (int b = 0; b < BN / 64; ++b) tma_store_2d(&tmD, stg + b * 16384, n0 + 64 * b, (int)m0);
+                            bulk_commit_group();
+                        }
+                    }
+                    named_bar_sync(1, kEpiWarps * 32);
+                    if (!*tile_go) {
+                        ok = false;
+                        break;
+                    }
+                    continue;
+                }
+                if (!ok) break;
+#pragma unroll
+                for (int j = 0; j < HALF / 32; ++j) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[j][i]);
+                    if (dbg_cell((int64_t)m0 + row, (int64_t)n0 + colbase + j * 32, 32, out_rows, a.N, a.status))
+                        store_row<32>(a.D, a.ldD, a.out_f32, (int64_t)m0 + row, (int64_t)n0 + colbase + j * 32, v);
+                }
             } else {
                 const uint32_t buf = cc % L::kNbuf;
                 const float sab = a.sA[0] * a.sB[0];
@@ -721,7 +872,7 @@ template <int BN, int STAGES, bool PROMOTE, int SBG, int GMODE, bool TSTORE = fa
 static int run_gemm(const CUtensorMap &mA, const CUtensorMap &mB, const CUtensorMap &mD, uint32_t idesc,
                     const GemmArgs &args, int grid, cudaStream_t st)
 {
-    using L = GemmSmem<BN, STAGES, TSTORE>;
+    using L = GemmSmem<BN, STAGES, TSTORE, SBG == SB_MX>;
     static_assert(L::kBytes <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
     auto kern = k_gemm<BN, STAGES, PROMOTE, SBG, GMODE, TSTORE>;
     static bool attr_done[64] = {};
@@ -793,10 +944,12 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const 
     }
 }
 
-// MXFP8: every 32-deep block of K is multiplied into an accumulator of its own
-// and promoted with X_A(m, b) * X_B(n, b) = 2^(eA + eB - 254).
+// MXFP8: the tensor cores apply X_A(m, b) * X_B(n, b) = 2^(eA + eB - 254) to
+// every 32-deep block (kind::mxf8f6f4.block_scale) and the whole K accumulates
+// in tensor memory.
 int launch_gemm_mx(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const uint8_t *eA, const void *B,
-                   int fmtB, const uint8_t *eB, void *D, int out_dtype, int64_t ldD, int *status, cudaStream_t st)
+                   int fmtB, const uint8_t *eB, bool tiled, void *D, int out_dtype, int64_t ldD, int *status,
+                   cudaStream_t st)
 {
     if (M == 0 || N == 0) return FP8_OK;
     if (K == 0) {
@@ -813,7 +966,7 @@ int launch_gemm_mx(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, con
     g.M = (int)M;
     g.N = (int)N;
     g.K = (int)K;
-    g.granA = FP8_GRAN_1x128;   // per-row scales of A in the slot
+    g.granA = FP8_GRAN_1x128;
     g.D = D;
     g.ldD = ldD;
     g.out_f32 = out_dtype == FP8_OUT_F32;
@@ -821,12 +974,21 @@ int launch_gemm_mx(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, con
     g.eA = eA;
     g.eB = eB;
     g.ldE = K / 32;
+    g.mx_vec = (K % 512 == 0) && (reinterpret_cast<uintptr_t>(eA) % 16 == 0) && (reinterpret_cast<uintptr_t>(eB) % 16 == 0);
+    g.mx_tiled = tiled;
     g.raster_gm = raster_band(M, M * K, N * K);
     const int64_t ntiles = (M / 128) * (N / BN);
     const int grid = (int)std::min<int64_t>(ntiles, sm_count());
-    const uint32_t idesc = idesc_f8f6f4(fmtA, fmtB, 128, BN);
-    if (BN == 256) return run_gemm<256, 4, true, SB_MX, G_NONE>(mA, mB, mA, idesc, g, grid, st);
-    return run_gemm<128, 6, true, SB_MX, G_NONE>(mA, mB, mA, idesc, g, grid, st);
+    const uint32_t idesc = idesc_mxf8f6f4(fmtA, fmtB, 128, BN);
+    if (BN == 256) {
+        if (!g.out_f32 && K <= kTmaStoreMaxK) {
+            CUtensorMap mD;
+            if (!make_out_map(&mD, D, (uint64_t)N, (uint64_t)M, (uint64_t)ldD)) return FP8_ERR_CUDA;
+            return run_gemm<256, 3, false, SB_MX, G_NONE, true>(mA, mB, mD, idesc, g, grid, st);
+        }
+        return run_gemm<256, 4, false, SB_MX, G_NONE>(mA, mB, mA, idesc, g, grid, st);
+    }
+    return run_gemm<128, 6, false, SB_MX, G_NONE>(mA, mB, mA, idesc, g, grid, st);
 }
 
 int launch_grouped_gemm(int G, const int32_t *offsets, int64_t Mcap, int64_t N, int64_t K, const void *A,

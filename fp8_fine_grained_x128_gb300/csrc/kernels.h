@@ -18,8 +18,9 @@ int *status_word_ptr();
 // quant.cu
 int launch_quant_1x128(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, void *q, float *s,
                        void *qT, float *sT, int *status, cudaStream_t st);
+// tiled: scale codes in the GEMM's 512-byte tile layout instead of row-major
 int launch_quant_mx(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, void *q, uint8_t *e8,
-                    int *status, cudaStream_t st);
+                    bool tiled, int *status, cudaStream_t st);
 int launch_quant_128x128(const void *w, int64_t rows, int64_t cols, int64_t ldw, int fmt, void *q, float *s,
                          void *qT, float *sT, int *status, cudaStream_t st);
 // batch matrices of [rows][cols] stored back to back (scales likewise)
@@ -51,7 +52,8 @@ int launch_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const 
                 const void *B, int fmtB, const float *sB, int granB, void *D, int out_dtype, int64_t ldD,
                 int *status, cudaStream_t st);
 int launch_gemm_mx(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const uint8_t *eA, const void *B,
-                   int fmtB, const uint8_t *eB, void *D, int out_dtype, int64_t ldD, int *status, cudaStream_t st);
+                   int fmtB, const uint8_t *eB, bool tiled, void *D, int out_dtype, int64_t ldD, int *status,
+                   cudaStream_t st);
 int launch_grouped_gemm(int G, const int32_t *offsets, int64_t Mcap, int64_t N, int64_t K, const void *A,
                         const float *sA, const void *B, const float *sB, void *D, int out_dtype, int64_t ldD,
                         int *status, cudaStream_t st);

@@ -12,6 +12,12 @@
 // power of two, so no element saturates); an all-zero block gets X = 1.  The
 // codes are RNE_satfinite(x / X), and x / X = x * 2^-e is an exact product.
 //
+// The scale codes go out either row-major [rows][cols/32] or in the layout the
+// MXFP8 GEMM copies straight into tensor memory ("tiled"): for rows and cols
+// multiples of 128, the codes of rows 128 rb .. 128 rb + 127 and 32-blocks
+// 4 kc .. 4 kc + 3 form a 512-byte tile at (kc * rows/128 + rb) * 512, row r
+// at byte 16 (r % 32) + 4 ((r % 128) / 32) + (block % 4) inside it.
+//
 // A streaming kernel (HBM-bound: 2 B read, 1 + 1/32 B written per element):
 // every lane loads 16 bytes (8 BF16), four consecutive lanes hold one block
 // and reduce its amax with two shuffles, and the exponent is read off the
@@ -59,7 +65,7 @@ __device__ __forceinline__ uint2 mx_codes8(uint4 v, float inv)
 // lane, loaded before any is used).  A row holds cols / 8 vectors, a multiple
 // of 4, so the four lanes of a quad always share one block; all 32 lanes run
 // every iteration (lanes past the end carry zeros) so the shuffles are full.
-template <int FMT>
+template <int FMT, bool TILED>
 __global__ void __launch_bounds__(256) k_quant_mx(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
                                                   int64_t ldx, uint8_t *__restrict__ q, uint8_t *__restrict__ e8,
                                                   int *status)
@@ -93,13 +99,20 @@ __global__ void __launch_bounds__(256) k_quant_mx(const uint16_t *__restrict__ x
             const float inv = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e in [-127, 120]
             const uint2 codes = mx_codes8<FMT>(v[u], inv);
             if (dbg_span(i * 8, 8, rows * cols, status)) *reinterpret_cast<uint2 *>(q + i * 8) = codes;
-            if ((lane & 3) == 0 && dbg_span(i >> 2, 1, rows * (cols / 32), status)) e8[i >> 2] = (uint8_t)(e + 127);
+            if ((lane & 3) == 0) {
+                int64_t off = i >> 2;   // block index, row-major
+                if (TILED) {
+                    const int64_t kb = cols / 32, r = off / kb, k = off - r * kb;
+                    off = ((k >> 2) * (rows >> 7) + (r >> 7)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (k & 3);
+                }
+                if (dbg_span(off, 1, rows * (cols / 32), status)) e8[off] = (uint8_t)(e + 127);
+            }
         }
     }
 }
 
 int launch_quant_mx(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, void *q, uint8_t *e8,
-                    int *status, cudaStream_t st)
+                    bool tiled, int *status, cudaStream_t st)
 {
     const int64_t nvec = rows * (cols / 8);
     if (nvec == 0) return FP8_OK;
@@ -108,10 +121,13 @@ int launch_quant_mx(const void *x, int64_t rows, int64_t cols, int64_t ldx, int 
         (unsigned)std::max<int64_t>(1, std::min<int64_t>((nvec + per_block - 1) / per_block, (int64_t)sm_count() * 4));
     auto X = static_cast<const uint16_t *>(x);
     auto Q = static_cast<uint8_t *>(q);
-    if (fmt == FP8_E5M2)
-        k_quant_mx<FP8_E5M2><<<grid, 256, 0, st>>>(X, rows, cols, ldx, Q, e8, status);
-    else
-        k_quant_mx<FP8_E4M3><<<grid, 256, 0, st>>>(X, rows, cols, ldx, Q, e8, status);
+    if (fmt == FP8_E5M2) {
+        if (tiled) k_quant_mx<FP8_E5M2, true><<<grid, 256, 0, st>>>(X, rows, cols, ldx, Q, e8, status);
+        else k_quant_mx<FP8_E5M2, false><<<grid, 256, 0, st>>>(X, rows, cols, ldx, Q, e8, status);
+    } else {
+        if (tiled) k_quant_mx<FP8_E4M3, true><<<grid, 256, 0, st>>>(X, rows, cols, ldx, Q, e8, status);
+        else k_quant_mx<FP8_E4M3, false><<<grid, 256, 0, st>>>(X, rows, cols, ldx, Q, e8, status);
+    }
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

@@ -237,6 +237,19 @@ FP8FG_API int fp8_quant_pertensor_current(const void *x, int64_t rows, int64_t c
 FP8FG_API int fp8_quant_mx(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt,
                            void *q, uint8_t *e8, void *stream);
 
+/* fp8_quant_mx with the scale codes written in the layout fp8_mx_gemm_tiled
+ * reads (the library's own layout; the pages fix none): for rows and cols
+ * multiples of 128, the codes of rows 128 rb .. 128 rb + 127 and 32-blocks
+ * 4 kc .. 4 kc + 3 form one 512-byte tile at byte (kc * rows/128 + rb) * 512;
+ * inside it the code of row r, block b sits at byte
+ * 16 (r % 32) + 4 ((r % 128) / 32) + (b % 4).  Same codes, values and
+ * errors as fp8_quant_mx; only the position of each scale code differs.
+ *   x, q: as fp8_quant_mx.  rows % 128 == 0, cols % 128 == 0.
+ *   e8_tiled: rows * cols / 32 bytes (16-byte aligned if fp8_mx_gemm_tiled
+ *   will read it).  rows or cols == 0 is a no-op. */
+FP8FG_API int fp8_quant_mx_tiled(const void *x, int64_t rows, int64_t cols, int64_t ldx, int fmt, void *q,
+                                 uint8_t *e8_tiled, void *stream);
+
 /* MXFP8 GEMM ([Infra] "Scaling strategies and stability": per-block scaling,
  * each block of a tensor with its own scale factor; "Blackwell MXFP8 and
  * NVFP4: looking ahead"; block and scale encoding per the readings of
@@ -244,15 +257,26 @@ FP8FG_API int fp8_quant_mx(const void *x, int64_t rows, int64_t cols, int64_t ld
  * fmtB), K contiguous, and their scale exponents eA [M][K/32], eB [N][K/32]
  * as fp8_quant_mx writes them (X = 2^(e - 127)):
  *   D[m][n] = sum_b X_A(m, b) * X_B(n, b) * sum_{k in 32-block b} qA[m][k] * qB[n][k].
- * Every 32-block is multiplied on the tensor cores into an FP32 accumulator
- * of its own and promoted into an FP32 running sum with its two scales (the
- * same scheme as fp8_blockscaled_gemm's 128-deep chunks, four times as
- * often).  D [M][ldD] BF16 (RN) or FP32.  M, N, K % 128 == 0; A, B, D
- * 16-byte aligned, eA, eB 4-byte aligned, ldD * element size a multiple of
- * 16 bytes.  K == 0 writes zeros; M or N == 0 is a no-op. */
+ * The tensor cores apply the two scales to every 32-block themselves
+ * (tcgen05.mma kind::mxf8f6f4.block_scale, scale codes read as UE8M0) and
+ * accumulate the whole K in FP32 in tensor memory; no promotion in
+ * registers.  Scale codes are 0..254 (what fp8_quant_mx writes; the format
+ * reads 255 as NaN).  D [M][ldD] BF16 (RN) or FP32.  M, N, K % 128 == 0; A,
+ * B, D 16-byte aligned, eA, eB 4-byte aligned, ldD * element size a
+ * multiple of 16 bytes.  K == 0 writes zeros; M or N == 0 is a no-op. */
 FP8FG_API int fp8_mx_gemm(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const uint8_t *eA,
                           const void *B, int fmtB, const uint8_t *eB, void *D, int out_dtype, int64_t ldD,
                           void *stream);
+
+/* fp8_mx_gemm with both operands' scale codes in the tiled layout of
+ * fp8_quant_mx_tiled (eA_tiled for M rows, eB_tiled for N rows, K / 32 codes
+ * per row).  The tiles are fetched by bulk copies beside the operand tiles, so
+ * no thread of the GEMM reorders them; the result is bit-identical to
+ * fp8_mx_gemm on the same codes.  eA_tiled and eB_tiled 16-byte aligned;
+ * everything else as fp8_mx_gemm. */
+FP8FG_API int fp8_mx_gemm_tiled(int64_t M, int64_t N, int64_t K, const void *A, int fmtA, const uint8_t *eA_tiled,
+                                const void *B, int fmtB, const uint8_t *eB_tiled, void *D, int out_dtype,
+                                int64_t ldD, void *stream);
 
 /* The same delayed-scaling step for callers that cannot allocate device
  * memory -- for example code that runs inside another framework's fixed

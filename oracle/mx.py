@@ -98,6 +98,28 @@ def dequant_mx(q: np.ndarray, e8: np.ndarray, fmt: int = E4M3) -> np.ndarray:
     return (d * np.ldexp(1.0, e8.astype(np.int64) - E8_BIAS)[..., None]).reshape(R, C)
 
 
+def mx_tile_scales(e8: np.ndarray) -> np.ndarray:
+    """The library's GEMM-ready arrangement of MXFP8 scale codes (a layout of
+    its own; the pages fix none): e8 [R, KB] with R % 128 == 0 and KB % 4 ==
+    0 becomes R * KB bytes in which the codes of rows 128 rb .. 128 rb + 127
+    and 32-blocks 4 kc .. 4 kc + 3 form the 512-byte tile number
+    kc * (R / 128) + rb, and the code of row r, block b sits at byte
+    16 (r % 32) + 4 ((r % 128) // 32) + b % 4 inside its tile.  A pure
+    permutation of the codes."""
+    e8 = np.asarray(e8, np.uint8)
+    R, KB = e8.shape
+    if R % 128 or KB % 4:
+        raise ValueError("rows must be a multiple of 128 and blocks a multiple of 4")
+    t = e8.reshape(R // 128, 4, 32, KB // 4, 4)          # [rb][(r % 128) // 32][r % 32][kc][b % 4]
+    return np.ascontiguousarray(t.transpose(3, 0, 2, 1, 4)).reshape(-1)
+
+
+def mx_untile_scales(tiled: np.ndarray, R: int, KB: int) -> np.ndarray:
+    """Inverse of mx_tile_scales."""
+    t = np.asarray(tiled, np.uint8).reshape(KB // 4, R // 128, 32, 4, 4)
+    return np.ascontiguousarray(t.transpose(1, 3, 2, 0, 4)).reshape(R, KB)
+
+
 def mx_gemm_points(qA, eA, fmtA, qB, eB, fmtB, pm, pn, chunk: int = 2048) -> np.ndarray:
     """R16 at the output points (pm, pn): A [M, K] and B [N, K] MXFP8 (scale
     codes [M, K/32] and [N, K/32]); unrounded FP64 values."""

@@ -168,6 +168,24 @@ def test_host_validation_without_launch(lib):
     assert lib.fp8_quant_mx(good, 4, 64, 68, 0, good, good, S) == fg.ERR_ALIGNMENT
     assert lib.fp8_quant_mx(good, 4, 64, 64, 0, P(4100), good, S) == fg.ERR_ALIGNMENT
     assert lib.fp8_quant_mx(None, 0, 64, 64, 1, None, None, S) == fg.OK
+    # MXFP8 quantizer, tiled scale codes: whole 128 x 128 tiles only
+    assert lib.fp8_quant_mx_tiled(good, 100, 128, 128, 0, good, good, S) == fg.ERR_SHAPE
+    assert lib.fp8_quant_mx_tiled(good, 128, 64, 64, 0, good, good, S) == fg.ERR_SHAPE
+    assert lib.fp8_quant_mx_tiled(good, 128, 128, 128, 5, good, good, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_quant_mx_tiled(good, 128, 128, 128, 0, good, None, S) == fg.ERR_INVALID_ARG
+    assert lib.fp8_quant_mx_tiled(odd, 128, 128, 128, 0, good, good, S) == fg.ERR_ALIGNMENT
+    assert lib.fp8_quant_mx_tiled(None, 0, 128, 128, 1, None, None, S) == fg.OK
+    # MXFP8 GEMMs: the row-major scale codes need 4-byte alignment, the tiles 16
+    assert lib.fp8_mx_gemm(100, 128, 128, good, 0, good, good, 0, good, good, 0, 128, S) == fg.ERR_SHAPE
+    assert lib.fp8_mx_gemm(128, 128, 128, good, 0, P(4098), good, 0, good, good, 0, 128, S) == fg.ERR_ALIGNMENT
+    assert lib.fp8_mx_gemm_tiled(128, 128, 100, good, 0, good, good, 0, good, good, 0, 128, S) == fg.ERR_SHAPE
+    assert lib.fp8_mx_gemm_tiled(128, 128, 128, good, 0, P(4100), good, 0, good, good, 0, 128, S) == \
+        fg.ERR_ALIGNMENT
+    assert lib.fp8_mx_gemm_tiled(128, 128, 128, good, 0, good, good, 0, P(4104), good, 0, 128, S) == \
+        fg.ERR_ALIGNMENT
+    assert lib.fp8_mx_gemm_tiled(128, 128, 128, good, 2, good, good, 0, good, good, 0, 128, S) == \
+        fg.ERR_INVALID_ARG
+    assert lib.fp8_mx_gemm_tiled(0, 128, 128, None, 0, None, None, 0, None, good, 0, 128, S) == fg.OK
     assert lib.fp8_selftest_wait_timeout(0, S) == fg.ERR_INVALID_ARG
     assert lib.fp8_device_status(S, None) == fg.ERR_INVALID_ARG
 

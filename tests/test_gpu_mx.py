@@ -74,6 +74,38 @@ def test_mx_quant_exponent_edges(fmt):
     assert np.array_equal(e8, re8) and np.array_equal(q, rq)
 
 
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+@pytest.mark.parametrize("shape,ldx", [((256, 1024), None), ((128, 128), None), ((384, 512), 640)])
+def test_mx_quant_tiled_bit_exact(fmt, shape, ldx):
+    """quant_mx_tiled: the same codes as the oracle, the scale codes at the
+    positions of the oracle's GEMM-ready tiling (mx_tile_scales)."""
+    R, C = shape
+    xb = synth.bf16_normal(shape, 44, 1.0, 1e-3, 50.0)
+    if ldx is None:
+        x = dev_bf16(xb)
+    else:
+        full = np.zeros((R, ldx), np.uint16)
+        full[:, :C] = xb
+        x = dev_bf16(full)[:, :C]
+    q = torch.full((R, C), 0x55, dtype=torch.uint8, device="cuda")
+    e8t = torch.full((R * C // 32,), 0x55, dtype=torch.uint8, device="cuda")
+    fg.quant_mx_tiled(x, fmt, q, e8t)
+    assert_status_ok()
+    rq, re8, st = mx.quant_mx(xb, fmt)
+    assert st == oracle.OK
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(e8t.cpu().numpy(), mx.mx_tile_scales(re8))
+
+
+def test_mx_quant_tiled_needs_whole_tiles():
+    x = torch.zeros((100, 128), dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((100, 128), dtype=torch.uint8, device="cuda")
+    e8t = torch.empty(400, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fg.Fp8Error) as e:
+        fg.quant_mx_tiled(x, fg.E4M3, q, e8t)
+    assert e.value.code == fg.ERR_SHAPE
+
+
 def test_mx_quant_nonfinite_is_reported_and_empty_is_a_no_op():
     xb = synth.bf16_normal((4, 64), 42)
     xb[1, 33] = 0x7FC0
@@ -136,6 +168,61 @@ def test_mx_gemm_full_compare(case):
     assert torch.equal(d16, d32.to(torch.bfloat16))
 
 
+@pytest.mark.parametrize("case", MX_CASES, ids=[c[0] for c in MX_CASES])
+def test_mx_gemm_tiled_bit_identical_to_row_major(case):
+    """mx_gemm_tiled on the oracle's tiling of the scale codes: bit for bit the
+    output of mx_gemm (whose scale words are reordered by a warp of the GEMM
+    instead of fetched in tile order), FP32 and BF16, and within the oracle's
+    tolerance."""
+    from gpu_helpers import dev_u8, gemm_tolerance_check, guarded
+    name, M, N, K, fa, fb = case
+    qa, ea = mx_operand(M, K, 51, fa)
+    qb, eb = mx_operand(N, K, 52, fb, std=0.5)
+    ref = mx.mx_gemm_full(qa, ea, fa, qb, eb, fb)
+    for dt in (torch.float32, torch.bfloat16):
+        d_rm = run_mx_gemm(qa, ea, fa, qb, eb, fb, dt)
+        D = guarded((M, N), dt)
+        fg.mx_gemm_tiled(dev_u8(qa), fa, dev_u8(mx.mx_tile_scales(ea)), dev_u8(qb), fb,
+                         dev_u8(mx.mx_tile_scales(eb)), D)
+        assert_status_ok()
+        assert torch.equal(D, d_rm)
+    gemm_tolerance_check(D.float().cpu().numpy().astype(np.float64), ref, bf16_out=True)
+
+
+def test_mx_gemm_tiled_needs_16_byte_aligned_tiles():
+    from gpu_helpers import dev_u8
+    M, N, K = 128, 128, 128
+    qa, ea = mx_operand(M, K, 53, oracle.E4M3)
+    buf = torch.zeros(M * K // 32 + 16, dtype=torch.uint8, device="cuda")
+    off = buf[4:4 + M * K // 32]
+    D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    with pytest.raises(fg.Fp8Error) as e:
+        fg.mx_gemm_tiled(dev_u8(qa), fg.E4M3, off, dev_u8(qa), fg.E4M3, dev_u8(mx.mx_tile_scales(ea)), D)
+    assert e.value.code == fg.ERR_ALIGNMENT
+
+
+def test_mx_gemm_exponents_at_4_byte_offsets():
+    """K a multiple of 512 with the exponent arrays 4-byte but not 16-byte
+    aligned (views at a 4-byte offset): the kernel reads the words one chunk at
+    a time instead of four at once, with the same result as aligned arrays."""
+    from gpu_helpers import dev_u8
+    M, N, K = 256, 512, 1024
+    qa, ea = mx_operand(M, K, 61, oracle.E4M3)
+    qb, eb = mx_operand(N, K, 62, oracle.E4M3, std=0.5)
+    aligned = run_mx_gemm(qa, ea, oracle.E4M3, qb, eb, oracle.E4M3, torch.float32)
+
+    def offset_view(e):
+        buf = torch.zeros(e.size + 16, dtype=torch.uint8, device="cuda")
+        v = buf[4:4 + e.size].view(e.shape)
+        v.copy_(dev_u8(e))
+        assert v.data_ptr() % 16 == 4
+        return v
+    D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    fg.mx_gemm(dev_u8(qa), fg.E4M3, offset_view(ea), dev_u8(qb), fg.E4M3, offset_view(eb), D)
+    assert_status_ok()
+    assert torch.equal(D, aligned)
+
+
 def test_mx_gemm_block_scales_are_applied_per_32_block():
     """Operands whose 32-blocks carry very different exponents (2^-20 .. 2^20
     within one row): a scale applied per 128-chunk or per row instead of per
@@ -154,28 +241,42 @@ def test_mx_gemm_block_scales_are_applied_per_32_block():
 
 def test_mx_gemm_headline_shape_sampled():
     """The block-scaled GEMM's headline shape, 8192 x 28672 x 4096: X and W_gu
-    of the MLP step quantized to MXFP8 on the GPU (the quantizer is pinned
-    bit-exactly above), then the GEMM against the oracle's exact per-block
-    sum from the GPU's own codes and exponents on >= 2^20 stratified outputs
-    (every 128 x 128 tile hit >= 16 times)."""
-    from gpu_helpers import bf16_to_f64, gemm_tolerance_check, host_u16, sample_points_dense
+    of the MLP step quantized to MXFP8 by the oracle; the GPU quantizer gives
+    the same codes in both scale layouts; the GEMM from the row-major and from
+    the tiled scales gives one bit-identical D, checked against the oracle's
+    exact per-block sum on >= 2^20 stratified outputs (every 128 x 128 tile
+    hit >= 16 times)."""
+    from gpu_helpers import bf16_to_f64, dev_u8, gemm_tolerance_check, host_u16, sample_points_dense
     M, N, K = 8192, 28672, 4096
     xb = synth.bf16_normal((M, K), 0, 1.0, 1e-3, 50.0)
     wb = synth.bf16_normal((N, K), 1000, 0.02)
     ops = []
     for bits in (xb, wb):
         R = bits.shape[0]
+        rq, re8, st = mx.quant_mx(bits, oracle.E4M3)
+        assert st == oracle.OK
+        x = dev_bf16(bits)
         q = torch.empty((R, K), dtype=torch.uint8, device="cuda")
         e8 = torch.empty((R, K // 32), dtype=torch.uint8, device="cuda")
-        fg.quant_mx(dev_bf16(bits), fg.E4M3, q, e8)
-        ops.append((q, e8))
-    assert_status_ok()
-    (qa, ea), (qb, eb) = ops
+        e8t = torch.empty(R * K // 32, dtype=torch.uint8, device="cuda")
+        fg.quant_mx(x, fg.E4M3, q, e8)
+        assert_status_ok()
+        assert np.array_equal(q.cpu().numpy(), rq) and np.array_equal(e8.cpu().numpy(), re8)
+        fg.quant_mx_tiled(x, fg.E4M3, q, e8t)
+        assert_status_ok()
+        assert np.array_equal(q.cpu().numpy(), rq) and np.array_equal(e8t.cpu().numpy(), mx.mx_tile_scales(re8))
+        del x
+        ops.append((rq, re8, dev_u8(rq), dev_u8(re8), e8t))
+    (rqa, rea, qa, ea, eat), (rqb, reb, qb, eb, ebt) = ops
     D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     fg.mx_gemm(qa, fg.E4M3, ea, qb, fg.E4M3, eb, D)
     assert_status_ok()
+    Dt = torch.empty_like(D)
+    fg.mx_gemm_tiled(qa, fg.E4M3, eat, qb, fg.E4M3, ebt, Dt)
+    assert_status_ok()
+    assert torch.equal(D, Dt)
+    del Dt
     pm, pn = sample_points_dense(M, N, seed=9)
-    ref = mx.mx_gemm_points(qa.cpu().numpy(), ea.cpu().numpy(), oracle.E4M3, qb.cpu().numpy(), eb.cpu().numpy(),
-                            oracle.E4M3, pm, pn)
+    ref = mx.mx_gemm_points(rqa, rea, oracle.E4M3, rqb, reb, oracle.E4M3, pm, pn)
     got = D[torch.from_numpy(pm).cuda(), torch.from_numpy(pn).cuda()]
     gemm_tolerance_check(bf16_to_f64(host_u16(got)), ref, bf16_out=True)

@@ -183,3 +183,31 @@ def test_gemm_reduces_to_the_block_scaled_gemm_when_scales_agree():
     sb = np.ldexp(1.0, cb - 127).T.astype(np.float32).copy()     # S[K/128][N]
     ref = oracle.gemm_full(qa, oracle.E4M3, sa, oracle.GRAN_1x128, qb, oracle.E4M3, sb, oracle.GRAN_1x128)
     assert np.allclose(got, ref, rtol=1e-13, atol=1e-13 * np.abs(ref).max())
+
+
+def test_tile_scales_structure_and_inverse():
+    """The GEMM-ready scale layout (mx_tile_scales): every 512-byte tile holds
+    the codes of exactly one rectangle of 128 rows x 4 blocks, the tiles of one
+    group of four blocks next to each other in row order; inside a tile the
+    16-byte row j holds the four-block words of rows j, j + 32, j + 64, j + 96
+    in that order (what a 32-row copy to all four lane quarters of the tensor
+    memory needs); mx_untile_scales inverts it."""
+    R, KB = 256, 12
+    rr, kk = np.meshgrid(np.arange(R), np.arange(KB), indexing="ij")
+    tr = mx.mx_tile_scales(rr.astype(np.uint8)).astype(int).reshape(KB // 4, R // 128, 32, 4, 4)
+    tk = mx.mx_tile_scales(kk.astype(np.uint8)).astype(int).reshape(KB // 4, R // 128, 32, 4, 4)
+    j = np.arange(32)[:, None, None]
+    q = np.arange(4)[None, :, None]
+    b = np.arange(4)[None, None, :]
+    for kc in range(KB // 4):
+        for rb in range(R // 128):
+            assert set(tr[kc, rb].ravel()) == set(range(128 * rb, 128 * rb + 128))
+            assert set(tk[kc, rb].ravel()) == set(range(4 * kc, 4 * kc + 4))
+            assert np.array_equal(tr[kc, rb], np.broadcast_to(128 * rb + 32 * q + j, (32, 4, 4)))
+            assert np.array_equal(tk[kc, rb], np.broadcast_to(4 * kc + b, (32, 4, 4)))
+    e = np.random.default_rng(3).integers(0, 255, (384, 8), dtype=np.uint8)
+    t = mx.mx_tile_scales(e)
+    assert t.size == e.size and np.array_equal(np.sort(t), np.sort(e.ravel()))
+    assert np.array_equal(mx.mx_untile_scales(t, 384, 8), e)
+    with pytest.raises(ValueError):
+        mx.mx_tile_scales(np.zeros((100, 8), np.uint8))
