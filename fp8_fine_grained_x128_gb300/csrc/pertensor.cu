@@ -834,23 +834,27 @@ __device__ __forceinline__ void l2_priority_normal(const void *p)
         asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(p) : "memory");
 }
 
-// Amax of the contiguous vectors [0, nvec) of x, grid-strided, U loads in flight.
+// Contiguous x: every CTA takes kCurVecs consecutive 16-byte vectors, all of
+// a thread's loads in flight at once (no serial remainder), and the grid
+// covers the tensor in as many waves as it needs.
+constexpr int kCurU = 8;
+constexpr int64_t kCurVecs = 256 * kCurU;
+
 template <bool KEEP>
-__device__ __forceinline__ uint32_t amax_flat(const uint16_t *__restrict__ x, int64_t nvec, int64_t stride)
+__device__ __forceinline__ uint32_t amax_cta(const uint16_t *__restrict__ x, int64_t nvec)
 {
-    constexpr int U = 8;
     const uint64_t pol = KEEP ? l2_policy_evict_last() : 0;
-    auto load = [&](int64_t i) { return KEEP ? ldg_stream_policy(x + i * 8, pol) : ldg_stream(x + i * 8); };
-    uint32_t m = 0;
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + (U - 1) * stride < nvec; i += U * stride) {
-        uint4 v[U];
+    const int64_t base = (int64_t)blockIdx.x * kCurVecs + threadIdx.x;
+    uint4 v[kCurU];
 #pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = load(i + u * stride);
-#pragma unroll
-        for (int u = 0; u < U; ++u) m = max(m, absmax8(v[u]));
+    for (int u = 0; u < kCurU; ++u) {
+        const int64_t i = base + u * 256;
+        v[u] = make_uint4(0, 0, 0, 0);
+        if (i < nvec) v[u] = KEEP ? ldg_stream_policy(x + i * 8, pol) : ldg_stream(x + i * 8);
     }
-    for (; i < nvec; i += stride) m = max(m, absmax8(load(i)));
+    uint32_t m = 0;
+#pragma unroll
+    for (int u = 0; u < kCurU; ++u) m = max(m, absmax8(v[u]));
     return m;
 }
 
@@ -865,9 +869,9 @@ __global__ void __launch_bounds__(256) k_amax_scale(const uint16_t *__restrict__
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     uint32_t m = 0;
     if (keep_in_l2(x, cols, ldx)) {
-        m = amax_flat<true>(x, nvec, stride);
+        m = amax_cta<true>(x, nvec);
     } else if (ldx == cols) {
-        m = amax_flat<false>(x, nvec, stride);
+        m = amax_cta<false>(x, nvec);
     } else {
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
             const int64_t r = i / vpr, c = (i - r * vpr) * 8;
@@ -899,29 +903,27 @@ __global__ void __launch_bounds__(256) k_quant_scale(const uint16_t *__restrict_
     const Divider2 d(*scale);
     const int64_t vpr = cols / 8, nvec = rows * vpr;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    if (ldx == cols) {   // contiguous: flat 16-byte vectors, four loads in flight
+    if (ldx == cols) {   // contiguous: kCurVecs vectors per CTA, as in pass 1
         const bool keep = keep_in_l2(x, cols, ldx);
-        constexpr int U = 4;
-        int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-        for (; i + (U - 1) * stride < nvec; i += U * stride) {
-            uint4 v[U];
+        const int64_t base = (int64_t)blockIdx.x * kCurVecs + threadIdx.x;
+        uint4 v[kCurU];
 #pragma unroll
-            for (int u = 0; u < U; ++u) v[u] = ldg_stream(x + (i + u * stride) * 8);
-            if (keep) {
-#pragma unroll
-                for (int u = 0; u < U; ++u) l2_priority_normal(x + (i + u * stride) * 8);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const uint2 c = quant8p<FMT>(v[u], d);
-                if (dbg_span((i + u * stride) * 8, 8, nvec * 8, status))
-                    *reinterpret_cast<uint2 *>(q + (i + u * stride) * 8) = c;
-            }
+        for (int u = 0; u < kCurU; ++u) {
+            const int64_t i = base + u * 256;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (i < nvec) v[u] = ldg_stream(x + i * 8);
         }
-        for (; i < nvec; i += stride) {
-            const uint2 c = quant8p<FMT>(ldg_stream(x + i * 8), d);
+        if (keep) {
+#pragma unroll
+            for (int u = 0; u < kCurU; ++u)
+                if (base + u * 256 < nvec) l2_priority_normal(x + (base + u * 256) * 8);
+        }
+#pragma unroll
+        for (int u = 0; u < kCurU; ++u) {
+            const int64_t i = base + u * 256;
+            if (i >= nvec) break;
+            const uint2 c = quant8p<FMT>(v[u], d);
             if (dbg_span(i * 8, 8, nvec * 8, status)) *reinterpret_cast<uint2 *>(q + i * 8) = c;
-            if (keep) l2_priority_normal(x + i * 8);
         }
     } else {
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
@@ -1053,8 +1055,15 @@ int launch_pertensor_current(const void *x, int64_t rows, int64_t cols, int64_t 
                              void *ws, int *status, cudaStream_t st)
 {
     const int64_t nvec = rows * (cols / 8);
-    const unsigned ba = (unsigned)std::max<int64_t>(1, std::min<int64_t>((nvec + 255) / 256, (int64_t)sm_count() * 4));
-    const unsigned bq = (unsigned)std::max<int64_t>(1, std::min<int64_t>((nvec + 255) / 256, (int64_t)sm_count() * 8));
+    // contiguous x: one CTA per kCurVecs vectors; strided x: a grid-strided loop
+    const bool flat = ldx == cols;
+    const int64_t flat_grid = std::max<int64_t>(1, (nvec + kCurVecs - 1) / kCurVecs);
+    const unsigned ba = (unsigned)(flat ? flat_grid
+                                        : std::max<int64_t>(1, std::min<int64_t>((nvec + 255) / 256,
+                                                                                 (int64_t)sm_count() * 4)));
+    const unsigned bq = (unsigned)(flat ? flat_grid
+                                        : std::max<int64_t>(1, std::min<int64_t>((nvec + 255) / 256,
+                                                                                 (int64_t)sm_count() * 8)));
     auto X = static_cast<const uint16_t *>(x);
     auto W = static_cast<PtWorkspace *>(ws);
     auto Q = static_cast<uint8_t *>(q);
