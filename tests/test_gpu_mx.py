@@ -149,6 +149,8 @@ MX_CASES = [
     ("bn128_tail", 384, 384, 640, oracle.E4M3, oracle.E4M3),
     ("waves", 1024, 1536, 1024, oracle.E4M3, oracle.E4M3),
     ("e5m2_a", 256, 256, 384, oracle.E5M2, oracle.E4M3),
+    ("one_chunk", 128, 256, 128, oracle.E4M3, oracle.E5M2),      # K = 128: a one-chunk group
+    ("smallest", 128, 128, 128, oracle.E5M2, oracle.E5M2),       # one tile, BN = 128
 ]
 
 
@@ -187,6 +189,28 @@ def test_mx_gemm_tiled_bit_identical_to_row_major(case):
         assert_status_ok()
         assert torch.equal(D, d_rm)
     gemm_tolerance_check(D.float().cpu().numpy().astype(np.float64), ref, bf16_out=True)
+
+
+def test_mx_gemm_tiled_empty_shapes():
+    """K == 0 writes zeros (FP32 and BF16, ldD > N leaves the padding alone);
+    M == 0 or N == 0 is a no-op."""
+    from gpu_helpers import CANARY_BYTE, guarded
+    for dt in (torch.float32, torch.bfloat16):
+        full = guarded((256, 384 + 64), dt)
+        D = full[:, :384]
+        z = torch.empty((256, 0), dtype=torch.uint8, device="cuda")
+        fg.mx_gemm_tiled(z, fg.E4M3, torch.empty(0, dtype=torch.uint8, device="cuda"),
+                         torch.empty((384, 0), dtype=torch.uint8, device="cuda"), fg.E4M3,
+                         torch.empty(0, dtype=torch.uint8, device="cuda"), D)
+        assert_status_ok()
+        assert bool((D == 0).all())
+        assert bool((full[:, 384:].contiguous().view(torch.uint8) == CANARY_BYTE).all())
+    D0 = torch.empty((0, 128), dtype=torch.float32, device="cuda")
+    fg.mx_gemm_tiled(torch.empty((0, 128), dtype=torch.uint8, device="cuda"), fg.E4M3,
+                     torch.empty(0, dtype=torch.uint8, device="cuda"),
+                     torch.empty((128, 128), dtype=torch.uint8, device="cuda"), fg.E4M3,
+                     torch.zeros(512, dtype=torch.uint8, device="cuda"), D0)
+    assert_status_ok()
 
 
 def test_mx_gemm_tiled_needs_16_byte_aligned_tiles():
