@@ -40,6 +40,12 @@
 //               straight from registers.  The two accumulators alternate per
 //               chunk, so the tensor cores fill one while the epilogue drains
 //               the other.
+// MXFP8 mode: warp 1 first copies each stage's scale words from shared into
+// tensor memory (tcgen05.cp) and issues kind::mxf8f6f4.block_scale MMAs;
+// the scale words reach shared memory by two bulk copies per stage from the
+// producer (tiled codes) or from warp 2, which reorders row-major codes; one
+// accumulator per tile, which the epilogue drains at once and hands back
+// before it stores the tile.
 // Every mbarrier wait is bounded (about 1 s): on a timeout the CTA records
 // FP8_ERR_TIMEOUT, tells the other roles through a shared flag, waits for
 // its own copies and MMAs in flight (bounded again), frees the tensor memory
