@@ -248,24 +248,45 @@ __global__ void __launch_bounds__(kFillThreads) k_moe_fill(const int32_t *__rest
 // ---------------------------------------------------------------- gather
 
 // One warp per dispatched row: K FP8 bytes and K/128 scales of its token.
+// Each lane has its 16-byte vectors of a row (four per 2048 bytes) and its
+// scale in flight at once before any is stored (35.6 against 36.9 us for
+// one load and store at a time on 73728 rows x 2048; the bulk-copy engine
+// through per-lane shared buffers measured 37.0 us, and loads without L1
+// allocation with streaming stores 42.8 us).
 __global__ void __launch_bounds__(256) k_moe_gather(const uint8_t *__restrict__ q, const float *__restrict__ s,
                                                     int64_t T, int64_t K, const int32_t *__restrict__ row_token,
                                                     const int32_t *__restrict__ offsets, int E, int64_t Mcap,
                                                     uint8_t *__restrict__ qg, float *__restrict__ sg, int *status)
 {
+    constexpr int U = 4;
     const int lane = threadIdx.x & 31;
     const int64_t total = min((int64_t)offsets[E], Mcap);
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t nv = K / 16, nkb = K / 128;
     for (int64_t r = w0; r < total; r += nw) {
         const int64_t t = row_token[r];
         if (t < 0 || t >= T) continue;
         const uint4 *src = reinterpret_cast<const uint4 *>(q + t * K);
         uint4 *dst = reinterpret_cast<uint4 *>(qg + r * K);
-        for (int64_t i = lane; i < K / 16; i += 32)
-            if (dbg_cell(r, i * 16, 16, Mcap, K, status)) dst[i] = src[i];
-        for (int64_t kb = lane; kb < K / 128; kb += 32)
-            if (dbg_cell(kb, r, 1, K / 128, Mcap, status)) sg[kb * Mcap + r] = s[kb * T + t];
+        for (int64_t i0 = 0; i0 < nv; i0 += 32 * U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + 32 * u + lane;
+                if (i < nv) v[u] = src[i];
+            }
+            float sc = 0.0f;
+            const int64_t kb = i0 / 8 + lane;   // this round's scales: 32 U vectors = 4 U chunks of 128
+            const bool has_sc = lane < 4 * U && kb < nkb;
+            if (has_sc) sc = s[kb * T + t];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + 32 * u + lane;
+                if (i < nv && dbg_cell(r, i * 16, 16, Mcap, K, status)) dst[i] = v[u];
+            }
+            if (has_sc && dbg_cell(kb, r, 1, nkb, Mcap, status)) sg[kb * Mcap + r] = sc;
+        }
     }
 }
 
