@@ -97,6 +97,19 @@ def test_mx_quant_tiled_bit_exact(fmt, shape, ldx):
     assert np.array_equal(e8t.cpu().numpy(), mx.mx_tile_scales(re8))
 
 
+def test_mx_quant_tiled_nonfinite_is_reported_and_empty_is_a_no_op():
+    xb = synth.bf16_normal((128, 256), 45)
+    xb[77, 200] = 0xFF80                           # -Inf
+    q = torch.empty((128, 256), dtype=torch.uint8, device="cuda")
+    e8t = torch.empty(128 * 256 // 32, dtype=torch.uint8, device="cuda")
+    fg.quant_mx_tiled(dev_bf16(xb), fg.E4M3, q, e8t)
+    assert fg.device_status() == fg.ERR_NONFINITE
+    fg.quant_mx_tiled(torch.empty((0, 128), dtype=torch.bfloat16, device="cuda"), fg.E4M3,
+                      torch.empty((0, 128), dtype=torch.uint8, device="cuda"),
+                      torch.empty(0, dtype=torch.uint8, device="cuda"))
+    assert_status_ok()
+
+
 def test_mx_quant_tiled_needs_whole_tiles():
     x = torch.zeros((100, 128), dtype=torch.bfloat16, device="cuda")
     q = torch.empty((100, 128), dtype=torch.uint8, device="cuda")
