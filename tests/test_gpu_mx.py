@@ -276,6 +276,44 @@ def test_mx_gemm_block_scales_are_applied_per_32_block():
     gemm_tolerance_check(d32.cpu().numpy().astype(np.float64), ref, bf16_out=False)
 
 
+@pytest.mark.parametrize("layout", ["row_major", "tiled"])
+@pytest.mark.parametrize("case", ["complementary", "tiny"])
+def test_mx_gemm_extreme_scale_codes(layout, case):
+    """Scale codes at the ends of the UE8M0 range, on positive codes (no
+    cancellation, so a relative bound of 1e-5 holds for FP32 accumulation
+    and shows any scale applied wrongly).  complementary: per 32-block eA in
+    {0, 1, 2, 252, 253, 254} and eB = 254 - eA, so X_A alone is 2^-127 or
+    2^127 while every scale product is 1 (a product formed after applying the
+    two factors one at a time in binary32 would overflow or flush).  tiny: eA
+    in {0, ..., 4} with eB = 127, so single products fall into binary32's
+    subnormal range (a flush to zero would show)."""
+    from gpu_helpers import dev_u8, gemm_tolerance_check
+    rng = np.random.default_rng(17)
+    M, N, K = 256, 256, 512
+    qa = rng.integers(0x08, 0x7E, (M, K), dtype=np.uint8)
+    qb = rng.integers(0x08, 0x7E, (N, K), dtype=np.uint8)
+    if case == "complementary":
+        codes = np.array([0, 1, 2, 252, 253, 254], np.uint8)
+        ea = np.broadcast_to(codes[rng.integers(0, codes.size, (1, K // 32))], (M, K // 32)).copy()
+        eb = np.broadcast_to((254 - ea[:1].astype(np.int64)).astype(np.uint8), (N, K // 32)).copy()
+    else:
+        ea = rng.integers(0, 5, (M, K // 32)).astype(np.uint8)
+        eb = np.full((N, K // 32), 127, np.uint8)
+    ref = mx.mx_gemm_full(qa, ea, oracle.E4M3, qb, eb, oracle.E4M3)
+    assert np.all(np.isfinite(ref)) and np.all(ref > 0)
+    D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    if layout == "tiled":
+        fg.mx_gemm_tiled(dev_u8(qa), fg.E4M3, dev_u8(mx.mx_tile_scales(ea)), dev_u8(qb), fg.E4M3,
+                         dev_u8(mx.mx_tile_scales(eb)), D)
+    else:
+        fg.mx_gemm(dev_u8(qa), fg.E4M3, dev_u8(ea), dev_u8(qb), fg.E4M3, dev_u8(eb), D)
+    assert_status_ok()
+    got = D.cpu().numpy().astype(np.float64)
+    rel = np.abs(got - ref) / ref
+    assert float(rel.max()) <= 1e-5, float(rel.max())
+    gemm_tolerance_check(got, ref, bf16_out=False)
+
+
 def test_mx_gemm_headline_shape_sampled():
     """The block-scaled GEMM's headline shape, 8192 x 28672 x 4096: X and W_gu
     of the MLP step quantized to MXFP8 by the oracle; the GPU quantizer gives
