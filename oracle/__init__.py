@@ -61,54 +61,68 @@ def _P(t):
     return ctypes.POINTER(t)
 
 
+def _load(path: str):
+    """The oracle library at `path`, with every entry point's signature set."""
+    L = ctypes.CDLL(path)
+    i64, i32, f32, f64, u8, u16 = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                                   ctypes.c_double, ctypes.c_uint8, ctypes.c_uint16)
+    vp = ctypes.c_void_p
+    sig = {
+        "orc_version": (ctypes.c_int, []),
+        "orc_bf16_to_f32": (f32, [u16]),
+        "orc_fmax": (f32, [ctypes.c_int]),
+        "orc_fp8_decode": (f64, [u8, ctypes.c_int]),
+        "orc_fp8_encode": (u8, [f32, ctypes.c_int]),
+        "orc_fp8_encode_array": (None, [vp, i64, ctypes.c_int, vp]),
+        "orc_fp8_encode_bits_range": (None, [ctypes.c_uint32, i64, ctypes.c_int, vp]),
+        "orc_f64_to_bf16": (u16, [f64]),
+        "orc_quant_1x128": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp]),
+        "orc_quant_128x1_transposed": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp]),
+        "orc_quant_128x128": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp]),
+        "orc_fp8_transpose": (None, [vp, i64, i64, vp]),
+        "orc_f32_transpose": (None, [vp, i64, i64, vp]),
+        "orc_quant_stats": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, ctypes.c_int,
+                                           ctypes.c_int, vp]),
+        "orc_delayed_step": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp]),
+        "orc_gemm_points": (ctypes.c_int, [i64, i64, i64, vp, i64, ctypes.c_int, vp,
+                                           ctypes.c_int, i64, vp, i64, ctypes.c_int, vp,
+                                           ctypes.c_int, i64, i64, vp, vp, vp]),
+        "orc_grouped_gemm_points": (ctypes.c_int, [ctypes.c_int, vp, i64, i64, vp, vp, i64,
+                                                   vp, vp, i64, vp, vp, vp]),
+        "orc_grouped_wgrad_points": (ctypes.c_int, [ctypes.c_int, vp, i64, i64, i64, vp, ctypes.c_int,
+                                                    vp, vp, ctypes.c_int, vp, i64, vp, vp, vp, vp]),
+        "orc_quant_pertensor_current": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp]),
+        "orc_wgrad_recompute_error": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, i64, vp]),
+        "orc_adam_fp8_step": (ctypes.c_int, [i64, vp, vp, vp, vp, vp, vp] + [ctypes.c_float] * 9),
+        "orc_moe_route": (ctypes.c_int, [i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
+                                         vp, vp, vp, vp, vp, i64, vp, vp, vp, vp]),
+        "orc_moe_gather": (None, [vp, vp, i64, i64, vp, i64, i64, vp, vp]),
+        "orc_swiglu_fwd": (None, [vp, i64, i64, vp]),
+        "orc_swiglu_bwd": (None, [vp, vp, i64, i64, vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib():
     global _lib
     with _lock:
         if _lib is None:
-            L = ctypes.CDLL(build())
-            i64, i32, f32, f64, u8, u16 = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
-                                           ctypes.c_double, ctypes.c_uint8, ctypes.c_uint16)
-            vp = ctypes.c_void_p
-            sig = {
-                "orc_version": (ctypes.c_int, []),
-                "orc_bf16_to_f32": (f32, [u16]),
-                "orc_fmax": (f32, [ctypes.c_int]),
-                "orc_fp8_decode": (f64, [u8, ctypes.c_int]),
-                "orc_fp8_encode": (u8, [f32, ctypes.c_int]),
-                "orc_fp8_encode_array": (None, [vp, i64, ctypes.c_int, vp]),
-                "orc_fp8_encode_bits_range": (None, [ctypes.c_uint32, i64, ctypes.c_int, vp]),
-                "orc_f64_to_bf16": (u16, [f64]),
-                "orc_quant_1x128": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp]),
-                "orc_quant_128x1_transposed": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp]),
-                "orc_quant_128x128": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp]),
-                "orc_fp8_transpose": (None, [vp, i64, i64, vp]),
-                "orc_f32_transpose": (None, [vp, i64, i64, vp]),
-                "orc_quant_stats": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, ctypes.c_int,
-                                                   ctypes.c_int, vp]),
-                "orc_delayed_step": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int,
-                                                    ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp]),
-                "orc_gemm_points": (ctypes.c_int, [i64, i64, i64, vp, i64, ctypes.c_int, vp,
-                                                   ctypes.c_int, i64, vp, i64, ctypes.c_int, vp,
-                                                   ctypes.c_int, i64, i64, vp, vp, vp]),
-                "orc_grouped_gemm_points": (ctypes.c_int, [ctypes.c_int, vp, i64, i64, vp, vp, i64,
-                                                           vp, vp, i64, vp, vp, vp]),
-                "orc_grouped_wgrad_points": (ctypes.c_int, [ctypes.c_int, vp, i64, i64, i64, vp, ctypes.c_int,
-                                                            vp, vp, ctypes.c_int, vp, i64, vp, vp, vp, vp]),
-                "orc_quant_pertensor_current": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp]),
-                "orc_wgrad_recompute_error": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, i64, vp]),
-                "orc_adam_fp8_step": (ctypes.c_int, [i64, vp, vp, vp, vp, vp, vp] + [ctypes.c_float] * 9),
-                "orc_moe_route": (ctypes.c_int, [i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
-                                                 vp, vp, vp, vp, vp, i64, vp, vp, vp, vp]),
-                "orc_moe_gather": (None, [vp, vp, i64, i64, vp, i64, i64, vp, vp]),
-                "orc_swiglu_fwd": (None, [vp, i64, i64, vp]),
-                "orc_swiglu_bwd": (None, [vp, vp, i64, i64, vp]),
-            }
-            for name, (res, args) in sig.items():
-                fn = getattr(L, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = L
+            _lib = _load(build())
     return _lib
+
+
+def use_library(path: str) -> None:
+    """Tests only: route every wrapper below through the oracle library built
+    at `path` -- a modified copy of fp8fg_oracle.c with a planted mistake,
+    which the pins in tests/ must catch."""
+    global _lib
+    with _lock:
+        _lib = _load(path)
 
 
 def _ptr(a: np.ndarray):

@@ -41,6 +41,8 @@ def test_hand_delayed_sequence():
         # the quantization used exactly the scale in force before the step
         xv = synth.bf16_bits_to_f32(x)
         assert np.array_equal(q, oracle.fp8_encode(xv / np.float32(s_used), oracle.E4M3))
+        # the history window after the step, slot by slot
+        assert st.hist.tolist() == g["expected_history_after_each_step"][t]
     ev = lambda e: float(np.float32(Fraction(e)) if "/" not in e else
                          np.float32(np.float32(float(e.split('/')[0])) / np.float32(448.0)))
     assert used == [ev(e) for e in g["expected_scale_used_per_step"]]

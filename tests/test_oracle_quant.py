@@ -189,6 +189,60 @@ def test_subnormal_scale_kept():
     assert q[0, 0] == 0x7E
 
 
+# ------------------------------------------- the scale and the quotient, exactly
+#
+# R2 and R3 fix s = fp32(amax / fmax) and q = enc(fp32(x / s)): two IEEE
+# binary32 divisions.  The references below take each quotient of two binary32
+# numbers in binary64 and round it once to binary32.  That is the correctly
+# rounded binary32 quotient: the binary64 result carries 53 >= 2 * 24 + 2 bits,
+# so the second rounding cannot move it (S. A. Figueroa, "When is double
+# rounding innocuous?", SIGNUM Newsletter 30(3), 1995).  The FP8 step is torch's
+# float8 cast, itself pinned against the oracle's encoder in
+# test_oracle_formats.py.  Multiplying by a rounded reciprocal instead of
+# dividing changes the scale of some BF16 amax values and, for about a fifth of
+# the amax values below, the code of some x.
+
+_FMAX = {oracle.E4M3: 448.0, oracle.E5M2: 57344.0}
+_POS_BF16 = np.arange(1, 0x7F80, dtype=np.uint32)            # every positive finite BF16
+
+
+def _bf16_values(bits):
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32)
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_scale_of_every_bf16_amax_is_the_rounded_quotient(fmt):
+    x = np.zeros((len(_POS_BF16), 128), np.uint16)
+    x[:, 0] = _POS_BF16
+    x[:, 77] = _POS_BF16 ^ 0x8000           # the same magnitude with the other sign
+    _, s, st = oracle.quant_1x128(x, fmt)
+    assert st == oracle.OK
+    want = (_bf16_values(_POS_BF16).astype(np.float64) / _FMAX[fmt]).astype(np.float32)
+    assert np.array_equal(s[0], want)
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_codes_are_the_cast_of_the_rounded_quotient(fmt):
+    torch = pytest.importorskip("torch")
+    tdt = torch.float8_e4m3fn if fmt == oracle.E4M3 else torch.float8_e5m2
+    vals = _bf16_values(_POS_BF16)
+    rng = np.random.default_rng(29)
+    amax_bits = _POS_BF16[rng.integers(0x0800, len(_POS_BF16), 64)]   # scales in the normal range
+    rows = []
+    for a in amax_bits:
+        xs = _POS_BF16[vals <= _bf16_values(a)]
+        xs = np.where(rng.integers(0, 2, len(xs)) == 1, xs | 0x8000, xs)   # both signs
+        n_t = (len(xs) + 126) // 127
+        body = np.resize(xs, n_t * 127).reshape(n_t, 127)
+        rows.append(np.concatenate([np.full((n_t, 1), a, np.uint32), body], axis=1))
+    x = np.concatenate(rows).astype(np.uint16)
+    q, s, st = oracle.quant_1x128(x, fmt)
+    assert st == oracle.OK
+    quot = (synth.bf16_bits_to_f32(x).astype(np.float64) / s[0].astype(np.float64)[:, None]).astype(np.float32)
+    want = torch.from_numpy(quot).to(tdt).view(torch.uint8).numpy()
+    assert np.array_equal(q, want)
+
+
 # ---------------------------------------------------------------- monitors
 
 def numpy_counts(xg, qg, sg, fm):
