@@ -50,6 +50,20 @@ def test_hand_delayed_sequence():
     assert int(st.step[0]) == 5
 
 
+def test_all_zero_history_keeps_the_scale():
+    """Reading R5's degenerate case: while every amax in the window is 0 the
+    scale in force is kept (here the initial 1), and the first nonzero amax
+    sets it from the window's maximum."""
+    st = oracle.DelayedState(4)
+    zero = np.zeros((128, 256), np.uint16)
+    for t in range(3):
+        q, s_used, _, code = oracle.delayed_step(zero, st, oracle.E4M3)
+        assert code == oracle.OK and s_used == 1.0 and float(st.scale[0]) == 1.0
+        assert not q.any()
+    oracle.delayed_step(tensor_with_amax(8.0, 3), st, oracle.E4M3)
+    assert float(st.scale[0]) == np.float32(np.float32(8.0) / np.float32(448.0))
+
+
 def test_delayed_knobs_margin_and_most_recent():
     st = oracle.DelayedState(4)
     for t, a in enumerate([8.0, 2.0]):

@@ -128,3 +128,17 @@ def test_f64_to_bf16_matches_torch_on_binary32_values_and_single_rounding():
     x = 1.0 + 2.0 ** -8 + 2.0 ** -40
     assert int(oracle.f64_to_bf16([x])[0]) == 0x3F81
     assert int(oracle.f64_to_bf16([1.0 + 2.0 ** -8])[0]) == 0x3F80
+    assert int(oracle.f64_to_bf16([1.0 + 3 * 2.0 ** -8])[0]) == 0x3F82   # tie above an odd mantissa
+
+
+def test_f64_to_bf16_every_exact_tie_matches_torch():
+    """Every value exactly halfway between two neighbouring BF16 numbers (the
+    binary32 pattern of the lower one with 0x8000 in its low half), both
+    signs, subnormal and normal, up to the tie between the largest finite
+    BF16 and infinity: ties go to the even mantissa."""
+    u = np.arange(0, 0x7F80, dtype=np.uint32)
+    ties = ((u << 16) | 0x8000).view(np.float32)
+    ties = np.concatenate([ties, -ties])
+    ours = oracle.f64_to_bf16(ties.astype(np.float64))
+    ref = torch.from_numpy(ties).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)

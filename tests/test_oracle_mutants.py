@@ -46,6 +46,9 @@ MUTANTS = {
                                                "e - f.bias + 1);\n    return sign ? -v : v;")], [FORMATS]),
     "decode_e4m3_nan_code_misplaced": ("c", [("if (fmt == ORC_E4M3 && e == 15 && m == 7) return NAN;",
                                               "if (fmt == ORC_E4M3 && e == 15 && m == 6) return NAN;")], [FORMATS]),
+    "bf16_rounding_ties_toward_zero": ("c", [("else n = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;\n    val = n * quantum;\n    if (val >= ldexp(1.0, 128))",
+                                              "else n = fl;\n    val = n * quantum;\n    if (val >= ldexp(1.0, 128))")],
+                                       [FORMATS]),
     # scale and quotient (R2, R3: s = fp32(amax / fmax), q = enc(fp32(x / s)))
     "scale_by_reciprocal_of_fmax": ("c", [("return amax / fm;", "return amax * (1.0f / fm);")], [QUANT]),
     "scale_of_zero_group_is_zero": ("c", [("if (amax == 0.0f) return 1.0f;", "if (amax == 0.0f) return 0.0f;")],
@@ -78,6 +81,13 @@ MUTANTS = {
                                              [QUANT, MONITOR, GLUE]),
     "saturation_counts_exact_fmax": ("c", [("if (fabsf(quotient) > fm) sat++;", "if (fabsf(quotient) >= fm) sat++;")],
                                      [QUANT, MONITOR, GLUE]),
+    "pertensor_monitor_counts_signed_zeros_twice": ("c", [("px[key_bf16(xb)] = 1;", "px[xb] = 1;")],
+                                                    [GLUE, QUANT, MONITOR]),
+    "128x1_monitor_scale_grid_transposed": ("c", [("case ORC_GRAN_128x1: sc = s[grow * cols + gcol]; break;",
+                                                   "case ORC_GRAN_128x1: sc = s[gcol * (rows / 128) + grow]; break;")],
+                                            [QUANT, MONITOR]),
+    "128x1_monitor_reads_codes_untransposed": ("c", [("uint8_t qc = (gran == ORC_GRAN_128x1) ? q[c * rows + r] : q[r * cols + c];",
+                                                      "uint8_t qc = q[r * cols + c];")], [QUANT, MONITOR]),
     # delayed scaling (R5)
     "history_slot_one_ahead": ("c", [("hist[*step % hist_len] = amax;", "hist[(*step + 1) % hist_len] = amax;")],
                                [GLUE]),
@@ -85,6 +95,8 @@ MUTANTS = {
     "most_recent_ignored": ("c", [("if (algo == ORC_ALGO_MOST_RECENT) {", "if (algo == -1) {")], [GLUE]),
     "nonfinite_step_still_updates_history": ("c", [("    if (bad) return ORC_NONFINITE;\n    /* 2. record",
                                                     "    /* 2. record")], [GLUE]),
+    "scale_updated_from_an_empty_history": ("c", [("if (m > 0.0f) *scale = ldexpf(m, margin)",
+                                                   "*scale = ldexpf(m, margin)")], [GLUE]),
     # GEMM (R7)
     "gemm_drops_b_scale": ("c", [("d += (double)scale_at(sA, granA, ldsA, m, kb) * (double)scale_at(sB, granB, ldsB, n, kb) * p;",
                                   "d += (double)scale_at(sA, granA, ldsA, m, kb) * p;")], [GEMM]),
@@ -92,6 +104,8 @@ MUTANTS = {
                                                   "case ORC_GRAN_128x128: return sv[kb * ld + row / 128];")], [GEMM]),
     "gemm_scales_of_the_next_chunk": ("c", [("d += (double)scale_at(sA, granA, ldsA, m, kb)",
                                              "d += (double)scale_at(sA, granA, ldsA, m, (kb + 1) % (K / 128))")], [GEMM]),
+    "pertensor_gemm_drops_b_scale": ("c", [("return (double)sA[0] * (double)sB[0] * p;", "return (double)sA[0] * p;")],
+                                     [GEMM]),
     "grouped_gemm_expert_bound_inclusive": ("c", [("if (m >= off[e] && m < off[e + 1]) { g = e; break; }",
                                                    "if (m >= off[e] && m <= off[e + 1]) { g = e; break; }")], [GEMM]),
     "grouped_wgrad_scales_from_chunk_zero": ("c", [("sA + (r0 / 128) * N", "sA")], [GEMM]),
@@ -104,6 +118,8 @@ MUTANTS = {
     "adam_second_moment_of_g_not_g_squared": ("c", [("v = b2 * v + omb2 * gg;", "v = b2 * v + omb2 * gi;")], [ADAM]),
     "adam_v_scaled_with_e4m3_max": ("c", [("s_v = av == 0.0f ? 1.0f : av / 57344.0f;",
                                            "s_v = av == 0.0f ? 1.0f : av / 448.0f;")], [ADAM]),
+    "adam_v_encoded_as_e4m3": ("c", [("qv[blk * 128 + i] = orc_fp8_encode(vn[i] / s_v, ORC_E5M2);",
+                                      "qv[blk * 128 + i] = orc_fp8_encode(vn[i] / s_v, ORC_E4M3);")], [ADAM]),
     # routing, gather, SwiGLU (R8, R9)
     "route_ties_to_higher_index": ("c", [("if (best < 0 || z[e] > z[best]) best = e;",
                                           "if (best < 0 || z[e] >= z[best]) best = e;")], [GLUE]),
@@ -121,6 +137,7 @@ MUTANTS = {
                                                      "row_prob[r] = prob[t * E + e];")], [GLUE]),
     "swiglu_forward_drops_gate": ("c", [("h[r * F + j] = orc_f64_to_bf16(g * sig * u);",
                                          "h[r * F + j] = orc_f64_to_bf16(sig * u);")], [GLUE]),
+    "swiglu_up_grad_drops_gate": ("c", [("orc_f64_to_bf16(d * g * sig);", "orc_f64_to_bf16(d * sig);")], [GLUE]),
     # MXFP8 (R13-R16)
     "mx_untile_order_swapped": ("mx", [("t.transpose(1, 3, 2, 0, 4)", "t.transpose(1, 2, 3, 0, 4)")], [MX]),
     "mx_quotient_multiplies_by_the_scale": ("mx", [("quot = xb / np.ldexp(1.0, e)[..., None]",
