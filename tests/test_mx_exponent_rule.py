@@ -30,3 +30,17 @@ def test_bit_rule_equals_the_definition_for_every_bf16_amax(fmt, emax):
     want = mx.mx_scale_exponents(amax, fmt)
     got = np.array([exponent_from_bits(int(a), emax) for a in bits], np.int64)
     assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_definition_at_powers_of_two_and_at_the_clamps(fmt):
+    """The exponent rule itself, from its definition: amax = fmax * 2^j gives
+    e = j exactly, a hair above it gives j + 1, and both ends clamp to the
+    UE8M0 range [-127, 127] (code 254 at the top, 0 at the bottom)."""
+    fm = float(oracle.fmax(fmt))
+    j = np.arange(-140, 141)
+    on = np.ldexp(fm, j)
+    above = on * (1.0 + 2.0 ** -40)
+    assert np.array_equal(mx.mx_scale_exponents(on, fmt), np.clip(j, -127, 127))
+    assert np.array_equal(mx.mx_scale_exponents(above, fmt), np.clip(j + 1, -127, 127))
+    assert int(mx.mx_scale_exponents(np.float64(0.0), fmt)) == 0

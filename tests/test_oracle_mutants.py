@@ -49,6 +49,12 @@ MUTANTS = {
     "bf16_rounding_ties_toward_zero": ("c", [("else n = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;\n    val = n * quantum;\n    if (val >= ldexp(1.0, 128))",
                                               "else n = fl;\n    val = n * quantum;\n    if (val >= ldexp(1.0, 128))")],
                                        [FORMATS]),
+    "decode_subnormal_spacing_halved": ("c", [("v = ldexp((double)m, f.emin - f.mbits);",
+                                               "v = ldexp((double)m, f.emin - f.mbits - 1);")], [FORMATS]),
+    "bf16_subnormals_flushed": ("c", [("memcpy(&f, &u, sizeof f);\n    return f;",
+                                       "memcpy(&f, &u, sizeof f);\n    return (b & 0x7F80) == 0 ? 0.0f : f;")],
+                                [FORMATS]),
+    "nonfinite_inputs_not_reported": ("c", [("if (!isfinite(v)) bad = 1;", "if (0) bad = 1;")], [QUANT, GLUE]),
     # scale and quotient (R2, R3: s = fp32(amax / fmax), q = enc(fp32(x / s)))
     "scale_by_reciprocal_of_fmax": ("c", [("return amax / fm;", "return amax * (1.0f / fm);")], [QUANT]),
     "scale_of_zero_group_is_zero": ("c", [("if (amax == 0.0f) return 1.0f;", "if (amax == 0.0f) return 0.0f;")],
@@ -106,6 +112,8 @@ MUTANTS = {
                                              "d += (double)scale_at(sA, granA, ldsA, m, (kb + 1) % (K / 128))")], [GEMM]),
     "pertensor_gemm_drops_b_scale": ("c", [("return (double)sA[0] * (double)sB[0] * p;", "return (double)sA[0] * p;")],
                                      [GEMM]),
+    "grouped_gemm_weights_of_expert_zero": ("c", [("B + ((int64_t)g * N + n) * K", "B + ((int64_t)n) * K")],
+                                            [GEMM]),
     "grouped_gemm_expert_bound_inclusive": ("c", [("if (m >= off[e] && m < off[e + 1]) { g = e; break; }",
                                                    "if (m >= off[e] && m <= off[e + 1]) { g = e; break; }")], [GEMM]),
     "grouped_wgrad_scales_from_chunk_zero": ("c", [("sA + (r0 / 128) * N", "sA")], [GEMM]),
@@ -120,6 +128,10 @@ MUTANTS = {
                                            "s_v = av == 0.0f ? 1.0f : av / 448.0f;")], [ADAM]),
     "adam_v_encoded_as_e4m3": ("c", [("qv[blk * 128 + i] = orc_fp8_encode(vn[i] / s_v, ORC_E5M2);",
                                       "qv[blk * 128 + i] = orc_fp8_encode(vn[i] / s_v, ORC_E4M3);")], [ADAM]),
+    "adam_momentum_without_one_minus_beta": ("c", [("m = b1 * m + omb1 * gi;", "m = b1 * m + gi;")], [ADAM]),
+    "adam_update_with_wrong_sign": ("c", [("p[k] = p[k] - t;", "p[k] = p[k] + t;")], [ADAM]),
+    "adam_m_scaled_with_e5m2_max": ("c", [("s_m = am == 0.0f ? 1.0f : am / 448.0f;",
+                                           "s_m = am == 0.0f ? 1.0f : am / 57344.0f;")], [ADAM]),
     # routing, gather, SwiGLU (R8, R9)
     "route_ties_to_higher_index": ("c", [("if (best < 0 || z[e] > z[best]) best = e;",
                                           "if (best < 0 || z[e] >= z[best]) best = e;")], [GLUE]),
@@ -138,6 +150,12 @@ MUTANTS = {
     "swiglu_forward_drops_gate": ("c", [("h[r * F + j] = orc_f64_to_bf16(g * sig * u);",
                                          "h[r * F + j] = orc_f64_to_bf16(sig * u);")], [GLUE]),
     "swiglu_up_grad_drops_gate": ("c", [("orc_f64_to_bf16(d * g * sig);", "orc_f64_to_bf16(d * sig);")], [GLUE]),
+    "route_pads_with_the_last_free_tokens": ("c", [("for (t = 0; t < T && need > 0; ++t)",
+                                                    "for (t = T - 1; t >= 0 && need > 0; --t)")], [GLUE]),
+    "route_offsets_from_unpadded_counts": ("c", [("offsets[e + 1] = offsets[e] + padded[e];",
+                                                  "offsets[e + 1] = offsets[e] + counts[e];")], [GLUE]),
+    "swiglu_grad_sigmoid_sign_flipped": ("c", [("double sig = 1.0 / (1.0 + exp(-g));\n            dgu[",
+                                                "double sig = 1.0 / (1.0 + exp(g));\n            dgu[")], [GLUE]),
     # MXFP8 (R13-R16)
     "mx_untile_order_swapped": ("mx", [("t.transpose(1, 3, 2, 0, 4)", "t.transpose(1, 2, 3, 0, 4)")], [MX]),
     "mx_quotient_multiplies_by_the_scale": ("mx", [("quot = xb / np.ldexp(1.0, e)[..., None]",
@@ -148,6 +166,8 @@ MUTANTS = {
                                               "(e + E8_BIAS + 1).astype(np.uint8), OK")], [MX, MXRULE]),
     "mx_zero_block_smallest_scale": ("mx", [("e = np.where(pos, e, 0)", "e = np.where(pos, e, -E8_BIAS)")],
                                      [MX, MXRULE]),
+    "mx_exponent_clamped_one_short": ("mx", [("return np.clip(e, -E8_BIAS, E8_BIAS)", "return np.clip(e, -E8_BIAS, E8_BIAS - 1)")],
+                                      [MXRULE, MX]),
     "mx_blocks_strided_not_contiguous": ("mx", [("xb = x.reshape(R, C // MX_BLOCK, MX_BLOCK)",
                                                  "xb = x.reshape(R, MX_BLOCK, C // MX_BLOCK).transpose(0, 2, 1)")],
                                          [MX, MXRULE]),
