@@ -206,20 +206,40 @@ struct Divider2 {
 // shared by the standalone SwiGLU kernels and the quantizers that compute
 // SwiGLU while loading, so both round identically.  The 8-wide forms below
 // take 8 packed BF16 values per operand.
-// sigmoid(g) = 1 / (1 + e^-g) from the fast exponential and division: their
-// relative error (below 1e-5 for g >= -64) stays far inside half a BF16 ulp,
-// so the BF16 results are within one ulp of the correctly rounded ones.
+// sigmoid(g) = 1 / (1 + e^-g), with e^-g = 2^(-g log2 e) from the hardware
+// base-2 exponential and the reciprocal from the hardware reciprocal (PTX
+// ex2.approx.ftz.f32, rcp.approx.ftz.f32).  For g >= -64 the relative error is
+// below 1e-5: rounding the argument -g log2 e (|arg| <= 128) to binary32 moves
+// 2^arg by at most 128 * 7.3e-8 * ln 2 = 6.5e-6, and the two approximations
+// add about 2^-22 and 2^-23.  That stays far inside half a BF16 ulp, so the
+// BF16 results are within one ulp of the correctly rounded ones.  Neither
+// flush to zero changes a result there: a 2^arg below the normal range leaves
+// 1 + 2^arg == 1, and 1 + 2^arg < 2^93 keeps its reciprocal normal.
 // Below g = -64, 1 + e^g rounds to 1, so sigmoid(g) = e^g, taken from the
-// accurate exponential: e^-g itself would overflow FP32 below g = -88.7 (and
-// the fast division's range ends before that), while e^g keeps its value down
-// into the subnormals, where g * sigmoid(g) * u can still be a nonzero BF16.
-// Groups of 8 with no gate below -64 (all but extreme inputs) run without a
-// branch; the others go out of line.
+// accurate exponential: e^-g itself would overflow FP32 below g = -88.7, while
+// e^g keeps its value down into the subnormals, where g * sigmoid(g) * u can
+// still be a nonzero BF16.  Groups of 8 with no gate below -64 (all but
+// extreme inputs) run without a branch; the others go out of line.
+__device__ __forceinline__ float ex2_approx_ftz(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx_ftz(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <bool LEFT>
 __device__ __forceinline__ float swiglu_sigmoid(float g)
 {
+    constexpr float kLog2e = 1.44269504f;   // log2(e) rounded to binary32
     if (LEFT && g < -64.0f) return expf(g);
-    return __fdividef(1.0f, 1.0f + __expf(-g));
+    return rcp_approx_ftz(1.0f + ex2_approx_ftz(g * -kLog2e));
 }
 
 template <bool LEFT>
