@@ -149,9 +149,14 @@ struct Divider {
 
 // Packed form of the same division for the two BF16 values of a 32-bit word:
 // q0 = x*r, e = x - q0*s (exact), q = q0 + e*r, two lanes per instruction
-// (fma.rn.f32x2 rounds each lane like the scalar instruction).  For x = -0
-// it returns +0; callers restore the sign bit of zero quotients from x with
-// sign_bits4() on the codes.  Like the scalar form it gives NaN where x / s
+// (the f32x2 forms round each lane like the scalar instructions).  The
+// remainder is taken rounding toward minus infinity: a nonzero e is exact, so
+// its rounding mode changes nothing, and a zero x gives e = (+-0) * (-s) + x,
+// a sum of opposite zeros, which rounds to -0 in that mode.  Then for x = -0,
+// q = -0 * r + (-0) = -0, and for x = +0, q = -0 * r + (+0) = +0 (nearest):
+// every zero quotient carries the sign of x, as in the IEEE division, and the
+// FP8 conversion keeps it (-0 -> 0x80) with no sign fix-up on the codes.
+// Like the scalar form it gives NaN where x / s
 // overflows or x = +-Inf; quantizers whose scale cannot make x / s overflow
 // (scales from the group's own amax) need no check, the others redo a group
 // whose codes hold a NaN with __fdiv_rn (has_nan_code).
@@ -180,7 +185,7 @@ struct Divider2 {
         uint64_t x2, q0, e, q;
         asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "f"(xlo), "f"(xhi));
         asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(r2));
-        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(ns2), "l"(x2));
+        asm("fma.rm.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(ns2), "l"(x2));
         asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(e), "l"(r2), "l"(q0));
         asm("mov.b64 {%0, %1}, %2;" : "=f"(qlo), "=f"(qhi) : "l"(q));
     }
@@ -192,7 +197,7 @@ struct Divider2 {
             uint64_t x2, q0, e, q;
             asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "f"(xlo), "f"(xhi));
             asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(r2));
-            asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(ns2), "l"(x2));
+            asm("fma.rm.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(ns2), "l"(x2));
             asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(e), "l"(r2), "l"(q0));
             asm("mov.b64 {%0, %1}, %2;" : "=f"(qlo), "=f"(qhi) : "l"(q));
         } else {
@@ -397,8 +402,9 @@ __device__ __forceinline__ GroupScale half_warp_scales8(const uint32_t (&m)[8], 
 }
 
 // Sign bits of the 4 BF16 values in (w0 = x0,x1 ; w1 = x2,x3) placed at bit 7
-// of bytes 0..3: OR-ed into the 4 codes this restores -0 -> 0x80 (every other
-// code already carries the sign of its value).
+// of bytes 0..3: OR-ed into the 4 codes of the out-of-line IEEE paths, this
+// sets the sign of every code from its value (the packed fast paths need no
+// fix-up: their zero quotients already carry the sign).
 __device__ __forceinline__ uint32_t sign_bits4(uint32_t w0, uint32_t w1)
 {
     return __byte_perm(w0, w1, 0x7531) & 0x80808080u;
@@ -437,7 +443,7 @@ __device__ __forceinline__ uint32_t quant4p_fast(uint32_t w0, uint32_t w1, const
     float a, b, c, e;
     d.fast_div(w0, a, b);
     d.fast_div(w1, c, e);
-    return (cvt2<FMT>(a, b) | (cvt2<FMT>(c, e) << 16)) | sign_bits4(w0, w1);
+    return cvt2<FMT>(a, b) | (cvt2<FMT>(c, e) << 16);
 }
 
 template <int FMT>

@@ -95,8 +95,8 @@ __device__ __forceinline__ uint2 quant8_mon(uint4 v, const Divider2 &d, Counts &
         for (int e = 0; e < 8; ++e) qv[e] = r.q[e];
     }
     uint2 out;
-    out.x = (cvt2<FMT>(qv[0], qv[1]) | (cvt2<FMT>(qv[2], qv[3]) << 16)) | sign_bits4(v.x, v.y);
-    out.y = (cvt2<FMT>(qv[4], qv[5]) | (cvt2<FMT>(qv[6], qv[7]) << 16)) | sign_bits4(v.z, v.w);
+    out.x = cvt2<FMT>(qv[0], qv[1]) | (cvt2<FMT>(qv[2], qv[3]) << 16);
+    out.y = cvt2<FMT>(qv[4], qv[5]) | (cvt2<FMT>(qv[6], qv[7]) << 16);
     if (has_nan_code<FMT>(out.x) || has_nan_code<FMT>(out.y)) {
         // x NaN, x = +-Inf, or x / s overflowed in the fast division (the
         // scale comes from earlier steps): the IEEE quotients decide

@@ -104,7 +104,7 @@ __device__ __forceinline__ uint32_t quant_pair_cols_fast(uint32_t w, const ColDi
     uint64_t x2, q0, e, qq;
     asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "f"(xlo), "f"(xhi));
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(c.r2));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(c.ns2), "l"(x2));
+    asm("fma.rm.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(c.ns2), "l"(x2));
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(qq) : "l"(e), "l"(c.r2), "l"(q0));
     asm("mov.b64 {%0, %1}, %2;" : "=f"(qlo), "=f"(qhi) : "l"(qq));
     return cvt2<FMT>(qlo, qhi);
@@ -287,8 +287,7 @@ __global__ void __launch_bounds__(256, fused_ctas_per_sm<SRC>()) k_quant_1x128_f
             if (cfast) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    rw[i] = (quant_pair_cols_fast<FMT>(pr[i].x, d01) | (quant_pair_cols_fast<FMT>(pr[i].y, d23) << 16)) |
-                            sign_bits4(pr[i].x, pr[i].y);
+                    rw[i] = quant_pair_cols_fast<FMT>(pr[i].x, d01) | (quant_pair_cols_fast<FMT>(pr[i].y, d23) << 16);
             } else {
                 const uint4 c = quant_cols4x4_slow<FMT>(make_uint4(pr[0].x, pr[1].x, pr[2].x, pr[3].x),
                                                         make_uint4(pr[0].y, pr[1].y, pr[2].y, pr[3].y), d01.s0,
