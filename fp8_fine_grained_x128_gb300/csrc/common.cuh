@@ -189,6 +189,16 @@ struct Divider2 {
         asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(e), "l"(r2), "l"(q0));
         asm("mov.b64 {%0, %1}, %2;" : "=f"(qlo), "=f"(qhi) : "l"(q));
     }
+    // the same for two binary32 dividends
+    __device__ __forceinline__ void fast_div_f32(float xlo, float xhi, float &qlo, float &qhi) const
+    {
+        uint64_t x2, q0, e, q;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "f"(xlo), "f"(xhi));
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(r2));
+        asm("fma.rm.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(ns2), "l"(x2));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(e), "l"(r2), "l"(q0));
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(qlo), "=f"(qhi) : "l"(q));
+    }
     // quotients of (lo, hi) BF16 halves of w
     __device__ __forceinline__ void operator()(uint32_t w, float &qlo, float &qhi) const
     {

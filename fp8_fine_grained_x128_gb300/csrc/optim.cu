@@ -42,10 +42,24 @@ __device__ __forceinline__ void fp8x4_to_f32(uint32_t w, float (&f)[4])
     f[3] = __half2float(__ushort_as_half((unsigned short)(h23 >> 16)));
 }
 
+// Codes of 4 binary32 values with the block scale s (q = enc(x / s)).  The
+// scale comes from the block's own amax, so no |x / s| exceeds fmax by more
+// than a rounding and no quotient overflows; inside the fast range of s the
+// packed Markstein quotients are the correctly rounded ones wherever they can
+// decide a code, and they carry the sign of x even when zero.  A scale outside
+// that range (an all-tiny block: one per warp, so the branch is uniform) takes
+// the IEEE division.
 template <int FMT>
-__device__ __forceinline__ uint32_t f32x4_to_fp8(const float (&x)[4], const Divider &d)
+__device__ __forceinline__ uint32_t f32x4_to_fp8(const float (&x)[4], const Divider2 &d)
 {
-    return cvt2<FMT>(d(x[0]), d(x[1])) | (cvt2<FMT>(d(x[2]), d(x[3])) << 16);
+    if (d.fast) {
+        float q[4];
+        d.fast_div_f32(x[0], x[1], q[0], q[1]);
+        d.fast_div_f32(x[2], x[3], q[2], q[3]);
+        return cvt2<FMT>(q[0], q[1]) | (cvt2<FMT>(q[2], q[3]) << 16);
+    }
+    return cvt2<FMT>(__fdiv_rn(x[0], d.s), __fdiv_rn(x[1], d.s)) |
+           (cvt2<FMT>(__fdiv_rn(x[2], d.s), __fdiv_rn(x[3], d.s)) << 16);
 }
 
 __device__ __forceinline__ float warp_max(float v)
@@ -121,8 +135,8 @@ __global__ void __launch_bounds__(256) k_adamw_fp8(float *__restrict__ p, const 
         const float nsv = av == 0.0f ? 1.0f : __fdiv_rn(av, 57344.0f);
         if (dbg_span(k, 4, nblk * 128, status)) {
             __stcs(reinterpret_cast<float4 *>(p + k), make_float4(pp[0], pp[1], pp[2], pp[3]));
-            *reinterpret_cast<uint32_t *>(qm + k) = f32x4_to_fp8<FP8_E4M3>(m, Divider(nsm));
-            *reinterpret_cast<uint32_t *>(qv + k) = f32x4_to_fp8<FP8_E5M2>(v, Divider(nsv));
+            *reinterpret_cast<uint32_t *>(qm + k) = f32x4_to_fp8<FP8_E4M3>(m, Divider2(nsm));
+            *reinterpret_cast<uint32_t *>(qv + k) = f32x4_to_fp8<FP8_E5M2>(v, Divider2(nsv));
         }
         if (lane == 0 && dbg_span(b, 1, nblk, status)) {
             sm[b] = nsm;
