@@ -122,44 +122,21 @@ __host__ __device__ __forceinline__ bool fast_div_scale(float s)
 // e = x - q0*s is exact under FMA and RN(q0 + e*r) is the correctly rounded
 // quotient.  Valid while s and 1/s are normal, e does not underflow and
 // nothing overflows; callers use it only when fast_div_scale(s) and fall back
-// to __fdiv_rn otherwise.
-// A quotient that overflows (or x = +-Inf) turns q0 into +-Inf and q into NaN:
-// such a NaN from a non-NaN x is redone by __fdiv_rn.
-// The sign is forced from x so that -0 / s = -0 like the IEEE division.
-struct Divider {
-    float s, r;
-    bool fast;
-    __device__ __forceinline__ explicit Divider(float s_) : s(s_)
-    {
-        fast = fast_div_scale(s_);
-        r = fast ? __frcp_rn(s_) : 0.0f;
-    }
-    __device__ __forceinline__ float operator()(float x) const
-    {
-        if (fast) {
-            float q0 = __fmul_rn(x, r);
-            float e = __fmaf_rn(-q0, s, x);
-            float q = __fmaf_rn(e, r, q0);
-            if (q != q) return __fdiv_rn(x, s);
-            return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
-        }
-        return __fdiv_rn(x, s);
-    }
-};
-
-// Packed form of the same division for the two BF16 values of a 32-bit word:
-// q0 = x*r, e = x - q0*s (exact), q = q0 + e*r, two lanes per instruction
-// (the f32x2 forms round each lane like the scalar instructions).  The
-// remainder is taken rounding toward minus infinity: a nonzero e is exact, so
-// its rounding mode changes nothing, and a zero x gives e = (+-0) * (-s) + x,
-// a sum of opposite zeros, which rounds to -0 in that mode.  Then for x = -0,
-// q = -0 * r + (-0) = -0, and for x = +0, q = -0 * r + (+0) = +0 (nearest):
-// every zero quotient carries the sign of x, as in the IEEE division, and the
-// FP8 conversion keeps it (-0 -> 0x80) with no sign fix-up on the codes.
-// Like the scalar form it gives NaN where x / s
-// overflows or x = +-Inf; quantizers whose scale cannot make x / s overflow
-// (scales from the group's own amax) need no check, the others redo a group
-// whose codes hold a NaN with __fdiv_rn (has_nan_code).
+// to __fdiv_rn otherwise.  A quotient that overflows (or x = +-Inf) turns q0
+// into +-Inf and q into NaN.
+//
+// Packed form for two dividends (the BF16 halves of a 32-bit word, or two
+// binary32 values): q0 = x*r, e = x - q0*s (exact), q = q0 + e*r, two lanes
+// per instruction (the f32x2 forms round each lane like the scalar
+// instructions).  The remainder is taken rounding toward minus infinity: a
+// nonzero e is exact, so its rounding mode changes nothing, and a zero x gives
+// e = (+-0) * (-s) + x, a sum of opposite zeros, which rounds to -0 in that
+// mode.  Then for x = -0, q = -0 * r + (-0) = -0, and for x = +0,
+// q = -0 * r + (+0) = +0 (nearest): every zero quotient carries the sign of x,
+// as in the IEEE division, and the FP8 conversion keeps it (-0 -> 0x80) with
+// no sign fix-up on the codes.  Quantizers whose scale cannot make x / s
+// overflow (scales from the group's own amax) need no NaN check; the others
+// redo a group whose codes hold a NaN with __fdiv_rn (has_nan_code).
 struct Divider2 {
     uint64_t r2, ns2;
     float s;
